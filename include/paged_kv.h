@@ -1,0 +1,170 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 (sm_103a) paged KV cache library.
+ *
+ * Two operations make up the decode-step hot path of PagedAttention:
+ *
+ *   paged_kv_write          the reshape_and_cache scatter: each new token's key and
+ *                           value rows go into the physical slot that slot_mapping
+ *                           names.
+ *   paged_attention_decode  decode-phase attention of one query token per sequence
+ *                           over that sequence's cached tokens, found through its
+ *                           block table.
+ *
+ * Conventions shared by every call:
+ *   - Every array pointer is a DEVICE pointer owned by the caller. The library
+ *     allocates nothing and keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and never
+ *     synchronise, except paged_kv_device_errors.
+ *   - Arguments are validated on the host before any CUDA call. A rejected call
+ *     launches nothing and returns a negative pkv_status_t;
+ *     pkv_last_error_message() then describes the problem.
+ *   - Kernels check every block-table entry, slot and context length they read.
+ *     A bad one is skipped or clamped (never dereferenced), and a bit is set in
+ *     a per-device error word that paged_kv_device_errors reads.
+ *   - fp16 and bf16 are supported. Query, caches and output share one dtype.
+ *
+ * KV pool layout (both key_cache and value_cache):
+ *     [num_blocks][num_kv_heads][block_size][head_dim], row-major,
+ * so the block_size x head_dim tile of one (physical block, kv head) is one
+ * contiguous run of block_size * head_dim * 2 bytes. Token j of a sequence lives
+ * in physical block block_tables[s][j / block_size] at offset j % block_size.
+ * The pages fix the block / block table / slot vocabulary but not the byte
+ * layout; it is chosen so a whole tile moves with one bulk copy.
+ */
+#ifndef PAGED_KV_H_
+#define PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1, /* a null pointer, a negative size, inconsistent shapes */
+  PKV_ERR_UNSUPPORTED = -2, /* valid, but outside what the kernels are built for    */
+  PKV_ERR_WORKSPACE = -3,   /* split-K workspace missing, too small or misaligned   */
+  PKV_ERR_CUDA = -4,        /* a CUDA runtime call or a kernel launch failed        */
+  PKV_ERR_DEVICE_CHECK = -5 /* paged_kv_device_errors found a device-side error bit */
+} pkv_status_t;
+
+/* Bits of the per-device error word (see paged_kv_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 1u /* a block-table entry outside [0, num_blocks)            */
+#define PKV_DEVERR_CONTEXT 2u  /* a context length < 0 or above max_context_len or
+                                  max_blocks_per_seq * block_size (clamped)               */
+#define PKV_DEVERR_SLOT 4u     /* a slot_mapping entry >= num_blocks * block_size        */
+#define PKV_DEVERR_TIMEOUT 8u  /* a wait for a bulk copy gave up after its time limit   */
+
+/*
+ * paged_kv_write -- store the step's new keys and values in the paged pool.
+ *
+ * Source: "[vLLM] PagedAttention: OS 페이징 기법으로 KV 캐시를 관리하는 방법",
+ * section "PagedAttention 커널" (write_to_paged_cache -> ops.reshape_and_cache with
+ * slot_mapping); slot arithmetic as in "KV Cache와 PagedAttention 완전 해부",
+ * §5단계 and §6단계 (the 7th token of a request whose block is 42 goes to slot 6).
+ *
+ * For every token t with slot = slot_mapping[t] >= 0 and every kv head h:
+ *     key_cache  [slot / block_size][h][slot % block_size][:] = key  [t][h][:]
+ *     value_cache[slot / block_size][h][slot % block_size][:] = value[t][h][:]
+ * as a bit copy. Tokens with a negative slot are padding and are skipped.
+ *
+ *   key, value          [num_tokens][num_kv_heads][head_dim], contiguous
+ *   key_cache, value_cache  the pool, layout above; 16-byte aligned
+ *   slot_mapping        [num_tokens] int64
+ *   head_dim            64 or 128; block_size 8, 16 or 32
+ *
+ * Two tokens naming the same slot give an undefined winner. A slot at or past
+ * num_blocks * block_size is skipped and sets PKV_DEVERR_SLOT.
+ * num_tokens == 0 is a no-op that returns PKV_OK.
+ */
+pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
+                            void* value_cache, const int64_t* slot_mapping, int32_t num_tokens,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, pkv_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * paged_attention_workspace_size -- bytes of device workspace that
+ * paged_attention_decode needs for its split-K partial results.
+ *
+ * Contexts longer than partition_size tokens (0 selects the default, 512) are
+ * split into ceil(context_len / partition_size) partitions. Each partition keeps
+ * its running max m, its sum of exponentials l and its normalised output
+ * (fp32), and a separate reduce kernel merges them by log-sum-exp. Returns 0
+ * when max_context_len <= partition_size (no split; no workspace needed) and
+ * also for invalid arguments, which paged_attention_decode then rejects.
+ */
+size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                      int32_t max_context_len, int32_t partition_size);
+
+/*
+ * paged_attention_decode -- one decode step of attention over the paged pool.
+ *
+ * Source: "KV Cache와 PagedAttention 완전 해부", 부록 (softmax(Q K^T / sqrt d) V,
+ * computed block by block through the block table with a running softmax) and
+ * §6단계 (decode is matrix-vector and memory-bound); "vLLM: LLM 서빙 메모리 최적화의
+ * 교과서", 01 Problem Definition (a_ij, o_i) and eq. (4) (the block-wise form, equal
+ * to ordinary attention); "Sparse Computation and Memory Management for Efficient
+ * LLM Inference", Block-level Attention Formulation.
+ *
+ * For every sequence s, query head h, kv head g = h / (num_heads / num_kv_heads)
+ * and the first n = context_lens[s] cached tokens:
+ *     x_j = scale * dot(query[s][h][:], K_j)        j = 0 .. n-1
+ *     out[s][h][:] = sum_j softmax(x)_j * V_j
+ * where K_j, V_j are row j % block_size of the (block_tables[s][j / block_size], g)
+ * tile. n == 0 gives zeros. Accumulation is fp32; out is rounded to nearest-even
+ * into the query dtype.
+ *
+ *   out, query           [num_seqs][num_heads][head_dim], contiguous, 16-byte aligned
+ *   key_cache, value_cache  the pool, layout above; 16-byte aligned
+ *   block_tables         [num_seqs][max_blocks_per_seq] int32; entries at or past
+ *                        ceil(n / block_size) are never read
+ *   context_lens         [num_seqs] int32
+ *   max_context_len      host-side upper bound on every context_lens entry; sizes
+ *                        the launch (longer contexts are clamped, PKV_DEVERR_CONTEXT)
+ *   scale                usually 1 / sqrt(head_dim)
+ *   head_dim             64 or 128; block_size 8, 16 or 32
+ *   num_heads            a multiple of num_kv_heads (GQA when larger)
+ *   partition_size       0 = 512; else a multiple of block_size in
+ *                        [block_size, 128 * block_size]
+ *   workspace            paged_attention_workspace_size(...) bytes, 16-byte aligned;
+ *                        may be NULL when that size is 0
+ *
+ * Rows of out for every (s, h) are written by this call. The workspace is
+ * scratch: its contents need no initialisation and are not meaningful after the
+ * call. Concurrent calls must not share a workspace.
+ */
+pkv_status_t paged_attention_decode(void* out, const void* query, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    int32_t num_seqs, int32_t max_context_len, float scale,
+                                    int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                    int32_t partition_size, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * paged_kv_device_errors -- read the current device's error word (PKV_DEVERR_* bits
+ * set by kernels since it was last cleared) into *flags, and clear it if `clear`
+ * is non-zero. Synchronises the current device first. Returns PKV_OK, or
+ * PKV_ERR_CUDA if a CUDA call fails. The library sets *flags; callers compare
+ * against 0.
+ */
+pkv_status_t paged_kv_device_errors(uint32_t* flags, int32_t clear);
+
+/* Static string naming a status code. */
+const char* pkv_status_string(pkv_status_t status);
+
+/* Description of the last failed call on the calling thread ("" if none). */
+const char* pkv_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H_ */

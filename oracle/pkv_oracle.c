@@ -1,0 +1,193 @@
+/*
+ * CPU oracle for the paged KV cache hot path, plain C, fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the bench's
+ * CPU-baseline leg load this library; the CUDA library never calls it and
+ * shares no code, header or table with it.
+ *
+ * Two operations, each the plain definition written out:
+ *
+ *   oracle_write   -- the reshape_and_cache scatter: each new token's key and
+ *                     value rows are copied, bit for bit, into the slot that
+ *                     slot_mapping names (block = slot / B, offset = slot % B).
+ *                     "[vLLM] PagedAttention: OS 페이징 기법으로 KV 캐시를 관리하는
+ *                     방법", PagedAttention 커널 (write_to_paged_cache ->
+ *                     ops.reshape_and_cache); slot arithmetic as in "KV Cache와
+ *                     PagedAttention 완전 해부", §5단계 and §6단계 (block 42,
+ *                     slots 0..5, next token into slot 6).
+ *
+ *   oracle_decode  -- decode attention of one query token per sequence over its
+ *                     first context_lens[s] cached tokens. The cached K and V
+ *                     rows are first gathered through the block table into
+ *                     contiguous fp64 arrays, then
+ *                         x_j = scale * sum_d q[d] * K[j][d]
+ *                         w_j = exp(x_j - max x) / sum_i exp(x_i - max x)
+ *                         o[d] = sum_j w_j * V[j][d]
+ *                     "KV Cache와 PagedAttention 완전 해부", 부록 (Attention =
+ *                     softmax(Q K^T / sqrt d) V); "vLLM: LLM 서빙 메모리 최적화의
+ *                     교과서", 01 Problem Definition (a_ij, o_i) and eq. (4),
+ *                     whose block-wise form gives the same o_i. Subtracting
+ *                     max x leaves w unchanged (it cancels in the ratio).
+ *                     Query head h reads kv head h / (H / Hkv) (contiguous
+ *                     GQA groups). A context of 0 tokens gives o = 0.
+ *
+ * fp16/bf16 inputs are widened to double exactly from their bit patterns.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+static double widen_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x400), e - 25); /* (1024 + m) * 2^(e - 15 - 10) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double widen_bf16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double widen(uint16_t bits, int dtype) {
+    return dtype == 0 ? widen_f16(bits) : widen_bf16(bits);
+}
+
+double oracle_widen(uint16_t bits, int dtype) { return widen(bits, dtype); }
+
+/*
+ * Returns the number of tokens written, or -(t + 1) for the first token t
+ * whose slot lies outside the pool (nothing is written for that token).
+ */
+long long oracle_write(const uint16_t* key, const uint16_t* value, uint16_t* key_cache,
+                       uint16_t* value_cache, const int64_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size, long long num_blocks) {
+    long long written = 0, bad = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue; /* padding token */
+        if (slot >= (int64_t)num_blocks * block_size) {
+            if (!bad) bad = -(long long)(t + 1);
+            continue;
+        }
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
+            memcpy(key_cache + dst, key + src, sizeof(uint16_t) * head_dim);
+            memcpy(value_cache + dst, value + src, sizeof(uint16_t) * head_dim);
+        }
+        ++written;
+    }
+    return bad ? bad : written;
+}
+
+/* One (sequence, query head) pair. Returns 0, or -1 on a block id outside the pool. */
+static int decode_pair(double* out, const uint16_t* query, const uint16_t* key_cache,
+                       const uint16_t* value_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, double scale,
+                       int block_size, int num_heads, int num_kv_heads, int head_dim,
+                       long long num_blocks, int dtype, int s, int h) {
+    const int D = head_dim, B = block_size;
+    double* o = out + ((size_t)s * num_heads + h) * D;
+    int ctx = context_lens[s];
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (ctx <= 0) return 0;
+    const int group = num_heads / num_kv_heads;
+    const int g = h / group;
+
+    /* gather the sequence's K and V rows into contiguous arrays */
+    double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+    double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+    double* x = (double*)malloc(sizeof(double) * (size_t)ctx);
+    double* q = (double*)malloc(sizeof(double) * (size_t)D);
+    int rc = 0;
+    for (int j = 0; j < ctx && !rc; ++j) {
+        long long phys = block_tables[(size_t)s * max_blocks_per_seq + j / B];
+        if (phys < 0 || phys >= num_blocks) { rc = -1; break; }
+        size_t base = (((size_t)phys * num_kv_heads + g) * B + (j % B)) * D;
+        for (int d = 0; d < D; ++d) {
+            K[(size_t)j * D + d] = widen(key_cache[base + d], dtype);
+            V[(size_t)j * D + d] = widen(value_cache[base + d], dtype);
+        }
+    }
+    if (!rc) {
+        for (int d = 0; d < D; ++d) q[d] = widen(query[((size_t)s * num_heads + h) * D + d], dtype);
+        /* scores */
+        double mx = -INFINITY;
+        for (int j = 0; j < ctx; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += q[d] * K[(size_t)j * D + d];
+            x[j] = scale * acc;
+            if (x[j] > mx) mx = x[j];
+        }
+        /* softmax weights */
+        double den = 0.0;
+        for (int j = 0; j < ctx; ++j) {
+            x[j] = exp(x[j] - mx);
+            den += x[j];
+        }
+        /* weighted sum of values */
+        for (int j = 0; j < ctx; ++j) {
+            double w = x[j] / den;
+            for (int d = 0; d < D; ++d) o[d] += w * V[(size_t)j * D + d];
+        }
+    }
+    free(K);
+    free(V);
+    free(x);
+    free(q);
+    return rc;
+}
+
+/*
+ * out: [S][H][D] doubles (only the selected pairs are written).
+ * pairs: NULL for every (s, h), else npairs (s, h) int32 pairs.
+ * num_threads: <= 0 uses the OpenMP default. Returns 0, or -1 if any block id
+ * lies outside the pool.
+ */
+int oracle_decode(double* out, const uint16_t* query, const uint16_t* key_cache,
+                  const uint16_t* value_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int num_seqs, double scale, int block_size,
+                  int num_heads, int num_kv_heads, int head_dim, long long num_blocks, int dtype,
+                  const int32_t* pairs, long long npairs, int num_threads) {
+    long long n = pairs ? npairs : (long long)num_seqs * num_heads;
+    int rc = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc)
+#endif
+    for (long long i = 0; i < n; ++i) {
+        int s = pairs ? pairs[2 * i] : (int)(i / num_heads);
+        int h = pairs ? pairs[2 * i + 1] : (int)(i % num_heads);
+        rc |= decode_pair(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                          context_lens, scale, block_size, num_heads, num_kv_heads, head_dim,
+                          num_blocks, dtype, s, h);
+    }
+    return rc ? -1 : 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,159 @@
+"""ctypes binding of libpaged_kv.so (C ABI: include/paged_kv.h).
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes the call's stream, and a non-zero status becomes
+a PagedKVError. Every step of the computation runs in the library's kernels;
+there is no fallback of any kind, so a missing library raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
+
+PKV_F16, PKV_BF16 = 0, 1
+_DTYPE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT"}
+
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__(message)
+
+
+def load():
+    """Load the library (once). Raises PagedKVError if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise PagedKVError(None, f"{LIB_PATH} is missing: build it with "
+                                 "`python -m paged_kv_cache_91_gb300.build` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.paged_kv_write.restype = i32
+    lib.paged_kv_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+    lib.paged_attention_workspace_size.restype = sz
+    lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.paged_attention_decode.restype = i32
+    lib.paged_attention_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
+                                           i32, P, sz, P]
+    lib.paged_kv_device_errors.restype = i32
+    lib.paged_kv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [i32]
+    lib.pkv_last_error_message.restype = ctypes.c_char_p
+    lib.pkv_last_error_message.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(lib, status: int) -> None:
+    if status != 0:
+        name = lib.pkv_status_string(status).decode()
+        msg = lib.pkv_last_error_message().decode()
+        raise PagedKVError(status, f"{name}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda16(name: str, t: torch.Tensor) -> int:
+    if not t.is_cuda:
+        raise PagedKVError(-1, f"{name} must be a CUDA tensor")
+    if t.dtype not in _DTYPE:
+        raise PagedKVError(-1, f"{name} must be float16 or bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise PagedKVError(-1, f"{name} must be contiguous")
+    return _DTYPE[t.dtype]
+
+
+def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                   slot_mapping: torch.Tensor, stream=None) -> None:
+    """Scatter key/value [T][Hkv][D] into the pool [NB][Hkv][B][D] at slot_mapping [T] (int64)."""
+    lib = load()
+    dt = _cuda16("key_cache", key_cache)
+    for n, t in (("key", key), ("value", value), ("value_cache", value_cache)):
+        if _cuda16(n, t) != dt:
+            raise PagedKVError(-1, f"{n} dtype differs from key_cache")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise PagedKVError(-1, "slot_mapping must be a contiguous CUDA int64 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    T = slot_mapping.numel()
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D) or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between key/value, caches and slot_mapping")
+    _check(lib, lib.paged_kv_write(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping),
+                                   T, Hkv, D, B, NB, dt, _stream(key_cache, stream)))
+
+
+def paged_attention_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                                   partition_size: int = 0) -> int:
+    return int(load().paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                                                     partition_size))
+
+
+def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           scale: float, block_size: Optional[int] = None, num_kv_heads: Optional[int] = None,
+                           max_context_len: Optional[int] = None, partition_size: int = 0,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention: out[s][h] = softmax(scale q.K^T) V over the first context_lens[s] tokens.
+
+    ``max_context_len`` bounds every context length on the host; when omitted it
+    is max_blocks_per_seq * block_size (always safe, possibly more partitions).
+    ``workspace`` (uint8, >= paged_attention_workspace_size bytes) is allocated
+    here through torch when omitted and a split is needed.
+    """
+    lib = load()
+    dt = _cuda16("query", query)
+    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
+        if _cuda16(n, t) != dt:
+            raise PagedKVError(-1, f"{n} dtype differs from query")
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    if block_size is not None and block_size != B:
+        raise PagedKVError(-1, f"block_size {block_size} != key_cache.shape[2] {B}")
+    if num_kv_heads is not None and num_kv_heads != Hkv:
+        raise PagedKVError(-1, f"num_kv_heads {num_kv_heads} != key_cache.shape[1] {Hkv}")
+    S, H, D2 = query.shape
+    if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between query, out and caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise PagedKVError(-1, "block_tables must be [S][max_blocks] and context_lens [S]")
+    maxb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxb * B
+    need = int(lib.paged_attention_workspace_size(S, H, D, max_context_len, partition_size))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib, lib.paged_attention_decode(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
+        _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt, int(partition_size),
+        _ptr(workspace), wbytes, _stream(query, stream)))
+    return out
+
+
+def device_errors(clear: bool = True) -> int:
+    """The current device's error word (PKV_DEVERR_* bits); synchronises the device."""
+    lib = load()
+    v = ctypes.c_uint32(0)
+    _check(lib, lib.paged_kv_device_errors(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)

@@ -1,0 +1,353 @@
+"""Seeded synthetic decode batches for the paged KV cache.
+
+This module only builds inputs: context lengths, a physical block pool filled
+with N(0,1) keys and values, per-sequence block tables popped from a shuffled
+free list, the decode queries, and the one new token per sequence that the
+cache write stores. It holds none of the attention arithmetic; both the CUDA
+path and the CPU oracle consume what it returns.
+
+Shapes follow the pages' vocabulary ("KV Cache와 PagedAttention 완전 해부",
+§5단계; "Sparse Computation and Memory Management ...", Block-level Attention
+Formulation):
+
+  query        [S][H][D]            16-bit bit patterns (uint16)
+  key_cache    [NB][Hkv][B][D]      one contiguous B*D tile per (block, kv head)
+  value_cache  [NB][Hkv][B][D]
+  block_tables [S][max_blocks]      int32, logical block -> physical block, -1 past the end
+  context_lens [S]                  int32, tokens attended by each sequence
+  slot_mapping [T]                  int64, physical slot = block * B + offset, -1 = skip
+
+Every slot of the pool that no sequence's context covers holds a NaN canary,
+so any read past a context or into a free block shows up in the output.
+
+Values are drawn in float32 from numpy's PCG64 and rounded to nearest-even to
+fp16 or bf16. Large pools are drawn in fixed chunks of CHUNK_BLOCKS blocks,
+each chunk seeded by (seed, stream, chunk index), so the result does not depend
+on the number of threads used.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F16 = "f16"
+BF16 = "bf16"
+DTYPES = (F16, BF16)
+
+# NaN canaries (quiet NaN with a payload) written into every unused slot.
+CANARY = {F16: np.uint16(0x7E5A), BF16: np.uint16(0x7FDA)}
+
+CHUNK_BLOCKS = 64  # pool blocks per independently seeded chunk (fixed: part of the recipe)
+
+# seed streams
+_S_META, _S_QUERY, _S_KEY, _S_VALUE, _S_OUTLIER = 0, 1, 2, 3, 4
+
+
+def round_f32_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float32 values to nearest-even fp16/bf16; return the uint16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == F16:
+        return x.astype(np.float16).view(np.uint16)
+    if dtype == BF16:
+        u = x.view(np.uint32)
+        r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+        return r.astype(np.uint16)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of fp16/bf16 bit patterns to float32 (used only to build inputs)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == F16:
+        return bits.view(np.float16).astype(np.float32)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class DecodeBatch:
+    """One decode step's inputs for one attention layer."""
+
+    name: str
+    dtype: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    scale: float
+    query: np.ndarray
+    key_cache: np.ndarray
+    value_cache: np.ndarray
+    block_tables: np.ndarray
+    context_lens: np.ndarray
+    slot_mapping: np.ndarray
+    new_key: np.ndarray
+    new_value: np.ndarray
+    partition_size: int = 512
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.key_cache.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2
+
+    def new_token_slots(self) -> np.ndarray:
+        """Physical (block, offset) pairs the step's new tokens are written to ([T, 2])."""
+        s = self.slot_mapping
+        keep = s >= 0
+        return np.stack([s[keep] // self.block_size, s[keep] % self.block_size], axis=1)
+
+    def pool_before_write(self):
+        """Copies of the pools with the new tokens' slots reset to the canary."""
+        kc = self.key_cache.copy()
+        vc = self.value_cache.copy()
+        slots = self.new_token_slots()
+        kc[slots[:, 0], :, slots[:, 1], :] = CANARY[self.dtype]
+        vc[slots[:, 0], :, slots[:, 1], :] = CANARY[self.dtype]
+        return kc, vc
+
+
+# ----------------------------------------------------------------------------
+# pool construction
+
+
+def _fill_pool(seed: int, stream: int, shape, dtype: str, outlier_frac: float,
+               outlier_scale: float, threads: int) -> np.ndarray:
+    nb = shape[0]
+    out = np.empty(shape, dtype=np.uint16)
+    nchunks = (nb + CHUNK_BLOCKS - 1) // CHUNK_BLOCKS
+
+    def work(ci: int) -> None:
+        b0 = ci * CHUNK_BLOCKS
+        b1 = min(nb, b0 + CHUNK_BLOCKS)
+        rng = np.random.default_rng([seed, stream, ci])
+        x = rng.standard_normal((b1 - b0,) + tuple(shape[1:]), dtype=np.float32)
+        if outlier_frac > 0.0:
+            mrng = np.random.default_rng([seed, _S_OUTLIER, ci])
+            mask = mrng.random((b1 - b0,) + tuple(shape[1:3])) < outlier_frac
+            x[mask] *= np.float32(outlier_scale)
+        out[b0:b1] = round_f32_to(x, dtype)
+
+    if nchunks <= 1 or threads <= 1:
+        for ci in range(nchunks):
+            work(ci)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
+                head_dim: int, block_size: int, dtype: str, num_blocks: int | None = None,
+                pool_factor: float = 1.0, shared_prefix_tokens: int = 0,
+                key_outlier_frac: float = 0.0, key_outlier_scale: float = 8.0,
+                partition_size: int = 512, name: str = "custom",
+                threads: int | None = None) -> DecodeBatch:
+    """Build a seeded decode batch.
+
+    Physical blocks come from a free list that is a seeded permutation of the
+    pool; each sequence pops its blocks in logical order, the way blocks are
+    handed out on demand ("Sparse Computation and Memory Management ...",
+    Memory Allocation Pseudocode). With ``shared_prefix_tokens`` > 0 every
+    sequence's first blocks point at the same physical blocks ("KV Cache와
+    PagedAttention 완전 해부", §9단계 Prefix Caching).
+
+    The step's new token of sequence s is its last context position ctx_s - 1;
+    its K/V are already in the pool, and ``new_key``/``new_value`` hold a copy
+    so a test can clear the slot and have the cache write restore it.
+    """
+    if dtype not in DTYPES:
+        raise ValueError(dtype)
+    if num_heads % num_kv_heads:
+        raise ValueError("num_heads must be a multiple of num_kv_heads")
+    B = block_size
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    S = int(ctx.shape[0])
+    if (ctx < 0).any():
+        raise ValueError("negative context length")
+    if shared_prefix_tokens % B:
+        raise ValueError("shared prefix must be block aligned")
+    prefix_blocks = shared_prefix_tokens // B
+    if shared_prefix_tokens and (ctx <= shared_prefix_tokens).any():
+        raise ValueError("each sequence needs a private tail after the shared prefix")
+    nblk = (ctx + B - 1) // B
+    private = nblk - prefix_blocks if prefix_blocks else nblk
+    needed = int(prefix_blocks + private.sum())
+    if num_blocks is None:
+        num_blocks = max(1, int(math.ceil(pool_factor * needed)))
+    if num_blocks < needed:
+        raise ValueError(f"pool of {num_blocks} blocks < {needed} needed")
+    meta_rng = np.random.default_rng([seed, _S_META])
+    free_list = meta_rng.permutation(num_blocks).astype(np.int64)
+    max_blocks = max(1, int(nblk.max()) if S else 1)
+    tables = np.full((S, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    prefix = free_list[pos:pos + prefix_blocks]
+    pos += prefix_blocks
+    for s in range(S):
+        tables[s, :prefix_blocks] = prefix
+        n = int(private[s])
+        tables[s, prefix_blocks:prefix_blocks + n] = free_list[pos:pos + n]
+        pos += n
+
+    H, Hkv, D = num_heads, num_kv_heads, head_dim
+    qrng = np.random.default_rng([seed, _S_QUERY])
+    query = round_f32_to(qrng.standard_normal((S, H, D), dtype=np.float32), dtype)
+
+    threads = threads or max(1, min(32, os.cpu_count() or 1))
+    shape = (num_blocks, Hkv, B, D)
+    kc = _fill_pool(seed, _S_KEY, shape, dtype, key_outlier_frac, key_outlier_scale, threads)
+    vc = _fill_pool(seed, _S_VALUE, shape, dtype, 0.0, 1.0, threads)
+
+    # canary every slot no context covers
+    used = np.zeros((num_blocks, B), dtype=bool)
+    for s in range(S):
+        c = int(ctx[s])
+        for j in range(int(nblk[s])):
+            used[tables[s, j], :min(B, c - j * B)] = True
+    bi, oi = np.nonzero(~used)
+    kc[bi, :, oi, :] = CANARY[dtype]
+    vc[bi, :, oi, :] = CANARY[dtype]
+
+    slot_mapping = np.full(S, -1, dtype=np.int64)
+    new_key = np.zeros((S, Hkv, D), dtype=np.uint16)
+    new_value = np.zeros((S, Hkv, D), dtype=np.uint16)
+    for s in range(S):
+        c = int(ctx[s])
+        if c == 0:
+            continue
+        phys = int(tables[s, (c - 1) // B])
+        off = (c - 1) % B
+        slot_mapping[s] = phys * B + off
+        new_key[s] = kc[phys, :, off, :]
+        new_value[s] = vc[phys, :, off, :]
+    live = slot_mapping[slot_mapping >= 0]
+    if len(np.unique(live)) != len(live):
+        raise ValueError("two sequences write the same slot")
+
+    return DecodeBatch(
+        name=name, dtype=dtype, num_heads=H, num_kv_heads=Hkv, head_dim=D, block_size=B,
+        scale=1.0 / math.sqrt(D), query=query, key_cache=kc, value_cache=vc,
+        block_tables=tables, context_lens=ctx.astype(np.int32), slot_mapping=slot_mapping,
+        new_key=new_key, new_value=new_value, partition_size=partition_size,
+        meta=dict(seed=seed, pool_factor=pool_factor, shared_prefix_tokens=shared_prefix_tokens,
+                  key_outlier_frac=key_outlier_frac, needed_blocks=needed))
+
+
+# ----------------------------------------------------------------------------
+# the five workloads
+
+
+CONFIG_NAMES = {
+    1: "tiny paged decode (2 seqs, ctx 7/33, MHA 4x64, fp16)",
+    2: "LLaMA-2-13B-shaped decode (batch 64, MHA 40x128, fp16, ctx U[128,2048])",
+    3: "Qwen3-4B-shaped GQA decode (batch 256, 32q/8kv x128, bf16, geometric ctx)",
+    4: "shared-prefix decode (128 seqs, 1024-token shared prefix + U[64,512] tails, 32q/8kv, fp16)",
+    5: "long-context split-K decode (batch 16, ctx 32768, MHA 40x128, fp16, 1% keys x8)",
+}
+
+
+def config_context_lens(n: int) -> np.ndarray:
+    """Context lengths of workload n (drawn from the workload's own seed)."""
+    rng = np.random.default_rng(1000 + n)
+    if n == 1:
+        return np.array([7, 33], dtype=np.int64)
+    if n == 2:
+        return rng.integers(128, 2048, size=64, endpoint=True)
+    if n == 3:
+        return np.clip(15 + rng.geometric(1.0 / 985.0, size=256), 16, 8192)
+    if n == 4:
+        return 1024 + rng.integers(64, 512, size=128, endpoint=True)
+    if n == 5:
+        return np.full(16, 32768, dtype=np.int64)
+    raise ValueError(n)
+
+
+def make_config(n: int, threads: int | None = None) -> DecodeBatch:
+    """Workload n (1..5) at full size."""
+    ctx = config_context_lens(n)
+    seed = 1000 + n
+    common = dict(seed=seed, context_lens=ctx, block_size=16, name=f"cfg{n}", threads=threads)
+    if n == 1:
+        return build_batch(num_heads=4, num_kv_heads=4, head_dim=64, dtype=F16, num_blocks=16, **common)
+    if n == 2:
+        return build_batch(num_heads=40, num_kv_heads=40, head_dim=128, dtype=F16, pool_factor=1.2, **common)
+    if n == 3:
+        return build_batch(num_heads=32, num_kv_heads=8, head_dim=128, dtype=BF16, pool_factor=1.2, **common)
+    if n == 4:
+        return build_batch(num_heads=32, num_kv_heads=8, head_dim=128, dtype=F16, pool_factor=1.2,
+                           shared_prefix_tokens=1024, **common)
+    if n == 5:
+        return build_batch(num_heads=40, num_kv_heads=40, head_dim=128, dtype=F16, pool_factor=1.0,
+                           key_outlier_frac=0.01, key_outlier_scale=8.0, **common)
+    raise ValueError(n)
+
+
+# ----------------------------------------------------------------------------
+# byte accounting (what a decode step must read, by definition)
+
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """K and V bytes one token occupies across all layers: 2 * L * Hkv * D * bytes.
+
+    "KV Cache와 PagedAttention 완전 해부", §3단계 (KV Cache는 GPU 메모리에 얼마나 차지하나).
+    """
+    return 2 * num_layers * num_kv_heads * head_dim * elem_bytes
+
+
+def algorithmic_kv_bytes(batch: DecodeBatch) -> int:
+    """K+V bytes one decode step reads: every context token of every kv head, once."""
+    return int(batch.context_lens.astype(np.int64).sum()) * batch.num_kv_heads * batch.head_dim * 2 * batch.elem_bytes
+
+
+def unique_kv_bytes(batch: DecodeBatch) -> int:
+    """K+V bytes of the distinct physical slots read (shared prefix blocks counted once)."""
+    B = batch.block_size
+    seen = set()
+    n = 0
+    for s in range(batch.num_seqs):
+        c = int(batch.context_lens[s])
+        for j in range((c + B - 1) // B):
+            phys = int(batch.block_tables[s, j])
+            valid = min(B, c - j * B)
+            if phys in seen:
+                continue
+            seen.add(phys)
+            n += valid
+    return n * batch.num_kv_heads * batch.head_dim * 2 * batch.elem_bytes
+
+
+def as_torch(batch: DecodeBatch, device):
+    """The batch's arrays as torch tensors on ``device`` (bit patterns kept)."""
+    import torch
+
+    tdt = torch.float16 if batch.dtype == F16 else torch.bfloat16
+
+    def half(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(device)
+
+    return dict(
+        query=half(batch.query), key_cache=half(batch.key_cache), value_cache=half(batch.value_cache),
+        new_key=half(batch.new_key), new_value=half(batch.new_value),
+        block_tables=torch.from_numpy(batch.block_tables).to(device),
+        context_lens=torch.from_numpy(batch.context_lens).to(device),
+        slot_mapping=torch.from_numpy(batch.slot_mapping).to(device),
+    )

@@ -1,0 +1,29 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture(scope="session")
+def golden():
+    import json
+
+    with open(os.path.join(ROOT, "tests", "golden", "pages_examples.json")) as f:
+        return json.load(f)
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The CUDA library, built if missing; skips nothing: a GPU test without it fails."""
+    from paged_kv_cache_91_gb300 import binding
+
+    binding.load()
+    return binding
