@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the paged KV cache library on GB300.
+
+A step is one pass of the whole hot path over one synthetic batch: the cache
+write of one new token per sequence (paged_kv_write) followed by paged decode
+attention over every sequence's context (paged_attention_decode: the decode
+kernel, plus the log-sum-exp reduce when a context spans several partitions).
+
+Default workload: the LLaMA-2-13B-shaped decode batch (64 sequences, 40 MHA
+heads x 128, fp16, block 16, contexts U[128, 2048]). The pool (1.7 GB) is
+larger than L2, so no flush runs between steps.
+
+One JSON line on rank 0:
+  value         KV bytes read per step / step time (GB/s), inputs resident in HBM
+  tokens_per_s  sequences decoded per second (one layer)
+  roofline      the decode call's algorithmic bytes / its event-timed duration
+                against the measured HBM copy bandwidth
+  e2e           the same metric through the public API with the step's inputs
+                copied from pinned host memory and the output read back
+  cpu_baseline  the CPU oracle (fp64, all host cores) on a bounded sample
+
+--impl reference times the CPU oracle alone (the only other implementation of
+this path) on the same workload and prints the same line with "impl".
+Multi-GPU (torchrun): every rank decodes its own batch (weak scaling); the
+timed region is bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-read HBM GB/s (% of peak) and decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2: LLaMA-2-13B-shaped)")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--max-seqs", type=int, default=None, help="use only the workload's first N sequences")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# process group (weak scaling: one independent batch per rank)
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# byte accounting
+
+
+def step_bytes(batch, partition_size: int):
+    """Algorithmic bytes of one decode call: KV reads plus q, out, tables and split-K partials."""
+    import numpy as np
+
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    P = partition_size or 512
+    ctx = batch.context_lens.astype(np.int64)
+    kv = W.algorithmic_kv_bytes(batch)
+    S, H, D, B = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size
+    qo = 2 * S * H * D * batch.elem_bytes
+    tables = int(((ctx + B - 1) // B).sum()) * 4 + S * 4
+    nparts = (ctx + P - 1) // P
+    split = nparts > 1
+    partials = int((nparts[split] * H).sum()) * (D + 2) * 4 * 2
+    return kv, kv + qo + tables + partials
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_91_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it matches these kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("csrc_hash") != csrc_hash():
+        return None
+    return entry.get("dram_bytes_per_call")
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.windows = []
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]),
+                                 reasons=[r for r, v in zip(self.REASONS, parts[6:10]) if v.lower() == "active"]))
+            except (ValueError, IndexError):
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0, t1):
+        inside = [r for r in rows if t0 - 0.15 <= r["ts"] <= t1 + 0.15]
+        used = inside or sorted(rows, key=lambda r: min(abs(r["ts"] - t0), abs(r["ts"] - t1)))[:3]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({x for r in used for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in used), "sm_max_mhz": max(r["smax"] for r in used),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def gpu_id_for(device) -> str:
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:  # noqa: BLE001
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = torch.cuda.current_device() if device is None else torch.device(device).index or 0
+        return vis.split(",")[idx] if vis else str(idx)
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+
+
+def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1):
+    """Run the oracle over the given sequences (all heads) until budget_s; returns (seconds, reps)."""
+    import numpy as np
+
+    import oracle
+
+    pairs = np.array([(s, h) for s in seqs for h in range(batch.num_heads)], dtype=np.int32)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode_c(batch.query, batch.key_cache, batch.value_cache, batch.block_tables, batch.context_lens,
+                        batch.scale, batch.dtype, pairs=pairs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= min_reps and el >= budget_s:
+            return el, reps
+
+
+def sample_kv_bytes(batch, seqs):
+    ctx = batch.context_lens[list(seqs)].astype("int64").sum()
+    return int(ctx) * batch.num_kv_heads * batch.head_dim * 2 * batch.elem_bytes
+
+
+# ----------------------------------------------------------------------------
+
+
+def workload_config(batch, n, partition_size, pool_bytes):
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    return {
+        "workload": W.CONFIG_NAMES[n],
+        "num_seqs": batch.num_seqs, "num_heads": batch.num_heads, "num_kv_heads": batch.num_kv_heads,
+        "head_dim": batch.head_dim, "block_size": batch.block_size, "cache_dtype": batch.dtype,
+        "context_lens": {"min": int(batch.context_lens.min()), "mean": float(batch.context_lens.mean()),
+                         "max": int(batch.context_lens.max())},
+        "partition_size": partition_size or 512,
+        "new_tokens_per_step": int((batch.slot_mapping >= 0).sum()),
+        "pool_bytes": pool_bytes,
+        "l2": "inputs larger than L2 (KV pool > 129 MB); no flush between steps",
+    }
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    batch = W.make_config(args.config)
+    S = batch.num_seqs
+    # size each step's sample so warm-up + timed steps take about two minutes
+    t_one, _ = time_oracle(batch, [0], 0.0)
+    per_seq = max(t_one, 1e-4)
+    total_steps = args.steps + args.warmup
+    nseq = int(max(1, min(S, 120.0 / (total_steps * per_seq))))
+    rng = np.random.default_rng(7)
+    times = []
+    kv_total = 0
+    for k in range(total_steps):
+        seqs = sorted(rng.choice(S, size=nseq, replace=False).tolist())
+        t0 = time.perf_counter()
+        time_oracle(batch, seqs, 0.0)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+            kv_total += sample_kv_bytes(batch, seqs)
+    total = sum(times)
+    value = kv_total / total / 1e9
+    cores = oracle.max_threads()
+    sample = f"{nseq} of {S} sequences (all {batch.num_heads} heads) per step, drawn at random"
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(batch, args.config, args.partition_size, int(batch.key_cache.nbytes * 2)),
+        "tokens_per_s": round(nseq * len(times) / total, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, dist):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_91_gb300 import binding
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    binding.load()
+    batch = W.make_config(args.config, max_seqs=args.max_seqs)
+    P = args.partition_size
+    t = W.as_torch(batch, dev)
+    out = torch.empty_like(t["query"])
+    mcl = batch.max_context_len
+    ws_bytes = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, batch.head_dim, mcl, P)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nparts = -(-mcl // (P or 512))
+    launches_per_step = 2 + (1 if nparts > 1 else 0)
+    kv_bytes, call_bytes = step_bytes(batch, P)
+
+    def step(q, nk, nv, sm, bt, cl, o):
+        binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
+        binding.paged_attention_decode(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
+                                       max_context_len=mcl, partition_size=P, workspace=ws, stream=stream)
+
+    args_dev = (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"],
+                t["context_lens"], out)
+    sampler = ClockSampler(gpu_id_for(dev))
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    binding.device_errors(clear=True)
+
+    # --- device-resident timed region
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        binding.paged_kv_write(t["new_key"], t["new_value"], t["key_cache"], t["value_cache"], t["slot_mapping"],
+                               stream=stream)
+        ev[k][0].record(stream)
+        binding.paged_attention_decode(out, t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
+                                       t["context_lens"], batch.scale, max_context_len=mcl, partition_size=P,
+                                       workspace=ws, stream=stream)
+        ev[k][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall1 = time.time()
+    total_ms = start.elapsed_time(end)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = dist.max(total_ms)
+    dec_avg_ms = statistics.fmean(decode_ms)
+    errors = binding.device_errors(clear=True)
+
+    # --- end to end through the public API, inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        host = {k: t[k].cpu().pin_memory() for k in ("query", "new_key", "new_value", "slot_mapping",
+                                                      "block_tables", "context_lens")}
+        dbuf = {k: torch.empty_like(t[k]) for k in host}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            step(dbuf["query"], dbuf["new_key"], dbuf["new_value"], dbuf["slot_mapping"], dbuf["block_tables"],
+                 dbuf["context_lens"], out)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = dist.max(s0.elapsed_time(s1))
+        e2e_val = dist.sum(kv_bytes) * K / (e2e_ms / 1e3) / 1e9
+        e2e = {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / K, 4)}
+
+    rows = sampler.stop()
+    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1)
+
+    total_kv = dist.sum(kv_bytes)
+    value = total_kv * K / (total_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
+    workload = f"cfg{args.config}"
+    traffic = ncu_traffic(workload)
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        seqs = list(range(batch.num_seqs))
+        el, reps = time_oracle(batch, seqs, args.cpu_seconds)
+        cpu = {"value": round(kv_bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{reps} full decode pass(es) of the workload (all {batch.num_seqs} sequences x "
+                         f"{batch.num_heads} heads), fp64, {el:.1f} s"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if batch.dtype == "f16" else "bf16",
+            "accumulate": "f32", "data": "synthetic (seeded N(0,1) K/V/q, block tables from a shuffled free list)",
+            "config": workload_config(batch, args.config, P, int(batch.key_cache.nbytes * 2)),
+            "tokens_per_s": round(batch.num_seqs * dist.world * K / (total_ms / 1e3), 1),
+            "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
+                            "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
+            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode kernel"
+                         + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
+                         "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_call": call_bytes, "avg_call_ms": round(dec_avg_ms, 4)},
+            "gpu_launches": K * launches_per_step,
+            "clocks": clocks,
+            "device_errors": errors,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

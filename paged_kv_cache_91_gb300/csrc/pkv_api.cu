@@ -1,0 +1,362 @@
+// C ABI of the paged KV cache library: argument validation, the cache-write
+// kernel, the split-K log-sum-exp reduce kernel, dispatch of the decode kernels
+// and the per-device error word. See include/paged_kv.h for the contract.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "paged_kv.h"
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxDevices = 64;
+constexpr int kWarpsPerCta = 4;            // decode kernels
+constexpr int kMaxBlocksPerWarp = 32;      // one physical id per lane
+
+thread_local char g_msg[512] = "";
+
+pkv_status_t fail(pkv_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pkv_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32; }
+
+}  // namespace
+
+// Per-device error word; kernels get its address as an argument.
+__device__ unsigned int g_pkv_error_word;
+
+namespace {
+
+unsigned* error_word(int dev) {
+  static unsigned* ptrs[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!ptrs[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pkv_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(ptr);
+  }
+  return ptrs[dev];
+}
+
+// ---------------------------------------------------------------------------
+// cache write: one thread per 16-byte piece of a (token, kv head) row, K and V
+
+__global__ void pkv_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                 uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                                 const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads,
+                                 int pieces_per_row, int block_size, long long num_slots, unsigned* err) {
+  const long long total = (long long)num_tokens * num_kv_heads * pieces_per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int c = (int)(idx % pieces_per_row);
+    const long long r = idx / pieces_per_row;
+    const int h = (int)(r % num_kv_heads);
+    const int t = (int)(r / num_kv_heads);
+    const long long slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (c == 0 && h == 0) atomicOr(err, PKV_DEVERR_SLOT);
+      continue;
+    }
+    const long long blk = slot / block_size, off = slot - blk * block_size;
+    const size_t src = ((size_t)t * num_kv_heads + h) * pieces_per_row + c;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * pieces_per_row + c;
+    key_cache[dst] = __ldg(key + src);
+    value_cache[dst] = __ldg(value + src);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-K reduce: merge the partitions' (m_p, l_p, o_p) of one (seq, head) by
+// log-sum-exp: out = sum_p w_p o_p / sum_p w_p with w_p = l_p 2^(m_p - max m).
+
+template <typename T>
+__global__ void pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o,
+                                  const float* __restrict__ part_m, const float* __restrict__ part_l,
+                                  const int32_t* __restrict__ context_lens, int num_heads, int head_dim,
+                                  int partition_size, int max_partitions, int ctx_limit) {
+  extern __shared__ float wsh[];  // [max_partitions] weights
+  __shared__ float s_inv;
+  const int h = blockIdx.x, s = blockIdx.y;
+  int ctx = context_lens[s];
+  ctx = ctx < 0 ? 0 : (ctx > ctx_limit ? ctx_limit : ctx);
+  const int np = (ctx + partition_size - 1) / partition_size;
+  if (np <= 1) return;  // the decode kernel wrote this row directly
+  const size_t row = (size_t)s * num_heads + h;
+  const size_t base = row * max_partitions;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int q = lane; q < np; q += 32) M = fmaxf(M, part_m[base + q]);
+    M = warp_max(M);
+    float W = 0.f;
+    for (int q = lane; q < np; q += 32) {
+      const float mq = part_m[base + q];
+      const float wq = mq == -INFINITY ? 0.f : part_l[base + q] * fast_exp2(mq - M);
+      wsh[q] = wq;
+      W += wq;
+    }
+    W = warp_sum(W);
+    if (lane == 0) s_inv = W > 0.f ? 1.f / W : 0.f;
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+    float o = 0.f;
+    for (int q = 0; q < np; ++q) o += wsh[q] * part_o[(base + q) * head_dim + d];
+    out[row * head_dim + d] = Elem<T>::from_float(o * inv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps for the grouped-query kernel
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+  }
+  return fn;
+}
+
+// The pool viewed as a 2D array [num_blocks * num_kv_heads * block_size][head_dim],
+// copied in boxes of 64 dims x block_size rows with the 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* base, long long rows, int head_dim, int block_size,
+                   pkv_dtype_t dtype) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int max_partitions_for(int max_context_len, int partition_size) {
+  const int n = (max_context_len + partition_size - 1) / partition_size;
+  return n < 1 ? 1 : n;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status_t status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+  }
+  return "PKV_UNKNOWN_STATUS";
+}
+
+const char* pkv_last_error_message(void) { return g_msg; }
+
+pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache, void* value_cache,
+                            const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t num_blocks, pkv_dtype_t dtype,
+                            cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_kv_heads <= 0 || num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key, value and caches must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+  const int pieces = head_dim * 2 / 16;
+  const long long total = (long long)num_tokens * num_kv_heads * pieces;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  pkv_write_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(key_cache),
+      static_cast<uint4*>(value_cache), slot_mapping, num_tokens, num_kv_heads, pieces, block_size,
+      (long long)num_blocks * block_size, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write launch");
+  return PKV_OK;
+}
+
+size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                      int32_t max_context_len, int32_t partition_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0) return 0;
+  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int np = max_partitions_for(max_context_len, P);
+  if (np <= 1) return 0;
+  return (size_t)num_seqs * num_heads * np * (head_dim + 2) * sizeof(float);
+}
+
+pkv_status_t paged_attention_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+                                    float scale, int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                    int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
+                num_kv_heads);
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len < 0");
+  if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
+                max_context_len, (long long)max_blocks_per_seq * block_size);
+  if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
+  const int P = partition_size ? partition_size : kDefaultPartition;
+  if (P % block_size || P < block_size || P > kWarpsPerCta * kMaxBlocksPerWarp * block_size)
+    return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
+                block_size, kWarpsPerCta * kMaxBlocksPerWarp * block_size);
+  if (num_seqs > 65535 || num_heads > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
+
+  const int np = max_partitions_for(max_context_len, P);
+  const size_t need = paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_context_len, P);
+  if (need) {
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", need);
+    if (workspace_bytes < need)
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+    if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+
+  DecodeParams p{};
+  p.out = out;
+  p.query = query;
+  p.key_cache = static_cast<const unsigned char*>(key_cache);
+  p.value_cache = static_cast<const unsigned char*>(value_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  if (need) {
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_seqs * num_heads * np;
+    p.part_o = ws;
+    p.part_m = ws + rows * head_dim;
+    p.part_l = p.part_m + rows;
+  }
+  p.err = err;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.partition_size = P;
+  p.max_partitions = np;
+  p.ctx_limit = max_context_len;
+
+  const int G = p.group;
+  if (G >= 2 && G <= 8) {
+    CUtensorMap kmap, vmap;
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
+        !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+    e = dtype == PKV_F16 ? decode_mma_f16(p, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                         : decode_mma_bf16(p, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  } else {
+    e = dtype == PKV_F16 ? decode_simt_f16(p, head_dim, block_size, num_seqs, stream)
+                         : decode_simt_bf16(p, head_dim, block_size, num_seqs, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+
+  if (np > 1) {
+    const dim3 grid(num_heads, num_seqs);
+    const int threads = head_dim;
+    const size_t shm = (size_t)np * sizeof(float);
+    if (dtype == PKV_F16) {
+      pkv_reduce_kernel<__half><<<grid, threads, shm, stream>>>(static_cast<__half*>(out), p.part_o, p.part_m,
+                                                                p.part_l, context_lens, num_heads, head_dim, P, np,
+                                                                p.ctx_limit);
+    } else {
+      pkv_reduce_kernel<__nv_bfloat16><<<grid, threads, shm, stream>>>(
+          static_cast<__nv_bfloat16*>(out), p.part_o, p.part_m, p.part_l, context_lens, num_heads, head_dim, P,
+          np, p.ctx_limit);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+  }
+  return PKV_OK;
+}
+
+pkv_status_t paged_kv_device_errors(uint32_t* flags, int32_t clear) {
+  g_msg[0] = '\0';
+  if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is null");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_pkv_error_word, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_pkv_error_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  }
+  *flags = v;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,339 @@
+// Grouped-query decode attention over the paged KV pool on the tensor cores: one
+// CTA per (context partition, kv head, sequence) serving all G = H / Hkv query
+// heads of that kv head, so each KV tile is read from HBM once per group
+// ("Sparse Computation and Memory Management ...": GQA, 32 Q heads / 8 KV heads).
+//
+// With G >= 2 the per-block work is a dense contraction: for a 16-token slice
+// of a block, S^T[16 x G] = K[16 x D] . Q^T[D x G] and O^T[D x G] += V^T[D x 16] .
+// P^T[16 x G]. Both run as m16n8k16 warp MMAs with fp32 accumulation; the G
+// query heads sit in the n = 8 dimension (G <= 8). The score fragment is turned
+// into the PV operand in registers with movmatrix, so P never touches shared
+// memory. P is rounded to the cache dtype for the PV product, and the running
+// sum l adds the same rounded values, so weights and normaliser agree.
+//
+// Data movement: per-warp rings as in the CUDA-core kernel, but each tile comes
+// in through a 2D tensor map in boxes of 64 head dims x block_size tokens with
+// the 128-byte swizzle, which makes every ldmatrix phase conflict-free.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+template <int D, int BS, int NW, int SPW>
+struct MmaShape {
+  static constexpr int NBOX = D / 64;         // swizzled boxes per tile (64 dims x BS rows each)
+  static constexpr int BOXB = BS * 128;       // bytes of one box
+  static constexpr int TILE = NBOX * BOXB;    // = BS * D * 2
+  static constexpr int STAGE = 2 * TILE;      // K tile + V tile
+  static constexpr int RING = NW * SPW * STAGE;
+  static constexpr int BARS = RING;
+  static constexpr int SMEM_USED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
+  static constexpr int SMEM = SMEM_USED + 1024;  // slack to align the ring to 1024 bytes
+  static constexpr int CH = BS >= 16 ? BS / 16 : 1;  // 16-token slices per block
+  static constexpr int ROWS = BS >= 16 ? 16 : BS;    // real rows per slice
+  static constexpr int KT = D / 16;                  // k-steps of the score MMA / m-tiles of PV
+  static constexpr int RED_PER_WARP = (8 * D + 16) * 4;
+  static_assert(TILE == BS * D * 2, "tile bytes");
+  static_assert(BOXB % 1024 == 0, "swizzle atoms need 1024-byte aligned boxes");
+  static_assert(RED_PER_WARP <= SPW * STAGE, "reduction scratch reuses the warp's ring");
+};
+
+// Byte offset of 16-byte piece `piece` (of D/8) of token row `t` inside a tile
+// stored as NBOX swizzled boxes.
+template <int BS>
+__device__ __forceinline__ int swz_offset(int t, int piece) {
+  const int box = piece >> 3, chunk = piece & 7;
+  return box * (BS * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
+}
+
+template <typename T, int D, int BS, int NW, int SPW>
+__global__ void __launch_bounds__(NW * 32)
+    pkv_decode_gqa_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                              const __grid_constant__ CUtensorMap vmap) {
+  using Sh = MmaShape<D, BS, NW, SPW>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int ctx = clamp_context(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
+  const int P = p.partition_size;
+  const int tok0 = part * P;
+  const size_t row0 = (size_t)s * p.num_heads + (size_t)kvh * G;  // first query head row
+
+  if (ctx == 0) {
+    if (part == 0) {
+      T* out = reinterpret_cast<T*>(p.out) + row0 * D;
+      for (int i = threadIdx.x; i < G * D; i += NW * 32) out[i] = Elem<T>::from_float(0.f);
+    }
+    return;
+  }
+  if (tok0 >= ctx) return;
+  const int tok1 = min(tok0 + P, ctx);
+  const bool direct = ctx <= P;
+  const int blk0 = tok0 / BS;
+  const int nblk = (tok1 - tok0 + BS - 1) / BS;
+  const int nmine = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+
+  int my_phys = -1;
+  if (lane < nmine) {
+    const int v = p.block_tables[(size_t)s * p.max_blocks_per_seq + blk0 + warp + NW * lane];
+    if ((unsigned)v < (unsigned)p.num_blocks) {
+      my_phys = v;
+    } else {
+      atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+    }
+  }
+
+  unsigned char* ring = smem + warp * SPW * Sh::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BARS) + warp * SPW;
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < SPW; ++k) mbar_init(bars + k, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {
+    const int phys = __shfl_sync(kFull, my_phys, i);
+    if (lane == 0) {
+      uint64_t* bar = bars + (i % SPW);
+      unsigned char* st = ring + (i % SPW) * Sh::STAGE;
+      if (phys >= 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, Sh::STAGE);
+        const int y = (phys * p.num_kv_heads + kvh) * BS;  // first row of the tile
+#pragma unroll
+        for (int b = 0; b < Sh::NBOX; ++b) {
+          tma_load_2d(st + b * Sh::BOXB, &kmap, 64 * b, y, bar);
+          tma_load_2d(st + Sh::TILE + b * Sh::BOXB, &vmap, 64 * b, y, bar);
+        }
+      } else {
+        mbar_arrive(bar);
+      }
+    }
+  };
+  const int nfirst = nmine < SPW ? nmine : SPW;
+  for (int i = 0; i < nfirst; ++i) issue(i);
+  int issued = nfirst;
+
+  // Q^T as the B operand of the score MMA: lane holds head n = lane / 4,
+  // dims 2 (lane % 4) + {0, 1} (+ 8) of each 16-dim k-step. Heads >= G are zero.
+  const int n_head = lane >> 2, kq = (lane & 3) * 2;
+  uint32_t qb[Sh::KT][2];
+  {
+    const T* q = reinterpret_cast<const T*>(p.query) + (row0 + n_head) * D;
+#pragma unroll
+    for (int kk = 0; kk < Sh::KT; ++kk) {
+      if (n_head < G) {
+        qb[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(q + kk * 16 + kq));
+        qb[kk][1] = __ldg(reinterpret_cast<const uint32_t*>(q + kk * 16 + 8 + kq));
+      } else {
+        qb[kk][0] = 0u;
+        qb[kk][1] = 0u;
+      }
+    }
+  }
+
+  // running state of this lane's two heads (columns j0 = 2 (lane % 4), j0 + 1)
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float acc[Sh::KT][4];
+#pragma unroll
+  for (int mt = 0; mt < Sh::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+  const int mi = lane >> 3;       // which 8x8 matrix this lane addresses in ldmatrix
+  const int r8 = lane & 7;        // row inside that matrix
+  const int r0 = lane >> 2;       // accumulator rows r0 and r0 + 8
+  const float sl2 = p.scale_log2;
+
+  int failed_at = -1;
+  for (int i = 0; i < nmine; ++i) {
+    const int phys = __shfl_sync(kFull, my_phys, i);
+    const int k = i % SPW;
+    const bool ready = __all_sync(kFull, mbar_wait(bars + k, (i / SPW) & 1));
+    if (!ready) {
+      failed_at = i;
+      break;
+    }
+    if (phys >= 0) {
+      unsigned char* Ks = ring + k * Sh::STAGE;
+      unsigned char* Vs = Ks + Sh::TILE;
+      const int lb = warp + NW * i;
+      const int nvalid = min(BS, tok1 - (blk0 + lb) * BS);
+      if (nvalid < BS) {
+        // value rows past the context may hold anything (even NaN): zero them so
+        // that their zero weights contribute exactly zero
+        const int nz = (BS - nvalid) * (D / 8);
+        for (int idx = lane; idx < nz; idx += 32) {
+          const int t = nvalid + idx / (D / 8), piece = idx % (D / 8);
+          *reinterpret_cast<uint4*>(Vs + swz_offset<BS>(t, piece)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+#pragma unroll
+      for (int c = 0; c < Sh::CH; ++c) {
+        if (c * 16 < nvalid) {
+          // scores S^T[token][head] for 16 tokens
+          float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const int rr = r8 + ((mi & 1) << 3);  // A rows 0..15
+            const int t = BS >= 16 ? c * 16 + rr : (rr & (BS - 1));
+#pragma unroll
+            for (int kk = 0; kk < Sh::KT; ++kk) {
+              uint32_t a[4];
+              ldmatrix_x4(a, Ks + swz_offset<BS>(t, kk * 2 + (mi >> 1)));
+              Mma<T>::run(sacc, a, qb[kk][0], qb[kk][1]);
+            }
+          }
+          const int ta = c * 16 + r0, tb = ta + 8;
+          const bool va = (BS >= 16 || r0 < BS) && ta < nvalid;
+          const bool vb = BS >= 16 && tb < nvalid;
+          const float x00 = va ? sacc[0] * sl2 : -INFINITY;
+          const float x01 = va ? sacc[1] * sl2 : -INFINITY;
+          const float x10 = vb ? sacc[2] * sl2 : -INFINITY;
+          const float x11 = vb ? sacc[3] * sl2 : -INFINITY;
+          float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+          const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - mn0), fast_exp2(x01 - mn1));
+          const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - mn0), fast_exp2(x11 - mn1));
+          const float2 fa = Elem<T>::to_float2(pa), fb = Elem<T>::to_float2(pb);
+          float rs0 = fa.x + fb.x, rs1 = fa.y + fb.y;
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            rs0 += __shfl_xor_sync(kFull, rs0, o);
+            rs1 += __shfl_xor_sync(kFull, rs1, o);
+          }
+          l0 = l0 * al0 + rs0;
+          l1 = l1 * al1 + rs1;
+          m0 = mn0;
+          m1 = mn1;
+#pragma unroll
+          for (int mt = 0; mt < Sh::KT; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+          // P^T as the B operand of the PV MMA: transpose the 8x8 score fragments
+          const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
+          {
+            const int tr = r8 + ((mi >> 1) << 3);  // stored V rows 0..15
+            const int t = BS >= 16 ? c * 16 + tr : (tr & (BS - 1));
+#pragma unroll
+            for (int mt = 0; mt < Sh::KT; ++mt) {
+              uint32_t a[4];
+              ldmatrix_x4_trans(a, Vs + swz_offset<BS>(t, mt * 2 + (mi & 1)));
+              Mma<T>::run(acc[mt], a, b0, b1);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (i + SPW < nmine) {
+      issue(i + SPW);
+      ++issued;
+    }
+  }
+
+  if (failed_at >= 0) {
+    if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    for (int j = failed_at; j < issued; ++j) mbar_wait(bars + (j % SPW), (j / SPW) & 1);
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < Sh::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  }
+
+  // merge the warps: each warp writes [head][D] accumulators, m, l into its own ring slice
+  float* red = reinterpret_cast<float*>(ring);
+  float* red_m = red + 8 * D;
+  float* red_l = red_m + 8;
+  const int j0 = (lane & 3) * 2;
+#pragma unroll
+  for (int mt = 0; mt < Sh::KT; ++mt) {
+    const int d0 = mt * 16 + r0;
+    red[j0 * D + d0] = acc[mt][0];
+    red[(j0 + 1) * D + d0] = acc[mt][1];
+    red[j0 * D + d0 + 8] = acc[mt][2];
+    red[(j0 + 1) * D + d0 + 8] = acc[mt][3];
+  }
+  if (lane < 4) {
+    red_m[j0] = m0;
+    red_m[j0 + 1] = m1;
+    red_l[j0] = l0;
+    red_l[j0 + 1] = l1;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * SPW * Sh::STAGE)[8 * D + g]);
+    float L = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float* rw = reinterpret_cast<float*>(smem + w * SPW * Sh::STAGE);
+      const float mw = rw[8 * D + g];
+      const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+      L += rw[8 * D + 8 + g] * f;
+      o += rw[g * D + d] * f;
+    }
+    o = L > 0.f ? o / L : 0.f;
+    const size_t row = row0 + g;
+    if (direct) {
+      reinterpret_cast<T*>(p.out)[row * D + d] = Elem<T>::from_float(o);
+    } else {
+      p.part_o[(row * p.max_partitions + part) * D + d] = o;
+      if (d == 0) {
+        p.part_m[row * p.max_partitions + part] = M;
+        p.part_l[row * p.max_partitions + part] = L;
+      }
+    }
+  }
+}
+
+template <int D, int BS>
+constexpr int mma_stages() {
+  constexpr int stage = 2 * BS * D * 2;
+  constexpr int spw = (96 * 1024) / (4 * stage);
+  return spw < 2 ? 2 : (spw > 6 ? 6 : spw);
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_decode_gqa_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                  int num_seqs, cudaStream_t stream) {
+  constexpr int NW = 4;
+  constexpr int SPW = mma_stages<D, BS>();
+  using Sh = MmaShape<D, BS, NW, SPW>;
+  auto kern = pkv_decode_gqa_mma_kernel<T, D, BS, NW, SPW>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const dim3 grid(p.max_partitions, p.num_kv_heads, num_seqs);
+  kern<<<grid, NW * 32, Sh::SMEM, stream>>>(p, kmap, vmap);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

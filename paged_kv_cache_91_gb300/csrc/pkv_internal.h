@@ -1,0 +1,23 @@
+// Host-side entry points shared between the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+struct DecodeParams;
+
+// CUDA-core decode (any group size; one CTA per query head).
+cudaError_t decode_simt_f16(const DecodeParams& p, int head_dim, int block_size, int num_seqs,
+                            cudaStream_t stream);
+cudaError_t decode_simt_bf16(const DecodeParams& p, int head_dim, int block_size, int num_seqs,
+                             cudaStream_t stream);
+
+// Tensor-core grouped-query decode (2 <= group <= 8; one CTA per kv head).
+cudaError_t decode_mma_f16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+cudaError_t decode_mma_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+
+}  // namespace pkv

@@ -281,9 +281,11 @@ def config_context_lens(n: int) -> np.ndarray:
     raise ValueError(n)
 
 
-def make_config(n: int, threads: int | None = None) -> DecodeBatch:
-    """Workload n (1..5) at full size."""
+def make_config(n: int, threads: int | None = None, max_seqs: int | None = None) -> DecodeBatch:
+    """Workload n (1..5) at full size, or its first ``max_seqs`` sequences."""
     ctx = config_context_lens(n)
+    if max_seqs is not None:
+        ctx = ctx[:max_seqs]
     seed = 1000 + n
     common = dict(seed=seed, context_lens=ctx, block_size=16, name=f"cfg{n}", threads=threads)
     if n == 1:

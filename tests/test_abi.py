@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_kv.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_91_gb300 import build as b
+    from paged_kv_cache_91_gb300 import binding
+
+    b.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:pkv_status_t|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("paged_kv_write", "paged_attention_decode", "paged_attention_workspace_size",
+              "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    from paged_kv_cache_91_gb300 import binding
+
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(-3) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(7) == b"PKV_UNKNOWN_STATUS"
+
+
+def test_workspace_size(lib):
+    ws = lib.paged_attention_workspace_size
+    assert ws(64, 40, 128, 512, 512) == 0  # one partition: no workspace
+    assert ws(64, 40, 128, 513, 512) == 64 * 40 * 2 * 130 * 4
+    assert ws(16, 40, 128, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
+    assert ws(0, 40, 128, 4096, 0) == 0 and ws(4, 40, 128, -1, 0) == 0
+
+
+P = ctypes.c_void_p
+
+
+def fake(n=1):
+    """A non-null, 256-byte aligned address that is never dereferenced on the host path."""
+    return P(0x10000 * n)
+
+
+def decode(lib, **kw):
+    a = dict(out=fake(1), query=fake(2), key_cache=fake(3), value_cache=fake(4), block_tables=fake(5),
+             max_blocks_per_seq=8, context_lens=fake(6), num_seqs=2, max_context_len=128, scale=0.125,
+             block_size=16, num_heads=4, num_kv_heads=4, head_dim=64, num_blocks=16, dtype=0,
+             partition_size=0, workspace=None, workspace_bytes=0, stream=None)
+    a.update(kw)
+    return lib.paged_attention_decode(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(out=None), INVALID),
+    (dict(num_seqs=-1), INVALID),
+    (dict(num_heads=6, num_kv_heads=4), INVALID),
+    (dict(num_kv_heads=0), INVALID),
+    (dict(head_dim=96), UNSUPPORTED),
+    (dict(block_size=12), UNSUPPORTED),
+    (dict(dtype=5), INVALID),
+    (dict(scale=float("nan")), INVALID),
+    (dict(max_context_len=129), INVALID),           # > max_blocks_per_seq * block_size
+    (dict(partition_size=24), UNSUPPORTED),          # not a multiple of block_size
+    (dict(partition_size=16 * 129), UNSUPPORTED),    # more blocks than the kernel keeps per partition
+    (dict(query=P(0x10008)), INVALID),               # misaligned
+    (dict(max_blocks_per_seq=64, max_context_len=1024), WORKSPACE),   # split needs a workspace
+    (dict(max_blocks_per_seq=64, max_context_len=1024, workspace=fake(9), workspace_bytes=100), WORKSPACE),
+    (dict(num_seqs=70000), UNSUPPORTED),
+])
+def test_decode_rejects_on_host(lib, kw, status):
+    assert decode(lib, **kw) == status
+    assert lib.pkv_last_error_message() != b""
+
+
+def test_decode_empty_batch_is_a_noop(lib):
+    assert decode(lib, num_seqs=0, out=None, query=None) == OK
+
+
+def write(lib, **kw):
+    a = dict(key=fake(1), value=fake(2), key_cache=fake(3), value_cache=fake(4), slot_mapping=fake(5),
+             num_tokens=4, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8, dtype=1, stream=None)
+    a.update(kw)
+    return lib.paged_kv_write(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(key=None), INVALID),
+    (dict(slot_mapping=None), INVALID),
+    (dict(num_tokens=-2), INVALID),
+    (dict(head_dim=80), UNSUPPORTED),
+    (dict(block_size=64), UNSUPPORTED),
+    (dict(num_blocks=0), INVALID),
+    (dict(key_cache=P(0x30004)), INVALID),
+    (dict(dtype=2), INVALID),
+])
+def test_write_rejects_on_host(lib, kw, status):
+    assert write(lib, **kw) == status
+
+
+def test_write_zero_tokens_is_a_noop(lib):
+    assert write(lib, num_tokens=0, key=None) == OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    from paged_kv_cache_91_gb300 import binding
+
+    x = torch.zeros(2, 4, 64, dtype=torch.float16)
+    kc = torch.zeros(4, 4, 16, 64, dtype=torch.float16)
+    with pytest.raises(binding.PagedKVError):
+        binding.paged_attention_decode(x, x, kc, kc, torch.zeros(2, 1, dtype=torch.int32),
+                                       torch.zeros(2, dtype=torch.int32), 0.125)
+
+
+def test_package_does_not_import_the_oracle():
+    """The product package and its sources never reference the oracle."""
+    pkg = os.path.join(ROOT, "paged_kv_cache_91_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
+                assert "liboracle" not in src and "pkv_oracle" not in src, f
