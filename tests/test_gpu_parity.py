@@ -249,7 +249,7 @@ def test_bad_slot_is_reported_and_skipped():
 @pytest.mark.parametrize("D,B", [(64, 8), (64, 32), (128, 8), (128, 16), (128, 32)])
 def test_write_copies_arbitrary_bits(D, B):
     rng = np.random.default_rng(36)
-    NB, Hkv, T = 40, 3, 333
+    NB, Hkv, T = 60, 3, 333
     kc = rng.integers(0, 65536, size=(NB, Hkv, B, D), dtype=np.uint16)
     vc = rng.integers(0, 65536, size=(NB, Hkv, B, D), dtype=np.uint16)
     slots = rng.choice(NB * B, size=T, replace=False).astype(np.int64)
