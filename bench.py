@@ -126,16 +126,23 @@ def step_bytes(batch, partition_size: int):
     return kv, kv + qo + tables + partials
 
 
-def csrc_hash() -> str:
+KERNEL_SOURCES = {
+    "simt": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_f16.cu", "pkv_decode_simt_bf16.cu"),
+    "mma": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_f16.cu", "pkv_decode_mma_bf16.cu"),
+}
+
+
+def kernel_hash(kind: str) -> str:
+    """Hash of the sources that define one decode kernel (ties an ncu capture to the code it measured)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_91_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "paged_kv_cache_91_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it matches these kernels."""
+def ncu_traffic(workload: str, kind: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it matches the kernel's sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -143,7 +150,7 @@ def ncu_traffic(workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(workload)
-    if not entry or entry.get("csrc_hash") != csrc_hash():
+    if not entry or entry.get("kernel_hash") != kernel_hash(kind):
         return None
     return entry.get("dram_bytes_per_call")
 
@@ -419,7 +426,8 @@ def run_ours(args, dist):
     peak, peak_kind = hbm_peak()
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     workload = f"cfg{args.config}"
-    traffic = ncu_traffic(workload)
+    G = batch.num_heads // batch.num_kv_heads
+    traffic = ncu_traffic(workload, "mma" if 2 <= G <= 8 else "simt")
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
