@@ -148,6 +148,48 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
                                     int32_t partition_size, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the library-owned split-K scratch of
+ * paged_attention_decode_static_workspace: 32 MiB per device. It covers, for
+ * example, 16 sequences x 40 heads x 32768-token contexts at partition_size 512. */
+#define PKV_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+/*
+ * paged_attention_decode_static_workspace -- paged_attention_decode for callers
+ * that cannot allocate device memory at call time.
+ *
+ * The pages have no counterpart to this call; it exists for users of this
+ * library. Some callers cannot hand paged_attention_decode a workspace: a plain
+ * C host with no device allocator of its own, a process whose device memory is
+ * already fully reserved by another allocator (a new cudaMalloc would fail), or
+ * a latency-bound decode loop that must not call cudaMalloc (it can synchronise
+ * the device). This call takes the same arguments minus the workspace and uses
+ * a scratch array compiled into the library instead. It allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ *   - The scratch is PKV_STATIC_WORKSPACE_BYTES of device memory per GPU that
+ *     loads the library, held until the process exits.
+ *   - The first call on each device (with that device current) looks up the
+ *     scratch array's device address with cudaGetSymbolAddress; make that first
+ *     call before any stream capture on that device.
+ *   - A call whose split-K scratch (paged_attention_workspace_size) exceeds
+ *     PKV_STATIC_WORKSPACE_BYTES launches nothing and returns PKV_ERR_WORKSPACE,
+ *     with the sizes in pkv_last_error_message().
+ *   - Every call on a device shares the one scratch array, which keeps the last
+ *     call's contents. Nothing in it needs clearing: each call writes every
+ *     partial before reading it. Calls whose kernels overlap on the GPU (other
+ *     streams, other host threads) race on the scratch and give wrong results;
+ *     keep such calls on one stream, or use paged_attention_decode with
+ *     separate workspaces.
+ *
+ * Results, arguments and every other error behaviour are those of
+ * paged_attention_decode.
+ */
+pkv_status_t paged_attention_decode_static_workspace(
+    void* out, const void* query, const void* key_cache, const void* value_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+    float scale, int32_t block_size, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_blocks, pkv_dtype_t dtype, int32_t partition_size, cudaStream_t stream);
+
 /*
  * paged_kv_device_errors -- read the current device's error word (PKV_DEVERR_* bits
  * set by kernels since it was last cleared) into *flags, and clear it if `clear`

@@ -157,3 +157,40 @@ def device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(lib, lib.paged_kv_device_errors(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def paged_attention_decode_static_workspace(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                            value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                            context_lens: torch.Tensor, scale: float,
+                                            max_context_len: Optional[int] = None, partition_size: int = 0,
+                                            stream=None) -> torch.Tensor:
+    """paged_attention_decode without a caller workspace, for callers that cannot allocate device memory.
+
+    The split-K scratch is the library's own PKV_STATIC_WORKSPACE_BYTES (32 MiB)
+    array on each device, so nothing is allocated here or in the library.
+    Calls on one device share that array: calls that overlap on the GPU race.
+    """
+    lib = load()
+    fn = lib.paged_attention_decode_static_workspace
+    if fn.argtypes is None:
+        P, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        fn.restype = i32
+        fn.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32, i32, P]
+    dt = _cuda16("query", query)
+    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
+        if _cuda16(n, t) != dt:
+            raise PagedKVError(-1, f"{n} dtype differs from query")
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    S, H, _ = query.shape
+    if out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between query, out and caches")
+    maxb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxb * B
+    _check(lib, fn(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
+                   _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt,
+                   int(partition_size), _stream(query, stream)))
+    return out

@@ -166,6 +166,9 @@ int max_partitions_for(int max_context_len, int partition_size) {
 }
 
 }  // namespace
+
+void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 }  // namespace pkv
 
 using namespace pkv;

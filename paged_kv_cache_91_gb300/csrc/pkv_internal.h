@@ -20,4 +20,7 @@ cudaError_t decode_mma_f16(const DecodeParams& p, const CUtensorMap& kmap, const
 cudaError_t decode_mma_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             int head_dim, int block_size, int num_seqs, cudaStream_t stream);
 
+// Set the calling thread's pkv_last_error_message() text.
+void set_last_error_message(const char* msg);
+
 }  // namespace pkv
