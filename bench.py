@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2: LLaMA-2-13B-shaped)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--max-seqs", type=int, default=None, help="use only the workload's first N sequences")
+    ap.add_argument("--path", choices=["persistent", "partitioned"], default=None,
+                    help="decode path (default: the library's automatic choice)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
@@ -339,7 +341,11 @@ def run_ours(args, dist):
     t = W.as_torch(batch, dev)
     out = torch.empty_like(t["query"])
     mcl = batch.max_context_len
-    ws_bytes = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, batch.head_dim, mcl, P)
+    if args.path:
+        binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
+                                 "persistent": binding.DECODE_PERSISTENT}[args.path])
+    ws_bytes = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, batch.num_kv_heads,
+                                                      batch.head_dim, batch.block_size, mcl, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     nparts = -(-mcl // (P or 512))

@@ -42,7 +42,9 @@ def load():
     lib.paged_kv_write.restype = i32
     lib.paged_kv_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.paged_attention_workspace_size.restype = sz
-    lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pkv_set_decode_path.restype = i32
+    lib.pkv_set_decode_path.argtypes = [i32]
     lib.paged_attention_decode.restype = i32
     lib.paged_attention_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
                                            i32, P, sz, P]
@@ -101,10 +103,21 @@ def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tens
                                    T, Hkv, D, B, NB, dt, _stream(key_cache, stream)))
 
 
-def paged_attention_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
-                                   partition_size: int = 0) -> int:
-    return int(load().paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
-                                                     partition_size))
+DECODE_AUTO, DECODE_PARTITIONED, DECODE_PERSISTENT = 0, 1, 2
+
+
+def set_decode_path(path: int) -> int:
+    """Choose the decode path for later calls (DECODE_*); returns the previous choice."""
+    prev = int(load().pkv_set_decode_path(int(path)))
+    if prev < 0:
+        raise PagedKVError(-1, f"unknown decode path {path}")
+    return prev
+
+
+def paged_attention_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                   block_size: int, max_context_len: int, partition_size: int = 0) -> int:
+    return int(load().paged_attention_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                     max_context_len, partition_size))
 
 
 def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
@@ -140,7 +153,7 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     maxb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = maxb * B
-    need = int(lib.paged_attention_workspace_size(S, H, D, max_context_len, partition_size))
+    need = int(lib.paged_attention_workspace_size(S, H, Hkv, D, B, max_context_len, partition_size))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0

@@ -54,10 +54,16 @@ def _stale(target: str, inputs) -> bool:
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile what changed and link the library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "HOST_ARCH")
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile what changed and link the library; returns its path.
+
+    ``extra_flags`` (e.g. ``-DPKV_SIMT_RING_BYTES=65536``) with a separate
+    ``lib_path``/``build_dir`` builds a tuning variant beside the default library.
+    """
+    BUILD_ = build_dir
+    os.makedirs(BUILD_, exist_ok=True)
+    stamp = os.path.join(BUILD_, "HOST_ARCH")
     arch = platform.machine()
     if not os.path.exists(stamp) or open(stamp).read().strip() != arch:
         force = True  # objects from another host architecture
@@ -67,7 +73,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
     jobs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + deps):
             jobs.append((src, obj))
@@ -75,9 +81,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     def compile_one(job):
         src, obj = job
         tmp = obj + f".tmp{os.getpid()}"
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", tmp]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", tmp]
         r = subprocess.run(cmd, capture_output=True, text=True)
-        log = os.path.join(BUILD, os.path.basename(src) + ".log")
+        log = os.path.join(BUILD_, os.path.basename(src) + ".log")
         with open(log, "w") as f:
             f.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         if r.returncode != 0:
@@ -90,16 +96,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
             for src in ex.map(compile_one, jobs):
                 if verbose:
                     print("compiled", os.path.relpath(src, ROOT), file=sys.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr[-6000:]}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib_path)
         with open(stamp, "w") as f:
             f.write(arch + "\n")
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

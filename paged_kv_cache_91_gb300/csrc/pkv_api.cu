@@ -6,9 +6,13 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
+
+#include <atomic>
 
 #include "paged_kv.h"
 #include "pkv_common.cuh"
+#include "pkv_decode_stream.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -16,8 +20,6 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 constexpr int kMaxDevices = 64;
-constexpr int kWarpsPerCta = 4;            // decode kernels
-constexpr int kMaxBlocksPerWarp = 32;      // one physical id per lane
 
 thread_local char g_msg[512] = "";
 
@@ -165,6 +167,56 @@ int max_partitions_for(int max_context_len, int partition_size) {
   return n < 1 ? 1 : n;
 }
 
+std::atomic<int> g_decode_path{PKV_DECODE_AUTO};
+
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// How one decode call runs and what workspace it needs.
+struct Plan {
+  bool stream;  // persistent equal-work kernel (else the partitioned grid kernel)
+  bool mma;     // tensor-core grouped-query tile (else CUDA cores)
+  int ng, gc;   // head groups per sequence, query heads per group
+  int np;       // partitions per sequence on the grid path
+  int wcap;     // warps the stream path may use (multiple of kDecodeWarps)
+  size_t pre_bytes, need;
+};
+
+Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_context_len,
+               int partition_size) {
+  Plan pl{};
+  const int G = num_heads / num_kv_heads;
+  pl.mma = G >= 2 && G <= 8;
+  pl.ng = pl.mma ? num_kv_heads : num_heads;
+  pl.gc = pl.mma ? G : 1;
+  const long long mb = (max_context_len + block_size - 1) / block_size;
+  const long long tiles = (long long)num_seqs * pl.ng * mb;  // upper bound on the flattened tile count
+  const bool stream_ok = num_seqs <= kStreamMaxSeqs && tiles < (1LL << 31);
+  const int path = g_decode_path.load(std::memory_order_relaxed);
+  pl.stream = stream_ok && path == PKV_DECODE_PERSISTENT;
+  const int P = partition_size ? partition_size : kDefaultPartition;
+  pl.np = max_partitions_for(max_context_len, P);
+  if (pl.stream) {
+    long long w = tiles < kStreamMaxWarps ? tiles : kStreamMaxWarps;
+    if (w < 1) w = 1;
+    pl.wcap = (int)((w + kStreamWarps - 1) / kStreamWarps * kStreamWarps);
+    pl.pre_bytes = align256((size_t)(num_seqs + 1) * sizeof(int));
+    pl.need = pl.pre_bytes + (size_t)2 * pl.wcap * pl.gc * (head_dim + 2) * sizeof(float);
+  } else {
+    pl.need = pl.np > 1 ? (size_t)num_seqs * num_heads * pl.np * (head_dim + 2) * sizeof(float) : 0;
+  }
+  return pl;
+}
+
+int sm_count(int dev) {
+  static int counts[kMaxDevices] = {};
+  if (!counts[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 }  // namespace
 
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
@@ -224,13 +276,17 @@ pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
   return PKV_OK;
 }
 
-size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                      int32_t max_context_len, int32_t partition_size) {
-  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0) return 0;
-  const int P = partition_size ? partition_size : kDefaultPartition;
-  const int np = max_partitions_for(max_context_len, P);
-  if (np <= 1) return 0;
-  return (size_t)num_seqs * num_heads * np * (head_dim + 2) * sizeof(float);
+int32_t pkv_set_decode_path(int32_t path) {
+  if (path != PKV_DECODE_AUTO && path != PKV_DECODE_PARTITIONED && path != PKV_DECODE_PERSISTENT) return -1;
+  return g_decode_path.exchange(path);
+}
+
+size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t max_context_len, int32_t partition_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
+      block_size <= 0 || max_context_len < 0 || partition_size < 0)
+    return 0;
+  return make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, partition_size).need;
 }
 
 pkv_status_t paged_attention_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
@@ -258,9 +314,9 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
                 max_context_len, (long long)max_blocks_per_seq * block_size);
   if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
   const int P = partition_size ? partition_size : kDefaultPartition;
-  if (P % block_size || P < block_size || P > kWarpsPerCta * kMaxBlocksPerWarp * block_size)
+  if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
-                block_size, kWarpsPerCta * kMaxBlocksPerWarp * block_size);
+                block_size, kMaxPartitionBlocks * block_size);
   if (num_seqs > 65535 || num_heads > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
   if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
@@ -271,12 +327,11 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
   if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
     return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
 
-  const int np = max_partitions_for(max_context_len, P);
-  const size_t need = paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_context_len, P);
-  if (need) {
-    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", need);
-    if (workspace_bytes < need)
-      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, P);
+  if (pl.need) {
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", pl.need);
+    if (workspace_bytes < pl.need)
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, pl.need);
     if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
   }
 
@@ -293,13 +348,6 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
   p.value_cache = static_cast<const unsigned char*>(value_cache);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
-  if (need) {
-    float* ws = static_cast<float*>(workspace);
-    const size_t rows = (size_t)num_seqs * num_heads * np;
-    p.part_o = ws;
-    p.part_m = ws + rows * head_dim;
-    p.part_l = p.part_m + rows;
-  }
   p.err = err;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.max_blocks_per_seq = max_blocks_per_seq;
@@ -308,16 +356,56 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
   p.group = num_heads / num_kv_heads;
   p.num_blocks = num_blocks;
   p.partition_size = P;
-  p.max_partitions = np;
+  p.max_partitions = pl.np;
   p.ctx_limit = max_context_len;
 
-  const int G = p.group;
-  if (G >= 2 && G <= 8) {
-    CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof kmap);
+  memset(&vmap, 0, sizeof vmap);
+  if (pl.mma) {
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
     if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
         !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+  }
+
+  if (pl.stream) {
+    const int sms = sm_count(dev);
+    if (!sms) return fail(PKV_ERR_CUDA, "could not read the SM count of device %d", dev);
+    int occ = 0;
+    e = dtype == PKV_F16 ? decode_stream_occupancy_f16(head_dim, block_size, pl.mma, num_seqs, &occ)
+                         : decode_stream_occupancy_bf16(head_dim, block_size, pl.mma, num_seqs, &occ);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the persistent decode kernel");
+    if (occ < 1) occ = 1;
+    int grid = sms * occ;
+    if (grid > pl.wcap / kStreamWarps) grid = pl.wcap / kStreamWarps;
+    StreamParams sp{};
+    sp.p = p;
+    sp.num_seqs = num_seqs;
+    sp.ng = pl.ng;
+    sp.gc = pl.gc;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    sp.pre_out = reinterpret_cast<int*>(ws);
+    sp.slot_o = reinterpret_cast<float*>(ws + pl.pre_bytes);
+    sp.slot_m = sp.slot_o + (size_t)2 * pl.wcap * pl.gc * head_dim;
+    sp.slot_l = sp.slot_m + (size_t)2 * pl.wcap * pl.gc;
+    e = dtype == PKV_F16 ? decode_stream_f16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream)
+                         : decode_stream_bf16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "persistent decode kernel launch");
+    e = dtype == PKV_F16 ? stream_reduce_f16(sp, head_dim, grid * kStreamWarps, stream)
+                         : stream_reduce_bf16(sp, head_dim, grid * kStreamWarps, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+    return PKV_OK;
+  }
+
+  if (pl.need) {
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_seqs * num_heads * pl.np;
+    p.part_o = ws;
+    p.part_m = ws + rows * head_dim;
+    p.part_l = p.part_m + rows;
+  }
+  if (pl.mma) {
     e = dtype == PKV_F16 ? decode_mma_f16(p, kmap, vmap, head_dim, block_size, num_seqs, stream)
                          : decode_mma_bf16(p, kmap, vmap, head_dim, block_size, num_seqs, stream);
   } else {
@@ -326,18 +414,18 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
-  if (np > 1) {
+  if (pl.np > 1) {
     const dim3 grid(num_heads, num_seqs);
     const int threads = head_dim;
-    const size_t shm = (size_t)np * sizeof(float);
+    const size_t shm = (size_t)pl.np * sizeof(float);
     if (dtype == PKV_F16) {
       pkv_reduce_kernel<__half><<<grid, threads, shm, stream>>>(static_cast<__half*>(out), p.part_o, p.part_m,
-                                                                p.part_l, context_lens, num_heads, head_dim, P, np,
-                                                                p.ctx_limit);
+                                                                p.part_l, context_lens, num_heads, head_dim, P,
+                                                                pl.np, p.ctx_limit);
     } else {
       pkv_reduce_kernel<__nv_bfloat16><<<grid, threads, shm, stream>>>(
           static_cast<__nv_bfloat16*>(out), p.part_o, p.part_m, p.part_l, context_lens, num_heads, head_dim, P,
-          np, p.ctx_limit);
+          pl.np, p.ctx_limit);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");

@@ -16,6 +16,26 @@
 namespace pkv {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4  // warps per decode CTA (build-time tuning knob)
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 1  // __launch_bounds__ minimum CTAs per SM (build-time tuning knob)
+#endif
+#ifndef PKV_GRID_HEAD_FASTEST
+#define PKV_GRID_HEAD_FASTEST 0  // partitioned grid: 1 = blockIdx.x walks heads (build-time tuning knob)
+#endif
+#ifndef PKV_PROXY_FENCE
+// 1: fence.proxy.async before every stage refill (build-time knob). With 0 the
+// fence runs only where generic stores went into the stage (tail zeroing); reads
+// of a stage have all returned their values before the refill is issued.
+#define PKV_PROXY_FENCE 0
+#endif
+constexpr int kDecodeWarps = PKV_DECODE_WARPS;
+// A warp keeps one physical block id per lane, so a partition spans at most
+// kDecodeWarps * 32 blocks.
+constexpr int kMaxPartitionBlocks = kDecodeWarps * 32;
 // Upper bound on one wait for a bulk copy, in SM clock cycles (about 1 s at 2 GHz).
 constexpr long long kWaitLimitCycles = 2000000000ll;
 

@@ -1,7 +1,7 @@
-// Grouped-query decode attention over the paged KV pool on the tensor cores: one
-// CTA per (context partition, kv head, sequence) serving all G = H / Hkv query
-// heads of that kv head, so each KV tile is read from HBM once per group
-// ("Sparse Computation and Memory Management ...": GQA, 32 Q heads / 8 KV heads).
+// Grouped-query decode attention over the paged KV pool on the tensor cores,
+// serving all G = H / Hkv query heads of one kv head together, so each KV tile
+// is read from HBM once per group ("Sparse Computation and Memory Management
+// ...": GQA, 32 Q heads / 8 KV heads).
 //
 // With G >= 2 the per-block work is a dense contraction: for a 16-token slice
 // of a block, S^T[16 x G] = K[16 x D] . Q^T[D x G] and O^T[D x G] += V^T[D x 16] .
@@ -11,52 +11,182 @@
 // memory. P is rounded to the cache dtype for the PV product, and the running
 // sum l adds the same rounded values, so weights and normaliser agree.
 //
-// Data movement: per-warp rings as in the CUDA-core kernel, but each tile comes
-// in through a 2D tensor map in boxes of 64 head dims x block_size tokens with
-// the 128-byte swizzle, which makes every ldmatrix phase conflict-free.
+// Tiles come in through a 2D tensor map in boxes of 64 head dims x block_size
+// tokens with the 128-byte swizzle, which makes every ldmatrix phase
+// conflict-free. MmaTile holds the per-tile arithmetic shared by the grid
+// kernel below (one CTA per (partition, kv head, sequence), per-warp rings) and
+// the persistent kernel (pkv_decode_stream.cuh).
 #pragma once
 
 #include "pkv_common.cuh"
 
 namespace pkv {
 
-template <int D, int BS, int NW, int SPW>
-struct MmaShape {
-  static constexpr int NBOX = D / 64;         // swizzled boxes per tile (64 dims x BS rows each)
-  static constexpr int BOXB = BS * 128;       // bytes of one box
-  static constexpr int TILE = NBOX * BOXB;    // = BS * D * 2
-  static constexpr int STAGE = 2 * TILE;      // K tile + V tile
-  static constexpr int RING = NW * SPW * STAGE;
-  static constexpr int BARS = RING;
-  static constexpr int SMEM_USED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
-  static constexpr int SMEM = SMEM_USED + 1024;  // slack to align the ring to 1024 bytes
-  static constexpr int CH = BS >= 16 ? BS / 16 : 1;  // 16-token slices per block
-  static constexpr int ROWS = BS >= 16 ? 16 : BS;    // real rows per slice
-  static constexpr int KT = D / 16;                  // k-steps of the score MMA / m-tiles of PV
-  static constexpr int RED_PER_WARP = (8 * D + 16) * 4;
-  static_assert(TILE == BS * D * 2, "tile bytes");
-  static_assert(BOXB % 1024 == 0, "swizzle atoms need 1024-byte aligned boxes");
-  static_assert(RED_PER_WARP <= SPW * STAGE, "reduction scratch reuses the warp's ring");
-};
-
 // Byte offset of 16-byte piece `piece` (of D/8) of token row `t` inside a tile
-// stored as NBOX swizzled boxes.
+// stored as D/64 swizzled boxes of BS rows x 128 bytes.
 template <int BS>
 __device__ __forceinline__ int swz_offset(int t, int piece) {
   const int box = piece >> 3, chunk = piece & 7;
   return box * (BS * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
 }
 
+template <typename T, int D, int BS>
+struct MmaTile {
+  static constexpr int NBOX = D / 64;       // swizzled boxes per tile (64 dims x BS rows each)
+  static constexpr int BOXB = BS * 128;     // bytes of one box
+  static constexpr int TILE = NBOX * BOXB;  // = BS * D * 2
+  static constexpr int CH = BS >= 16 ? BS / 16 : 1;  // 16-token slices per block
+  static constexpr int KT = D / 16;                  // k-steps of the score MMA / m-tiles of PV
+  static_assert(TILE == BS * D * 2, "tile bytes");
+  static_assert(BOXB % 1024 == 0, "swizzle atoms need 1024-byte aligned boxes");
+
+  // Q^T as the B operand of the score MMA: lane holds head n = lane / 4,
+  // dims 2 (lane % 4) + {0, 1} (+ 8) of each 16-dim k-step. Heads >= G are zero.
+  // `q` points at the group's first query row (G rows of D), global or shared.
+  static __device__ __forceinline__ void load_qb(uint32_t (&qb)[KT][2], const T* q, int G, int lane) {
+    const int n_head = lane >> 2, kq = (lane & 3) * 2;
+    const T* qr = q + n_head * D;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      if (n_head < G) {
+        qb[kk][0] = *reinterpret_cast<const uint32_t*>(qr + kk * 16 + kq);
+        qb[kk][1] = *reinterpret_cast<const uint32_t*>(qr + kk * 16 + 8 + kq);
+      } else {
+        qb[kk][0] = 0u;
+        qb[kk][1] = 0u;
+      }
+    }
+  }
+
+  // Fold one (block, kv head) tile into the lane's running state for its two
+  // heads (columns j0 = 2 (lane % 4), j0 + 1): tokens 0 .. nvalid-1 take part.
+  // Zeroes the value rows past nvalid in shared memory (the stage then needs a
+  // proxy fence before the copy engine refills it).
+  static __device__ __forceinline__ void run(unsigned char* Ks, unsigned char* Vs, int nvalid,
+                                             const uint32_t (&qb)[KT][2], int lane, float sl2, float& m0,
+                                             float& m1, float& l0, float& l1, float (&acc)[KT][4]) {
+    const int mi = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix
+    const int r8 = lane & 7;   // row inside that matrix
+    const int r0 = lane >> 2;  // accumulator rows r0 and r0 + 8
+    if (nvalid < BS) {
+      // value rows past the context may hold anything (even NaN): zero them so
+      // that their zero weights contribute exactly zero
+      const int nz = (BS - nvalid) * (D / 8);
+      for (int idx = lane; idx < nz; idx += 32) {
+        const int t = nvalid + idx / (D / 8), piece = idx % (D / 8);
+        *reinterpret_cast<uint4*>(Vs + swz_offset<BS>(t, piece)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      if (c * 16 < nvalid) {
+        // scores S^T[token][head] for 16 tokens, in two accumulation chains
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          float sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+          const int rr = r8 + ((mi & 1) << 3);  // A rows 0..15
+          const int t = BS >= 16 ? c * 16 + rr : (rr & (BS - 1));
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            uint32_t a[4];
+            ldmatrix_x4(a, Ks + swz_offset<BS>(t, kk * 2 + (mi >> 1)));
+            if (kk & 1) {
+              Mma<T>::run(sacc2, a, qb[kk][0], qb[kk][1]);
+            } else {
+              Mma<T>::run(sacc, a, qb[kk][0], qb[kk][1]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
+        }
+        const int ta = c * 16 + r0, tb = ta + 8;
+        const bool va = (BS >= 16 || r0 < BS) && ta < nvalid;
+        const bool vb = BS >= 16 && tb < nvalid;
+        const float x00 = va ? sacc[0] * sl2 : -INFINITY;
+        const float x01 = va ? sacc[1] * sl2 : -INFINITY;
+        const float x10 = vb ? sacc[2] * sl2 : -INFINITY;
+        const float x11 = vb ? sacc[3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - mn0), fast_exp2(x01 - mn1));
+        const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - mn0), fast_exp2(x11 - mn1));
+        const float2 fa = Elem<T>::to_float2(pa), fb = Elem<T>::to_float2(pb);
+        float rs0 = fa.x + fb.x, rs1 = fa.y + fb.y;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          rs0 += __shfl_xor_sync(kFull, rs0, o);
+          rs1 += __shfl_xor_sync(kFull, rs1, o);
+        }
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          acc[mt][0] *= al0;
+          acc[mt][1] *= al1;
+          acc[mt][2] *= al0;
+          acc[mt][3] *= al1;
+        }
+        // P^T as the B operand of the PV MMA: transpose the 8x8 score fragments
+        const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
+        {
+          const int tr = r8 + ((mi >> 1) << 3);  // stored V rows 0..15
+          const int t = BS >= 16 ? c * 16 + tr : (tr & (BS - 1));
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, Vs + swz_offset<BS>(t, mt * 2 + (mi & 1)));
+            Mma<T>::run(acc[mt], a, b0, b1);
+          }
+        }
+      }
+    }
+  }
+
+  // Issue the tensor-map copies of one (block, kv head) tile pair into a stage.
+  static __device__ __forceinline__ void issue_tiles(unsigned char* st, const CUtensorMap* kmap,
+                                                     const CUtensorMap* vmap, int y, uint64_t* bar) {
+#pragma unroll
+    for (int b = 0; b < NBOX; ++b) {
+      tma_load_2d(st + b * BOXB, kmap, 64 * b, y, bar);
+      tma_load_2d(st + TILE + b * BOXB, vmap, 64 * b, y, bar);
+    }
+  }
+};
+
+template <int D, int BS, int NW, int SPW>
+struct MmaShape {
+  static constexpr int TILE = BS * D * 2;
+  static constexpr int STAGE = 2 * TILE;  // K tile + V tile
+  static constexpr int RING = NW * SPW * STAGE;
+  static constexpr int BARS = RING;
+  static constexpr int SMEM_USED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
+  static constexpr int SMEM = SMEM_USED + 1024;  // slack to align the ring to 1024 bytes
+  static constexpr int RED_PER_WARP = (8 * D + 16) * 4;
+  static_assert(RED_PER_WARP <= SPW * STAGE, "reduction scratch reuses the warp's ring");
+};
+
 template <typename T, int D, int BS, int NW, int SPW>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
     pkv_decode_gqa_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap) {
   using Sh = MmaShape<D, BS, NW, SPW>;
+  using Tile = MmaTile<T, D, BS>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int part = PKV_GRID_HEAD_FASTEST ? blockIdx.y : blockIdx.x;
+  const int kvh = PKV_GRID_HEAD_FASTEST ? blockIdx.x : blockIdx.y;
+  const int s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = clamp_context(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -102,20 +232,17 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncwarp();
 
+  unsigned zeroed = 0;  // stages whose tail rows were zeroed since their last refill
   auto issue = [&](int i) {
     const int phys = __shfl_sync(kFull, my_phys, i);
     if (lane == 0) {
       uint64_t* bar = bars + (i % SPW);
       unsigned char* st = ring + (i % SPW) * Sh::STAGE;
       if (phys >= 0) {
-        fence_proxy_async_smem();
+        // generic stores (tail zeroing) into this stage must be ordered before the copy's writes
+        if (PKV_PROXY_FENCE || ((zeroed >> (i % SPW)) & 1u)) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, Sh::STAGE);
-        const int y = (phys * p.num_kv_heads + kvh) * BS;  // first row of the tile
-#pragma unroll
-        for (int b = 0; b < Sh::NBOX; ++b) {
-          tma_load_2d(st + b * Sh::BOXB, &kmap, 64 * b, y, bar);
-          tma_load_2d(st + Sh::TILE + b * Sh::BOXB, &vmap, 64 * b, y, bar);
-        }
+        Tile::issue_tiles(st, &kmap, &vmap, (phys * p.num_kv_heads + kvh) * BS, bar);
       } else {
         mbar_arrive(bar);
       }
@@ -125,34 +252,14 @@ __global__ void __launch_bounds__(NW * 32)
   for (int i = 0; i < nfirst; ++i) issue(i);
   int issued = nfirst;
 
-  // Q^T as the B operand of the score MMA: lane holds head n = lane / 4,
-  // dims 2 (lane % 4) + {0, 1} (+ 8) of each 16-dim k-step. Heads >= G are zero.
-  const int n_head = lane >> 2, kq = (lane & 3) * 2;
-  uint32_t qb[Sh::KT][2];
-  {
-    const T* q = reinterpret_cast<const T*>(p.query) + (row0 + n_head) * D;
-#pragma unroll
-    for (int kk = 0; kk < Sh::KT; ++kk) {
-      if (n_head < G) {
-        qb[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(q + kk * 16 + kq));
-        qb[kk][1] = __ldg(reinterpret_cast<const uint32_t*>(q + kk * 16 + 8 + kq));
-      } else {
-        qb[kk][0] = 0u;
-        qb[kk][1] = 0u;
-      }
-    }
-  }
+  uint32_t qb[Tile::KT][2];
+  Tile::load_qb(qb, reinterpret_cast<const T*>(p.query) + row0 * D, G, lane);
 
   // running state of this lane's two heads (columns j0 = 2 (lane % 4), j0 + 1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float acc[Sh::KT][4];
+  float acc[Tile::KT][4];
 #pragma unroll
-  for (int mt = 0; mt < Sh::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-  const int mi = lane >> 3;       // which 8x8 matrix this lane addresses in ldmatrix
-  const int r8 = lane & 7;        // row inside that matrix
-  const int r0 = lane >> 2;       // accumulator rows r0 and r0 + 8
-  const float sl2 = p.scale_log2;
+  for (int mt = 0; mt < Tile::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
   int failed_at = -1;
   for (int i = 0; i < nmine; ++i) {
@@ -165,87 +272,15 @@ __global__ void __launch_bounds__(NW * 32)
     }
     if (phys >= 0) {
       unsigned char* Ks = ring + k * Sh::STAGE;
-      unsigned char* Vs = Ks + Sh::TILE;
       const int lb = warp + NW * i;
       const int nvalid = min(BS, tok1 - (blk0 + lb) * BS);
-      if (nvalid < BS) {
-        // value rows past the context may hold anything (even NaN): zero them so
-        // that their zero weights contribute exactly zero
-        const int nz = (BS - nvalid) * (D / 8);
-        for (int idx = lane; idx < nz; idx += 32) {
-          const int t = nvalid + idx / (D / 8), piece = idx % (D / 8);
-          *reinterpret_cast<uint4*>(Vs + swz_offset<BS>(t, piece)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        __syncwarp();
-      }
-#pragma unroll
-      for (int c = 0; c < Sh::CH; ++c) {
-        if (c * 16 < nvalid) {
-          // scores S^T[token][head] for 16 tokens
-          float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-          {
-            const int rr = r8 + ((mi & 1) << 3);  // A rows 0..15
-            const int t = BS >= 16 ? c * 16 + rr : (rr & (BS - 1));
-#pragma unroll
-            for (int kk = 0; kk < Sh::KT; ++kk) {
-              uint32_t a[4];
-              ldmatrix_x4(a, Ks + swz_offset<BS>(t, kk * 2 + (mi >> 1)));
-              Mma<T>::run(sacc, a, qb[kk][0], qb[kk][1]);
-            }
-          }
-          const int ta = c * 16 + r0, tb = ta + 8;
-          const bool va = (BS >= 16 || r0 < BS) && ta < nvalid;
-          const bool vb = BS >= 16 && tb < nvalid;
-          const float x00 = va ? sacc[0] * sl2 : -INFINITY;
-          const float x01 = va ? sacc[1] * sl2 : -INFINITY;
-          const float x10 = vb ? sacc[2] * sl2 : -INFINITY;
-          const float x11 = vb ? sacc[3] * sl2 : -INFINITY;
-          float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-          }
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-          const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - mn0), fast_exp2(x01 - mn1));
-          const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - mn0), fast_exp2(x11 - mn1));
-          const float2 fa = Elem<T>::to_float2(pa), fb = Elem<T>::to_float2(pb);
-          float rs0 = fa.x + fb.x, rs1 = fa.y + fb.y;
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            rs0 += __shfl_xor_sync(kFull, rs0, o);
-            rs1 += __shfl_xor_sync(kFull, rs1, o);
-          }
-          l0 = l0 * al0 + rs0;
-          l1 = l1 * al1 + rs1;
-          m0 = mn0;
-          m1 = mn1;
-#pragma unroll
-          for (int mt = 0; mt < Sh::KT; ++mt) {
-            acc[mt][0] *= al0;
-            acc[mt][1] *= al1;
-            acc[mt][2] *= al0;
-            acc[mt][3] *= al1;
-          }
-          // P^T as the B operand of the PV MMA: transpose the 8x8 score fragments
-          const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
-          {
-            const int tr = r8 + ((mi >> 1) << 3);  // stored V rows 0..15
-            const int t = BS >= 16 ? c * 16 + tr : (tr & (BS - 1));
-#pragma unroll
-            for (int mt = 0; mt < Sh::KT; ++mt) {
-              uint32_t a[4];
-              ldmatrix_x4_trans(a, Vs + swz_offset<BS>(t, mt * 2 + (mi & 1)));
-              Mma<T>::run(acc[mt], a, b0, b1);
-            }
-          }
-        }
-      }
+      Tile::run(Ks, Ks + Sh::TILE, nvalid, qb, lane, p.scale_log2, m0, m1, l0, l1, acc);
+      if (nvalid < BS) zeroed |= 1u << k;
     }
     __syncwarp();
     if (i + SPW < nmine) {
       issue(i + SPW);
+      zeroed &= ~(1u << k);
       ++issued;
     }
   }
@@ -256,16 +291,16 @@ __global__ void __launch_bounds__(NW * 32)
     m0 = m1 = -INFINITY;
     l0 = l1 = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < Sh::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    for (int mt = 0; mt < Tile::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   }
 
   // merge the warps: each warp writes [head][D] accumulators, m, l into its own ring slice
   float* red = reinterpret_cast<float*>(ring);
   float* red_m = red + 8 * D;
   float* red_l = red_m + 8;
-  const int j0 = (lane & 3) * 2;
+  const int j0 = (lane & 3) * 2, r0 = lane >> 2;
 #pragma unroll
-  for (int mt = 0; mt < Sh::KT; ++mt) {
+  for (int mt = 0; mt < Tile::KT; ++mt) {
     const int d0 = mt * 16 + r0;
     red[j0 * D + d0] = acc[mt][0];
     red[(j0 + 1) * D + d0] = acc[mt][1];
@@ -307,17 +342,21 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
+#ifndef PKV_MMA_RING_BYTES
+#define PKV_MMA_RING_BYTES (64 * 1024)  // ring bytes per CTA (build-time tuning knob)
+#endif
+
 template <int D, int BS>
 constexpr int mma_stages() {
   constexpr int stage = 2 * BS * D * 2;
-  constexpr int spw = (96 * 1024) / (4 * stage);
-  return spw < 2 ? 2 : (spw > 6 ? 6 : spw);
+  constexpr int spw = (PKV_MMA_RING_BYTES) / (kDecodeWarps * stage);
+  return spw < 1 ? 1 : (spw > 6 ? 6 : spw);
 }
 
 template <typename T, int D, int BS>
 cudaError_t launch_decode_gqa_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   int num_seqs, cudaStream_t stream) {
-  constexpr int NW = 4;
+  constexpr int NW = kDecodeWarps;
   constexpr int SPW = mma_stages<D, BS>();
   using Sh = MmaShape<D, BS, NW, SPW>;
   auto kern = pkv_decode_gqa_mma_kernel<T, D, BS, NW, SPW>;
@@ -331,7 +370,8 @@ cudaError_t launch_decode_gqa_mma(const DecodeParams& p, const CUtensorMap& kmap
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const dim3 grid(p.max_partitions, p.num_kv_heads, num_seqs);
+  const dim3 grid(PKV_GRID_HEAD_FASTEST ? p.num_kv_heads : p.max_partitions,
+                  PKV_GRID_HEAD_FASTEST ? p.max_partitions : p.num_kv_heads, num_seqs);
   kern<<<grid, NW * 32, Sh::SMEM, stream>>>(p, kmap, vmap);
   return cudaGetLastError();
 }

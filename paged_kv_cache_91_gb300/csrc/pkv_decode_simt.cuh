@@ -1,30 +1,28 @@
-// Decode attention over the paged KV pool on the CUDA cores: one CTA per
-// (context partition, query head, sequence). Used for MHA (one query head per kv
-// head, where the per-block work is a matrix-vector product) and as the general
-// path for group sizes the tensor-core kernel does not take.
+// Decode attention over the paged KV pool on the CUDA cores: used for MHA (one
+// query head per kv head, where the per-block work is a matrix-vector product)
+// and as the general path for group sizes the tensor-core kernel does not take.
 //
 // Method: "KV Cache와 PagedAttention 완전 해부", 부록 -- walk the sequence's
 // blocks through the block table, score each block's keys, update a running
 // softmax, accumulate the weighted values; "vLLM: LLM 서빙 메모리 최적화의
-// 교과서", eq. (4). The context is cut into partitions of partition_size tokens;
-// a single-partition context writes its output here, longer ones write
-// (m, l, o) partials that pkv_reduce_kernel merges.
+// 교과서", eq. (4).
 //
-// Data movement: each warp owns a private ring of SPW stages. A stage holds the
-// K tile and the V tile of one (physical block, kv head) pair, each one
-// contiguous block_size x head_dim run in the pool, brought in by two linear
-// bulk copies (TMA engine) that complete on the stage's mbarrier. A warp
-// consumes its blocks round-robin (warp w takes local blocks w, w+NW, ...) and
-// refills the stage it just consumed, so up to NW * SPW tiles per CTA are in
-// flight without any cross-warp synchronisation in the main loop.
+// SimtTile holds the per-tile arithmetic shared by the grid kernel below and the
+// persistent kernel (pkv_decode_stream.cuh). The grid kernel runs one CTA per
+// (context partition, query head, sequence): each warp owns a private ring of
+// SPW stages, each stage the K tile and V tile of one (physical block, kv head)
+// pair brought in by two linear bulk copies (TMA engine) completing on the
+// stage's mbarrier; warp w takes the partition's blocks w, w+NW, ... and refills
+// the stage it just consumed. A single-partition context writes its output
+// directly; longer ones write (m, l, o) partials that pkv_reduce_kernel merges.
 #pragma once
 
 #include "pkv_common.cuh"
 
 namespace pkv {
 
-template <int D, int BS, int NW, int SPW>
-struct SimtShape {
+template <int D, int BS>
+struct SimtTileShape {
   static constexpr int TPC = BS < 16 ? BS : 16;  // tokens per score chunk
   static constexpr int CPB = BS / TPC;           // chunks per block
   static constexpr int LPT = 32 / TPC;           // lanes per token in the score pass
@@ -32,11 +30,6 @@ struct SimtShape {
   static constexpr int NCH = DPL / 8;            // 16-byte pieces per lane in the score pass
   static constexpr int DPV = D / 32;             // head dims per lane in the value pass
   static constexpr int TILE = BS * D * 2;        // bytes of one (block, kv head) tile
-  static constexpr int STAGE = 2 * TILE;         // K tile + V tile
-  static constexpr int RING = NW * SPW * STAGE;
-  static constexpr int BARS = RING;  // mbarriers follow the ring
-  static constexpr int RED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
-  static constexpr int SMEM = RED + NW * (D + 2) * 4;
   static_assert(NCH == 2 || NCH == 4 || NCH == 8, "score-pass piece count");
   static_assert(DPV == 2 || DPV == 4, "value-pass width");
 };
@@ -58,12 +51,134 @@ __device__ __forceinline__ int qk_rotation(int lane) {
   }
 }
 
+template <typename T, int D, int BS>
+struct SimtTile {
+  using Sh = SimtTileShape<D, BS>;
+
+  // This lane's slice of one query row for the score pass, scaled into the
+  // base-2 domain and stored in rotated piece order. `q` is the row's first
+  // element, in global or shared memory, 16-byte aligned.
+  static __device__ __forceinline__ void load_q(float (&qreg)[Sh::DPL], const T* q, int lane, float scale_log2) {
+    const int pt = lane % Sh::LPT;
+    const int rot = qk_rotation<Sh::LPT, Sh::NCH>(lane);
+#pragma unroll
+    for (int i = 0; i < Sh::NCH; ++i) {
+      const int piece = (i + rot) & (Sh::NCH - 1);
+      const uint4 raw = *reinterpret_cast<const uint4*>(q + pt * Sh::DPL + piece * 8);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = Elem<T>::to_float2(w[e]);
+        qreg[i * 8 + 2 * e] = f.x * scale_log2;
+        qreg[i * 8 + 2 * e + 1] = f.y * scale_log2;
+      }
+    }
+  }
+
+  // Fold one (block, kv head) tile into the warp's running state (m, l, acc):
+  // tokens 0 .. nvalid-1 of the tile take part, the rest are never read.
+  static __device__ __forceinline__ void run(const unsigned char* Ks, const unsigned char* Vs, int nvalid,
+                                             const float (&qreg)[Sh::DPL], int lane, float& m, float& l,
+                                             float (&acc)[Sh::DPV]) {
+    const int tl = lane / Sh::LPT, pt = lane % Sh::LPT;
+    const int rot = qk_rotation<Sh::LPT, Sh::NCH>(lane);
+#pragma unroll
+    for (int c = 0; c < Sh::CPB; ++c) {
+      if (c * Sh::TPC < nvalid) {
+        // scores of this chunk's tokens: LPT lanes per token, fp32 accumulation
+        const unsigned char* krow = Ks + (c * Sh::TPC + tl) * (D * 2) + pt * (Sh::DPL * 2);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < Sh::NCH; ++i2) {
+          const int piece = (i2 + rot) & (Sh::NCH - 1);
+          const uint4 raw = *reinterpret_cast<const uint4*>(krow + piece * 16);
+          const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
+          const float2 f2 = Elem<T>::to_float2(raw.z), f3 = Elem<T>::to_float2(raw.w);
+          a0 = fmaf(qreg[i2 * 8 + 0], f0.x, a0);
+          a1 = fmaf(qreg[i2 * 8 + 1], f0.y, a1);
+          a2 = fmaf(qreg[i2 * 8 + 2], f1.x, a2);
+          a3 = fmaf(qreg[i2 * 8 + 3], f1.y, a3);
+          a0 = fmaf(qreg[i2 * 8 + 4], f2.x, a0);
+          a1 = fmaf(qreg[i2 * 8 + 5], f2.y, a1);
+          a2 = fmaf(qreg[i2 * 8 + 6], f3.x, a2);
+          a3 = fmaf(qreg[i2 * 8 + 7], f3.y, a3);
+        }
+        float sc = (a0 + a1) + (a2 + a3);
+#pragma unroll
+        for (int o = Sh::LPT / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
+        const int nv = min(Sh::TPC, nvalid - c * Sh::TPC);
+        sc = tl < nv ? sc : -INFINITY;  // tokens past the context do not take part
+
+        // running softmax update; the LPT lanes of a token hold the same score,
+        // so the reductions run over the TPC distinct tokens only
+        float mx = sc;
+#pragma unroll
+        for (int o = Sh::LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        const float mnew = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - mnew);
+        const float pr = fast_exp2(sc - mnew);
+        float ps = pr;
+#pragma unroll
+        for (int o = Sh::LPT; o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
+        l = l * alpha + ps;
+        m = mnew;
+#pragma unroll
+        for (int e = 0; e < Sh::DPV; ++e) acc[e] *= alpha;
+
+        // weighted values: lane owns DPV consecutive head dims. A full chunk runs
+        // without per-token branches so its loads can all be in flight at once;
+        // a partial chunk never reads rows past the context.
+        const unsigned char* vrow = Vs + (c * Sh::TPC) * (D * 2) + lane * (Sh::DPV * 2);
+        if (nv == Sh::TPC) {
+#pragma unroll
+          for (int tt = 0; tt < Sh::TPC; ++tt) pv_row(acc, __shfl_sync(kFull, pr, tt * Sh::LPT), vrow + tt * (D * 2));
+        } else {
+#pragma unroll
+          for (int tt = 0; tt < Sh::TPC; ++tt) {
+            const float w = __shfl_sync(kFull, pr, tt * Sh::LPT);
+            if (tt < nv) pv_row(acc, w, vrow + tt * (D * 2));
+          }
+        }
+      }
+    }
+  }
+
+  // acc[e] += w * V[row][lane dims e]
+  static __device__ __forceinline__ void pv_row(float (&acc)[Sh::DPV], float w, const unsigned char* v) {
+    if constexpr (Sh::DPV == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(v);
+      const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
+      acc[0] = fmaf(w, f0.x, acc[0]);
+      acc[1] = fmaf(w, f0.y, acc[1]);
+      acc[2] = fmaf(w, f1.x, acc[2]);
+      acc[3] = fmaf(w, f1.y, acc[3]);
+    } else {
+      const uint32_t raw = *reinterpret_cast<const uint32_t*>(v);
+      const float2 f0 = Elem<T>::to_float2(raw);
+      acc[0] = fmaf(w, f0.x, acc[0]);
+      acc[1] = fmaf(w, f0.y, acc[1]);
+    }
+  }
+};
+
+template <int D, int BS, int NW, int SPW>
+struct SimtShape : SimtTileShape<D, BS> {
+  static constexpr int STAGE = 2 * SimtTileShape<D, BS>::TILE;  // K tile + V tile
+  static constexpr int RING = NW * SPW * STAGE;
+  static constexpr int BARS = RING;  // mbarriers follow the ring
+  static constexpr int RED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
+  static constexpr int SMEM = RED + NW * (D + 2) * 4;
+};
+
 template <typename T, int D, int BS, int NW, int SPW>
-__global__ void __launch_bounds__(NW * 32) pkv_decode_simt_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_kernel(const DecodeParams p) {
   using Sh = SimtShape<D, BS, NW, SPW>;
+  using Tile = SimtTile<T, D, BS>;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int part = PKV_GRID_HEAD_FASTEST ? blockIdx.y : blockIdx.x;
+  const int h = PKV_GRID_HEAD_FASTEST ? blockIdx.x : blockIdx.y;
+  const int s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = h / p.group;
   const int ctx = clamp_context(p, s, part == 0 && h == 0 && threadIdx.x == 0);
@@ -114,7 +229,7 @@ __global__ void __launch_bounds__(NW * 32) pkv_decode_simt_kernel(const DecodePa
       uint64_t* bar = bars + (i % SPW);
       unsigned char* st = ring + (i % SPW) * Sh::STAGE;
       if (phys >= 0) {
-        fence_proxy_async_smem();  // earlier reads of this stage before the copy's writes
+        if (PKV_PROXY_FENCE) fence_proxy_async_smem();  // earlier reads of this stage before the copy's writes
         mbar_arrive_expect_tx(bar, Sh::STAGE);
         const size_t off = (size_t)phys * block_stride + head_off;
         bulk_g2s(st, p.key_cache + off, Sh::TILE, bar);
@@ -128,25 +243,8 @@ __global__ void __launch_bounds__(NW * 32) pkv_decode_simt_kernel(const DecodePa
   for (int i = 0; i < nfirst; ++i) issue(i);
   int issued = nfirst;
 
-  // this lane's slice of q for the score pass, in base-2 units, in rotated piece order
-  const int tl = lane / Sh::LPT, pt = lane % Sh::LPT;
-  const int rot = qk_rotation<Sh::LPT, Sh::NCH>(lane);
   float qreg[Sh::DPL];
-  {
-    const T* q = reinterpret_cast<const T*>(p.query) + out_row * D + pt * Sh::DPL;
-#pragma unroll
-    for (int i = 0; i < Sh::NCH; ++i) {
-      const int piece = (i + rot) & (Sh::NCH - 1);
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q + piece * 8));
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = Elem<T>::to_float2(w[e]);
-        qreg[i * 8 + 2 * e] = f.x * p.scale_log2;
-        qreg[i * 8 + 2 * e + 1] = f.y * p.scale_log2;
-      }
-    }
-  }
+  Tile::load_q(qreg, reinterpret_cast<const T*>(p.query) + out_row * D, lane, p.scale_log2);
 
   float m = -INFINITY, l = 0.f;
   float acc[Sh::DPV];
@@ -164,68 +262,9 @@ __global__ void __launch_bounds__(NW * 32) pkv_decode_simt_kernel(const DecodePa
     }
     if (phys >= 0) {
       const unsigned char* Ks = ring + k * Sh::STAGE;
-      const unsigned char* Vs = Ks + Sh::TILE;
       const int lb = warp + NW * i;
       const int nvalid = min(BS, tok1 - (blk0 + lb) * BS);
-#pragma unroll
-      for (int c = 0; c < Sh::CPB; ++c) {
-        if (c * Sh::TPC < nvalid) {
-          // scores of this chunk's tokens: LPT lanes per token, fp32 accumulation
-          const unsigned char* krow = Ks + (c * Sh::TPC + tl) * (D * 2) + pt * (Sh::DPL * 2);
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int i2 = 0; i2 < Sh::NCH; ++i2) {
-            const int piece = (i2 + rot) & (Sh::NCH - 1);
-            const uint4 raw = *reinterpret_cast<const uint4*>(krow + piece * 16);
-            const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
-            const float2 f2 = Elem<T>::to_float2(raw.z), f3 = Elem<T>::to_float2(raw.w);
-            a0 = fmaf(qreg[i2 * 8 + 0], f0.x, a0);
-            a1 = fmaf(qreg[i2 * 8 + 1], f0.y, a1);
-            a2 = fmaf(qreg[i2 * 8 + 2], f1.x, a2);
-            a3 = fmaf(qreg[i2 * 8 + 3], f1.y, a3);
-            a0 = fmaf(qreg[i2 * 8 + 4], f2.x, a0);
-            a1 = fmaf(qreg[i2 * 8 + 5], f2.y, a1);
-            a2 = fmaf(qreg[i2 * 8 + 6], f3.x, a2);
-            a3 = fmaf(qreg[i2 * 8 + 7], f3.y, a3);
-          }
-          float sc = (a0 + a1) + (a2 + a3);
-#pragma unroll
-          for (int o = Sh::LPT / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
-          const int nv = min(Sh::TPC, nvalid - c * Sh::TPC);
-          sc = tl < nv ? sc : -INFINITY;  // tokens past the context do not take part
-
-          // running softmax update
-          const float mnew = fmaxf(m, warp_max(sc));
-          const float alpha = fast_exp2(m - mnew);
-          const float pr = fast_exp2(sc - mnew);
-          l = l * alpha + warp_sum(pt == 0 ? pr : 0.f);
-          m = mnew;
-#pragma unroll
-          for (int e = 0; e < Sh::DPV; ++e) acc[e] *= alpha;
-
-          // weighted values: lane owns DPV consecutive head dims
-          const unsigned char* vrow = Vs + (c * Sh::TPC) * (D * 2) + lane * (Sh::DPV * 2);
-#pragma unroll
-          for (int tt = 0; tt < Sh::TPC; ++tt) {
-            const float w = __shfl_sync(kFull, pr, tt * Sh::LPT);
-            if (tt < nv) {
-              if constexpr (Sh::DPV == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(vrow + tt * (D * 2));
-                const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
-                acc[0] = fmaf(w, f0.x, acc[0]);
-                acc[1] = fmaf(w, f0.y, acc[1]);
-                acc[2] = fmaf(w, f1.x, acc[2]);
-                acc[3] = fmaf(w, f1.y, acc[3]);
-              } else {
-                const uint32_t raw = *reinterpret_cast<const uint32_t*>(vrow + tt * (D * 2));
-                const float2 f0 = Elem<T>::to_float2(raw);
-                acc[0] = fmaf(w, f0.x, acc[0]);
-                acc[1] = fmaf(w, f0.y, acc[1]);
-              }
-            }
-          }
-        }
-      }
+      Tile::run(Ks, Ks + Sh::TILE, nvalid, qreg, lane, m, l, acc);
     }
     __syncwarp();
     if (i + SPW < nmine) {
@@ -283,17 +322,21 @@ __global__ void __launch_bounds__(NW * 32) pkv_decode_simt_kernel(const DecodePa
   }
 }
 
-// Stages per warp: about 96 KB of ring per CTA, at least 2 stages.
+#ifndef PKV_SIMT_RING_BYTES
+#define PKV_SIMT_RING_BYTES (64 * 1024)  // ring bytes per CTA (build-time tuning knob)
+#endif
+
+// Stages per warp: about PKV_SIMT_RING_BYTES of ring per CTA, 1 to 6 stages.
 template <int D, int BS>
 constexpr int simt_stages() {
   constexpr int stage = 2 * BS * D * 2;
-  constexpr int spw = (96 * 1024) / (4 * stage);
-  return spw < 2 ? 2 : (spw > 6 ? 6 : spw);
+  constexpr int spw = (PKV_SIMT_RING_BYTES) / (kDecodeWarps * stage);
+  return spw < 1 ? 1 : (spw > 6 ? 6 : spw);
 }
 
 template <typename T, int D, int BS>
 cudaError_t launch_decode_simt(const DecodeParams& p, int num_seqs, cudaStream_t stream) {
-  constexpr int NW = 4;
+  constexpr int NW = kDecodeWarps;
   constexpr int SPW = simt_stages<D, BS>();
   using Sh = SimtShape<D, BS, NW, SPW>;
   auto kern = pkv_decode_simt_kernel<T, D, BS, NW, SPW>;
@@ -307,7 +350,8 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int num_seqs, cudaStream_t
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const dim3 grid(p.max_partitions, p.num_heads, num_seqs);
+  const dim3 grid(PKV_GRID_HEAD_FASTEST ? p.num_heads : p.max_partitions,
+                  PKV_GRID_HEAD_FASTEST ? p.max_partitions : p.num_heads, num_seqs);
   kern<<<grid, NW * 32, Sh::SMEM, stream>>>(p);
   return cudaGetLastError();
 }

@@ -34,7 +34,8 @@ extern "C" pkv_status_t paged_attention_decode_static_workspace(
   static void* device_ptr[kMaxDevices] = {};
   char msg[256];
   const size_t need =
-      paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_context_len, partition_size);
+      paged_attention_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                                     partition_size);
   if (need > PKV_STATIC_WORKSPACE_BYTES) {
     snprintf(msg, sizeof msg,
              "split-K scratch of %zu bytes exceeds the static workspace of %u bytes; "

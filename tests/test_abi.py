@@ -54,10 +54,23 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.paged_attention_workspace_size
-    assert ws(64, 40, 128, 512, 512) == 0  # one partition: no workspace
-    assert ws(64, 40, 128, 513, 512) == 64 * 40 * 2 * 130 * 4
-    assert ws(16, 40, 128, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
-    assert ws(0, 40, 128, 4096, 0) == 0 and ws(4, 40, 128, -1, 0) == 0
+    prev = lib.pkv_set_decode_path(1)  # partitioned
+    try:
+        assert ws(64, 40, 40, 128, 16, 512, 512) == 0  # one partition: no workspace
+        assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
+        assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
+        assert ws(0, 40, 40, 128, 16, 4096, 0) == 0 and ws(4, 40, 40, 128, 16, -1, 0) == 0
+        assert lib.pkv_set_decode_path(2) == 1  # persistent
+        # prefix of S + 1 ints (256-byte aligned) + 2 partials of (D + 2) floats per warp and group head
+        assert ws(64, 40, 40, 128, 16, 2048, 0) == 512 + 2 * 2048 * 1 * 130 * 4
+        assert ws(256, 32, 8, 128, 16, 8192, 0) == 1280 + 2 * 2048 * 4 * 130 * 4
+        assert ws(2, 4, 4, 64, 16, 33, 0) == 256 + 2 * 24 * 66 * 4  # 2 seqs x 4 heads x 3 blocks = 24 warps
+        assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 8 * 66 * 4  # too many sequences: partitioned
+        assert lib.pkv_set_decode_path(7) == -1
+        assert lib.pkv_set_decode_path(0) == 2  # auto chooses the partitioned path
+        assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
+    finally:
+        lib.pkv_set_decode_path(prev)
 
 
 P = ctypes.c_void_p

@@ -63,7 +63,8 @@ def test_static_workspace_matches_decode_on_two_calls(cuda_lib):
                               num_kv_heads=c["num_kv_heads"], head_dim=128, block_size=16, dtype=c["dtype"],
                               pool_factor=1.2)
         mcl = batch.max_context_len
-        need = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, 128, mcl, c["P"])
+        need = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, batch.num_kv_heads, 128, 16,
+                                                      mcl, c["P"])
         assert 0 < need <= STATIC_BYTES  # the case exercises the split-K scratch
         t = W.as_torch(batch, DEV)
         ref = torch.empty_like(t["query"])
@@ -82,8 +83,8 @@ def test_static_workspace_matches_decode_on_two_calls(cuda_lib):
 def test_static_workspace_rejects_oversize_requests(cuda_lib):
     lib = binding.load()
     fn = static_entry(lib)
-    S, H, D, mcl, P = 64, 64, 128, 32768, 512
-    need = binding.paged_attention_workspace_size(S, H, D, mcl, P)
+    S, H, D, mcl, P = 3000, 64, 128, 32768, 512  # more sequences than the persistent path takes
+    need = binding.paged_attention_workspace_size(S, H, H, D, 16, mcl, P)
     assert need > STATIC_BYTES
     fake = ctypes.c_void_p(0x10000)
     st = fn(fake, fake, fake, fake, fake, mcl // 16, fake, S, mcl, 0.1, 16, H, H, D, 2048, 0, P, None)
