@@ -65,6 +65,7 @@ __global__ void pkv_write_kernel(const uint4* __restrict__ key, const uint4* __r
                                  uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
                                  const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads,
                                  int pieces_per_row, int block_size, long long num_slots, unsigned* err) {
+  pdl_begin();
   const long long total = (long long)num_tokens * num_kv_heads * pieces_per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
@@ -72,60 +73,145 @@ __global__ void pkv_write_kernel(const uint4* __restrict__ key, const uint4* __r
     const long long r = idx / pieces_per_row;
     const int h = (int)(r % num_kv_heads);
     const int t = (int)(r / num_kv_heads);
+    // the slot and the row pieces load together: the pieces do not depend on the slot
+    const size_t src = ((size_t)t * num_kv_heads + h) * pieces_per_row + c;
     const long long slot = __ldg(slot_mapping + t);
+    const uint4 kv = __ldg(key + src);
+    const uint4 vv = __ldg(value + src);
     if (slot < 0) continue;  // padding token
     if (slot >= num_slots) {
       if (c == 0 && h == 0) atomicOr(err, PKV_DEVERR_SLOT);
       continue;
     }
     const long long blk = slot / block_size, off = slot - blk * block_size;
-    const size_t src = ((size_t)t * num_kv_heads + h) * pieces_per_row + c;
     const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * pieces_per_row + c;
-    key_cache[dst] = __ldg(key + src);
-    value_cache[dst] = __ldg(value + src);
+    key_cache[dst] = kv;
+    value_cache[dst] = vv;
   }
 }
 
 // ---------------------------------------------------------------------------
 // split-K reduce: merge the partitions' (m_p, l_p, o_p) of one (seq, head) by
 // log-sum-exp: out = sum_p w_p o_p / sum_p w_p with w_p = l_p 2^(m_p - max m).
+// One warp per (seq, head) row, kReduceRows rows per CTA; lane p holds the
+// weight of partition p (p < 32 per round) and each lane merges D/32 dims.
 
-template <typename T>
-__global__ void pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o,
-                                  const float* __restrict__ part_m, const float* __restrict__ part_l,
-                                  const int32_t* __restrict__ context_lens, int num_heads, int head_dim,
-                                  int partition_size, int max_partitions, int ctx_limit) {
-  extern __shared__ float wsh[];  // [max_partitions] weights
-  __shared__ float s_inv;
-  const int h = blockIdx.x, s = blockIdx.y;
-  int ctx = context_lens[s];
-  ctx = ctx < 0 ? 0 : (ctx > ctx_limit ? ctx_limit : ctx);
+constexpr int kReduceRows = 4;
+constexpr int kReduceEarly = 4;  // partitions whose partial outputs are fetched with the first loads
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceRows)
+    pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o, const float* __restrict__ part_m,
+                      const float* __restrict__ part_l, const int32_t* __restrict__ context_lens, int num_seqs,
+                      int num_heads, int partition_size, int max_partitions, int ctx_limit) {
+  pdl_begin();
+  constexpr int DPL = D / 32;  // dims per lane: 4 (float4) or 2 (float2)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;  // = s * num_heads + h
+  if (row >= (size_t)num_seqs * num_heads) return;
+  const int s = (int)(row / num_heads);
+  const size_t base = row * max_partitions;
+  // One round of loads: the context length, this lane's partition (m, l), and the
+  // partial outputs of the first partitions. All are in bounds whatever the
+  // context length turns out to be; entries past the sequence's partitions are
+  // masked below.
+  const int ctx_raw = context_lens[s];
+  float mp = -INFINITY, lp = 0.f;
+  if (lane < max_partitions) {
+    mp = part_m[base + lane];
+    lp = part_l[base + lane];
+  }
+  float o_early[kReduceEarly][DPL];
+#pragma unroll
+  for (int k = 0; k < kReduceEarly; ++k) {
+    if (k < max_partitions) {
+      const float* o = part_o + (base + k) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(o);
+        o_early[k][0] = v.x; o_early[k][1] = v.y; o_early[k][2] = v.z; o_early[k][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(o);
+        o_early[k][0] = v.x; o_early[k][1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o_early[k][e] = 0.f;
+    }
+  }
+  const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > ctx_limit ? ctx_limit : ctx_raw);
   const int np = (ctx + partition_size - 1) / partition_size;
   if (np <= 1) return;  // the decode kernel wrote this row directly
-  const size_t row = (size_t)s * num_heads + h;
-  const size_t base = row * max_partitions;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int q = lane; q < np; q += 32) M = fmaxf(M, part_m[base + q]);
-    M = warp_max(M);
-    float W = 0.f;
-    for (int q = lane; q < np; q += 32) {
-      const float mq = part_m[base + q];
-      const float wq = mq == -INFINITY ? 0.f : part_l[base + q] * fast_exp2(mq - M);
-      wsh[q] = wq;
-      W += wq;
+  if (lane >= np) mp = -INFINITY;
+  // global max over all partitions (np may exceed 32)
+  float M = mp;
+  for (int p = 32 + lane; p < np; p += 32) M = fmaxf(M, part_m[base + p]);
+  M = warp_max(M);
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float W = 0.f;
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    float wp = 0.f;
+    if (p0 == 0) {
+      wp = mp == -INFINITY ? 0.f : lp * fast_exp2(mp - M);
+    } else if (p0 + lane < np) {
+      const float m2 = part_m[base + p0 + lane];
+      wp = m2 == -INFINITY ? 0.f : part_l[base + p0 + lane] * fast_exp2(m2 - M);
     }
-    W = warp_sum(W);
-    if (lane == 0) s_inv = W > 0.f ? 1.f / W : 0.f;
+    W += wp;
+    const int cnt = np - p0 < 32 ? np - p0 : 32;
+    int k = 0;
+    if (p0 == 0) {
+#pragma unroll
+      for (int q = 0; q < kReduceEarly; ++q) {
+        const float w = __shfl_sync(kFull, wp, q);
+        if (q < cnt) {
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, o_early[q][e], acc[e]);
+        }
+      }
+      k = kReduceEarly;
+    }
+    for (; k < cnt; ++k) {
+      const float w = __shfl_sync(kFull, wp, k);
+      const float* o = part_o + (base + p0 + k) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(o);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(o);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
   }
-  __syncthreads();
-  const float inv = s_inv;
-  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-    float o = 0.f;
-    for (int q = 0; q < np; ++q) o += wsh[q] * part_o[(base + q) * head_dim + d];
-    out[row * head_dim + d] = Elem<T>::from_float(o * inv);
+  W = warp_sum(W);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  T* dst = out + row * D + lane * DPL;
+  if constexpr (DPL == 4) {
+    uint2 v;
+    v.x = Elem<T>::pack2(acc[0] * inv, acc[1] * inv);
+    v.y = Elem<T>::pack2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = Elem<T>::pack2(acc[0] * inv, acc[1] * inv);
   }
+}
+
+template <typename T>
+cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cudaStream_t stream) {
+  const size_t rows = (size_t)num_seqs * p.num_heads;
+  const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
+  T* out = static_cast<T*>(p.out);
+  const float *po = p.part_o, *pm = p.part_m, *pl = p.part_l;
+  if (head_dim == 128)
+    return launch_kernel(pkv_reduce_kernel<T, 128>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
+                         p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
+  return launch_kernel(pkv_reduce_kernel<T, 64>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
+                       p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
 }
 
 // ---------------------------------------------------------------------------
@@ -267,11 +353,10 @@ pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
   const int threads = 256;
   long long blocks = (total + threads - 1) / threads;
   if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-  pkv_write_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(key_cache),
-      static_cast<uint4*>(value_cache), slot_mapping, num_tokens, num_kv_heads, pieces, block_size,
-      (long long)num_blocks * block_size, err);
-  e = cudaGetLastError();
+  e = launch_kernel(pkv_write_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(key_cache),
+                    static_cast<uint4*>(value_cache), slot_mapping, num_tokens, num_kv_heads, pieces, block_size,
+                    (long long)num_blocks * block_size, err);
   if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write launch");
   return PKV_OK;
 }
@@ -415,19 +500,8 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
   if (pl.np > 1) {
-    const dim3 grid(num_heads, num_seqs);
-    const int threads = head_dim;
-    const size_t shm = (size_t)pl.np * sizeof(float);
-    if (dtype == PKV_F16) {
-      pkv_reduce_kernel<__half><<<grid, threads, shm, stream>>>(static_cast<__half*>(out), p.part_o, p.part_m,
-                                                                p.part_l, context_lens, num_heads, head_dim, P,
-                                                                pl.np, p.ctx_limit);
-    } else {
-      pkv_reduce_kernel<__nv_bfloat16><<<grid, threads, shm, stream>>>(
-          static_cast<__nv_bfloat16*>(out), p.part_o, p.part_m, p.part_l, context_lens, num_heads, head_dim, P,
-          pl.np, p.ctx_limit);
-    }
-    e = cudaGetLastError();
+    e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream)
+                         : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
   }
   return PKV_OK;

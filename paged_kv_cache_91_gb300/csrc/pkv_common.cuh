@@ -62,6 +62,37 @@ struct DecodeParams {
   int ctx_limit;       // min(max_context_len, max_blocks_per_seq * block_size)
 };
 
+#ifndef PKV_USE_PDL
+#define PKV_USE_PDL 1  // launch with programmatic stream serialization (build-time knob)
+#endif
+
+// Programmatic dependent launch. Every kernel first waits until the kernels
+// before it in the stream have completed and their writes are visible (a no-op
+// without a programmatic dependency), then lets the next kernel start its launch
+// while this one runs. Inputs are only read after the wait, so the stream
+// order of reads and writes is that of ordinary launches.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization allowed (PKV_USE_PDL), else plainly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PKV_USE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -178,6 +178,7 @@ template <typename T, int D, int BS, int NW, int SPW>
 __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
     pkv_decode_gqa_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap) {
+  pdl_begin();
   using Sh = MmaShape<D, BS, NW, SPW>;
   using Tile = MmaTile<T, D, BS>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -372,8 +373,7 @@ cudaError_t launch_decode_gqa_mma(const DecodeParams& p, const CUtensorMap& kmap
   }
   const dim3 grid(PKV_GRID_HEAD_FASTEST ? p.num_kv_heads : p.max_partitions,
                   PKV_GRID_HEAD_FASTEST ? p.max_partitions : p.num_kv_heads, num_seqs);
-  kern<<<grid, NW * 32, Sh::SMEM, stream>>>(p, kmap, vmap);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(NW * 32), Sh::SMEM, stream, p, kmap, vmap);
 }
 
 }  // namespace pkv

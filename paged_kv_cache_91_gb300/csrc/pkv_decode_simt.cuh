@@ -172,6 +172,7 @@ struct SimtShape : SimtTileShape<D, BS> {
 
 template <typename T, int D, int BS, int NW, int SPW>
 __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_kernel(const DecodeParams p) {
+  pdl_begin();
   using Sh = SimtShape<D, BS, NW, SPW>;
   using Tile = SimtTile<T, D, BS>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -352,8 +353,7 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int num_seqs, cudaStream_t
   }
   const dim3 grid(PKV_GRID_HEAD_FASTEST ? p.num_heads : p.max_partitions,
                   PKV_GRID_HEAD_FASTEST ? p.max_partitions : p.num_heads, num_seqs);
-  kern<<<grid, NW * 32, Sh::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(NW * 32), Sh::SMEM, stream, p);
 }
 
 }  // namespace pkv

@@ -95,6 +95,7 @@ template <typename T, int D, int BS, int NW, int SPW, bool MMA>
 __global__ void __launch_bounds__(NW * 32, 1)
     pkv_decode_stream_kernel(const StreamParams sp, const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap) {
+  pdl_begin();
   using Sh = StreamShape<D, BS, NW, SPW, MMA>;
   using ST = SimtTile<T, D, BS>;
   using MT = MmaTile<T, D, BS>;
@@ -377,6 +378,7 @@ __global__ void pkv_stream_reduce_kernel(T* __restrict__ out, const float* __res
                                          const float* __restrict__ slot_m, const float* __restrict__ slot_l,
                                          const int* __restrict__ pre, int num_seqs, int num_heads, int head_dim,
                                          int ng, int gc, int nwarps) {
+  pdl_begin();
   __shared__ float s_max[8], s_inv[8];
   const int g = blockIdx.x, s = blockIdx.y;
   const int nb = pre[s + 1] - pre[s];
@@ -448,8 +450,7 @@ struct StreamLaunch {
 
   static cudaError_t launch(const StreamParams& sp, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                             cudaStream_t stream) {
-    kernel()<<<grid, NW * 32, Sh::smem_bytes(sp.num_seqs), stream>>>(sp, kmap, vmap);
-    return cudaGetLastError();
+    return launch_kernel(kernel(), dim3(grid), dim3(NW * 32), Sh::smem_bytes(sp.num_seqs), stream, sp, kmap, vmap);
   }
 };
 

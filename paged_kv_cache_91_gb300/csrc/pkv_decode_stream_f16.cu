@@ -43,11 +43,10 @@ cudaError_t decode_stream_f16(const StreamParams& sp, const CUtensorMap& kmap, c
 }
 
 cudaError_t stream_reduce_f16(const StreamParams& sp, int head_dim, int nwarps, cudaStream_t stream) {
-  const dim3 grid(sp.ng, sp.num_seqs);
-  pkv_stream_reduce_kernel<__half><<<grid, 128, 0, stream>>>(
-      static_cast<__half*>(sp.p.out), sp.slot_o, sp.slot_m, sp.slot_l, sp.pre_out, sp.num_seqs, sp.p.num_heads,
-      head_dim, sp.ng, sp.gc, nwarps);
-  return cudaGetLastError();
+  return launch_kernel(pkv_stream_reduce_kernel<__half>, dim3(sp.ng, sp.num_seqs), dim3(128), 0, stream,
+                       static_cast<__half*>(sp.p.out), (const float*)sp.slot_o, (const float*)sp.slot_m,
+                       (const float*)sp.slot_l, (const int*)sp.pre_out, sp.num_seqs, sp.p.num_heads, head_dim, sp.ng,
+                       sp.gc, nwarps);
 }
 
 }  // namespace pkv
