@@ -51,9 +51,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["decode-step", "copy-blocks"], default="decode-step",
+                    help="decode-step: the hot path (default); copy-blocks: the copy-on-write block copy alone")
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2: LLaMA-2-13B-shaped)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--max-seqs", type=int, default=None, help="use only the workload's first N sequences")
+    ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32],
+                    help="tokens per KV block (the pages' block-size ablation)")
     ap.add_argument("--path", choices=["persistent", "partitioned"], default=None,
                     help="decode path (default: the library's automatic choice)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -336,7 +340,7 @@ def run_ours(args, dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     binding.load()
-    batch = W.make_config(args.config, max_seqs=args.max_seqs)
+    batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size)
     P = args.partition_size
     t = W.as_torch(batch, dev)
     out = torch.empty_like(t["query"])
@@ -470,12 +474,59 @@ def run_ours(args, dist):
         print(json.dumps(line), flush=True)
 
 
+def run_copy_blocks(args, dist):
+    """Time paged_kv_copy_blocks: 256 disjoint (src, dst) block pairs of the workload's pool per call."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_91_gb300 import binding
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size)
+    t = W.as_torch(batch, dev)
+    NB = batch.num_blocks
+    npairs = min(256, NB // 2)
+    perm = np.random.default_rng(9).permutation(NB)
+    mapping = torch.from_numpy(np.stack([perm[:npairs], perm[npairs:2 * npairs]], axis=1).astype(np.int64)).to(dev)
+    block_bytes = batch.num_kv_heads * batch.block_size * batch.head_dim * 2
+    moved = 2 * 2 * npairs * block_bytes  # K and V, read and written
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        binding.paged_kv_copy_blocks(t["key_cache"], t["value_cache"], mapping, stream=stream)
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    a.record(stream)
+    for _ in range(K):
+        binding.paged_kv_copy_blocks(t["key_cache"], t["value_cache"], mapping, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(a.elapsed_time(b))
+    peak, peak_kind = hbm_peak()
+    gbs = dist.sum(moved) * K / (ms / 1e3) / 1e9
+    if dist.rank == 0:
+        print(json.dumps({
+            "metric": "copy-on-write block copy: HBM GB/s (read + write)", "op": "copy_blocks", "value": round(gbs, 2),
+            "unit": "GB/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+            "config": {"workload": W.CONFIG_NAMES[args.config], "pairs_per_call": npairs,
+                       "block_bytes_per_cache": block_bytes},
+            "roofline": {"bound": "hbm", "achieved": round(gbs / dist.world, 2), "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": round(gbs / dist.world / peak, 4)},
+            "gpu_launches": K, "device_errors": binding.device_errors()}), flush=True)
+
+
 def main():
     args = parse_args()
     dist = Dist()
     try:
         if args.impl == "reference":
             run_reference(args, dist)
+        elif args.op == "copy-blocks":
+            run_copy_blocks(args, dist)
         else:
             run_ours(args, dist)
     finally:

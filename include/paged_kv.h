@@ -89,6 +89,32 @@ pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
                             int32_t num_blocks, pkv_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * paged_kv_copy_blocks -- the copy of copy-on-write: whole physical blocks,
+ * every kv head's K and V rows, copied bit for bit.
+ *
+ * Source: "Sparse Computation and Memory Management for Efficient LLM
+ * Inference", Copy-on-Write (append_kv_with_cow copies a shared block to a new
+ * one with fused_block_copy before writing into it); "KV Cache와 PagedAttention
+ * 완전 해부", §9단계 (shared blocks with reference counts; a write into a shared
+ * block copies it first).
+ *
+ * For each pair i: block block_mapping[2i + 1] (dst) of key_cache and
+ * value_cache receives the contents of block block_mapping[2i] (src).
+ *
+ *   block_mapping   [num_pairs][2] int64 (src, dst), device memory
+ *   key_cache, value_cache  the pool, layout above; 16-byte aligned
+ *
+ * No block may be both a source and a destination in one call, and
+ * destinations must be distinct (the result is otherwise undefined). A pair
+ * naming a block outside [0, num_blocks) is skipped and sets
+ * PKV_DEVERR_BLOCK_ID. num_pairs == 0 is a no-op; at most 65535 pairs per call.
+ */
+pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping,
+                                  int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_blocks, pkv_dtype_t dtype,
+                                  cudaStream_t stream);
+
+/*
  * Decode paths (pkv_set_decode_path). Both compute the same result.
  *   PKV_DECODE_PERSISTENT  one wave of CTAs. The (sequence, head group, block)
  *                          tiles of the whole batch are split into equal ranges,
@@ -233,6 +259,17 @@ pkv_status_t paged_attention_decode_static_workspace(
  * against 0.
  */
 pkv_status_t paged_kv_device_errors(uint32_t* flags, int32_t clear);
+
+/*
+ * pkv_selftest_wait_timeout -- check the kernels' bounded wait on this GPU.
+ * Launches one warp that waits on a shared-memory barrier for 16 bytes that no
+ * copy will deliver. After limit_cycles SM cycles (at most about 1 s) the wait
+ * gives up and sets PKV_DEVERR_TIMEOUT in the error word, exactly as a decode
+ * kernel does when a tile copy never lands. The context stays usable. The
+ * pages have no counterpart; this exists to test failure reporting without a
+ * GPU fault.
+ */
+pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream);
 
 /* Static string naming a status code. */
 const char* pkv_status_string(pkv_status_t status);

@@ -63,6 +63,8 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, P, i32, f64, i32, i32, i32, i32, i64, i32,
                                       P, i64, i32]
+        lib.oracle_copy_blocks.restype = i64
+        lib.oracle_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i64]
         lib.oracle_widen.restype = f64
         lib.oracle_widen.argtypes = [ctypes.c_uint16, i32]
         lib.oracle_max_threads.restype = i32
@@ -94,6 +96,18 @@ def write_c(key_cache, value_cache, new_key, new_value, slot_mapping, block_size
                               block_size, kc.shape[0])
     if rc < 0:
         raise ValueError(f"slot of token {-rc - 1} lies outside the pool")
+    return kc, vc
+
+
+def copy_blocks_c(key_cache, value_cache, block_mapping):
+    """Copy whole physical blocks (src -> dst pairs) in copies of the pools."""
+    kc = np.ascontiguousarray(key_cache, dtype=np.uint16).copy()
+    vc = np.ascontiguousarray(value_cache, dtype=np.uint16).copy()
+    bm = np.ascontiguousarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+    NB, Hkv, B, D = kc.shape
+    rc = _load().oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(bm), bm.shape[0], Hkv, D, B, NB)
+    if rc < 0:
+        raise ValueError(f"pair {-rc - 1} names a block outside the pool")
     return kc, vc
 
 
@@ -153,6 +167,19 @@ def write_np(key_cache, value_cache, new_key, new_value, slot_mapping, block_siz
         blk, off = divmod(int(slot), block_size)
         kc[blk, :, off, :] = new_key[t]
         vc[blk, :, off, :] = new_value[t]
+    return kc, vc
+
+
+def copy_blocks_np(key_cache, value_cache, block_mapping):
+    """The copy-on-write block copy as numpy indexing on copies of the pools."""
+    kc = np.array(key_cache, dtype=np.uint16, copy=True)
+    vc = np.array(value_cache, dtype=np.uint16, copy=True)
+    bm = np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+    NB = kc.shape[0]
+    if bm.size and ((bm < 0).any() or (bm >= NB).any()):
+        raise ValueError("block outside the pool")
+    kc[bm[:, 1]] = np.asarray(key_cache)[bm[:, 0]]
+    vc[bm[:, 1]] = np.asarray(value_cache)[bm[:, 0]]
     return kc, vc
 
 

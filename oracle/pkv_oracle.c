@@ -16,6 +16,8 @@
  *                     PagedAttention 완전 해부", §5단계 and §6단계 (block 42,
  *                     slots 0..5, next token into slot 6).
  *
+ *   oracle_copy_blocks -- the copy-on-write block copy (see below).
+ *
  *   oracle_decode  -- decode attention of one query token per sequence over its
  *                     first context_lens[s] cached tokens. The cached K and V
  *                     rows are first gathered through the block table into
@@ -97,6 +99,34 @@ long long oracle_write(const uint16_t* key, const uint16_t* value, uint16_t* key
         ++written;
     }
     return bad ? bad : written;
+}
+
+/*
+ * The block copy of copy-on-write: for each pair (src, dst) of block_mapping,
+ * every kv head's K and V rows of physical block src are copied, bit for bit,
+ * into block dst. "Sparse Computation and Memory Management for Efficient LLM
+ * Inference", Copy-on-Write (append_kv_with_cow: fused_block_copy(phys,
+ * new_phys) before the write); "KV Cache와 PagedAttention 완전 해부", §9단계.
+ * Sources are read as they were before the call. Returns the number of pairs
+ * copied, or -(i + 1) for the first pair i naming a block outside the pool
+ * (that pair is skipped).
+ */
+long long oracle_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const int64_t* block_mapping,
+                             int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                             long long num_blocks) {
+    const size_t per_block = (size_t)num_kv_heads * block_size * head_dim;
+    long long copied = 0, bad = 0;
+    for (int i = 0; i < num_pairs; ++i) {
+        int64_t src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (!bad) bad = -(long long)(i + 1);
+            continue;
+        }
+        memmove(key_cache + dst * per_block, key_cache + src * per_block, sizeof(uint16_t) * per_block);
+        memmove(value_cache + dst * per_block, value_cache + src * per_block, sizeof(uint16_t) * per_block);
+        ++copied;
+    }
+    return bad ? bad : copied;
 }
 
 /* One (sequence, query head) pair. Returns 0, or -1 on a block id outside the pool. */

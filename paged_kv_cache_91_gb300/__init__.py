@@ -9,5 +9,6 @@ from .binding import (  # noqa: F401
     PagedKVError,
     paged_attention_decode,
     paged_attention_workspace_size,
+    paged_kv_copy_blocks,
     paged_kv_write,
 )

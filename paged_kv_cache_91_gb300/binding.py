@@ -54,6 +54,10 @@ def load():
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_last_error_message.restype = ctypes.c_char_p
     lib.pkv_last_error_message.argtypes = []
+    lib.paged_kv_copy_blocks.restype = i32
+    lib.paged_kv_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
+    lib.pkv_selftest_wait_timeout.restype = i32
+    lib.pkv_selftest_wait_timeout.argtypes = [i64, P]
     _lib = lib
     return lib
 
@@ -112,6 +116,22 @@ def set_decode_path(path: int) -> int:
     if prev < 0:
         raise PagedKVError(-1, f"unknown decode path {path}")
     return prev
+
+
+def paged_kv_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,
+                         stream=None) -> None:
+    """Copy whole physical blocks: block_mapping [num_pairs][2] int64 (src, dst) on the device."""
+    lib = load()
+    dt = _cuda16("key_cache", key_cache)
+    if _cuda16("value_cache", value_cache) != dt or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "value_cache must match key_cache")
+    if block_mapping.dtype != torch.int64 or not block_mapping.is_cuda or not block_mapping.is_contiguous():
+        raise PagedKVError(-1, "block_mapping must be a contiguous CUDA int64 tensor")
+    if block_mapping.numel() % 2:
+        raise PagedKVError(-1, "block_mapping must hold (src, dst) pairs")
+    NB, Hkv, B, D = key_cache.shape
+    _check(lib, lib.paged_kv_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_mapping),
+                                         block_mapping.numel() // 2, Hkv, D, B, NB, dt, _stream(key_cache, stream)))
 
 
 def paged_attention_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
@@ -207,3 +227,10 @@ def paged_attention_decode_static_workspace(out: torch.Tensor, query: torch.Tens
                    _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt,
                    int(partition_size), _stream(query, stream)))
     return out
+
+
+def selftest_wait_timeout(limit_cycles: int = 2_000_000) -> int:
+    """Run the bounded-wait self-test; returns the error word it leaves (PKV_DEVERR_TIMEOUT expected)."""
+    lib = load()
+    _check(lib, lib.pkv_selftest_wait_timeout(int(limit_cycles), _stream(torch.empty(0, device="cuda"), None)))
+    return device_errors(clear=True)

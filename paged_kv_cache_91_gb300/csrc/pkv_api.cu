@@ -215,6 +215,49 @@ cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cud
 }
 
 // ---------------------------------------------------------------------------
+// copy-on-write block copy: every 16-byte piece of physical block src (all kv
+// heads, K and V) goes to block dst. Grid: (pieces, pairs).
+
+__global__ void pkv_copy_blocks_kernel(uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                                       const int64_t* __restrict__ block_mapping, long long pieces_per_block,
+                                       long long num_blocks, unsigned* err) {
+  pdl_begin();
+  const int pair = blockIdx.y;
+  const long long src = block_mapping[2 * pair], dst = block_mapping[2 * pair + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, PKV_DEVERR_BLOCK_ID);
+    return;
+  }
+  const uint4* ks = key_cache + src * pieces_per_block;
+  const uint4* vs = value_cache + src * pieces_per_block;
+  uint4* kd = key_cache + dst * pieces_per_block;
+  uint4* vd = value_cache + dst * pieces_per_block;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < pieces_per_block; i += stride) {
+    const uint4 k = __ldg(ks + i), v = __ldg(vs + i);
+    kd[i] = k;
+    vd[i] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// self-test of the bounded wait: an mbarrier expects 16 transaction bytes that
+// no copy will ever deliver; the wait must give up after `limit` cycles and
+// report PKV_DEVERR_TIMEOUT. Nothing is in flight when the kernel returns.
+
+__global__ void pkv_wait_selftest_kernel(unsigned* err, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, 16);  // the phase now waits for 16 bytes that never come
+  }
+  __syncwarp();
+  const bool done = __all_sync(kFull, mbar_wait(&bar, 0, limit));
+  if (!done && threadIdx.x == 0) atomicOr(err, PKV_DEVERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
 // tensor maps for the grouped-query kernel
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -366,6 +409,37 @@ int32_t pkv_set_decode_path(int32_t path) {
   return g_decode_path.exchange(path);
 }
 
+pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping,
+                                  int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks, pkv_dtype_t dtype, cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs < 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_kv_heads <= 0 || num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (num_pairs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_pairs must be <= 65535 per call");
+  if (num_pairs == 0) return PKV_OK;
+  if (!key_cache || !value_cache || !block_mapping) return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+  const long long pieces = (long long)num_kv_heads * block_size * head_dim * 2 / 16;
+  const int threads = 256;
+  long long chunks = (pieces + threads * 4 - 1) / (threads * 4);  // about 4 pieces per thread
+  if (chunks < 1) chunks = 1;
+  e = launch_kernel(pkv_copy_blocks_kernel, dim3((unsigned)chunks, (unsigned)num_pairs), dim3(threads), 0, stream,
+                    static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), block_mapping, pieces,
+                    (long long)num_blocks, err);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_copy_blocks launch");
+  return PKV_OK;
+}
+
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                       int32_t block_size, int32_t max_context_len, int32_t partition_size) {
   if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
@@ -504,6 +578,21 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
                          : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
   }
+  return PKV_OK;
+}
+
+pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (limit_cycles <= 0 || limit_cycles > kWaitLimitCycles)
+    return fail(PKV_ERR_INVALID_ARG, "limit_cycles must be in (0, %lld]", kWaitLimitCycles);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+  pkv_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, (long long)limit_cycles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return PKV_OK;
 }
 

@@ -281,13 +281,18 @@ def config_context_lens(n: int) -> np.ndarray:
     raise ValueError(n)
 
 
-def make_config(n: int, threads: int | None = None, max_seqs: int | None = None) -> DecodeBatch:
-    """Workload n (1..5) at full size, or its first ``max_seqs`` sequences."""
+def make_config(n: int, threads: int | None = None, max_seqs: int | None = None,
+                block_size: int = 16) -> DecodeBatch:
+    """Workload n (1..5) at full size, or its first ``max_seqs`` sequences.
+
+    ``block_size`` other than 16 gives the same contexts paged in blocks of 8 or
+    32 tokens (the pages' block-size ablation; 16 is the default they report best).
+    """
     ctx = config_context_lens(n)
     if max_seqs is not None:
         ctx = ctx[:max_seqs]
     seed = 1000 + n
-    common = dict(seed=seed, context_lens=ctx, block_size=16, name=f"cfg{n}", threads=threads)
+    common = dict(seed=seed, context_lens=ctx, block_size=block_size, name=f"cfg{n}", threads=threads)
     if n == 1:
         return build_batch(num_heads=4, num_kv_heads=4, head_dim=64, dtype=F16, num_blocks=16, **common)
     if n == 2:

@@ -26,13 +26,14 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:pkv_status_t|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:pkv_status_t|size_t|int32_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("paged_kv_write", "paged_attention_decode", "paged_attention_workspace_size",
-              "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message"):
+              "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message", "pkv_set_decode_path",
+              "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks"):
         assert n in names
 
 

@@ -321,3 +321,92 @@ def test_more_sequences_than_the_persistent_path_takes():
     out = run_step(batch, t)
     torch.cuda.synchronize()
     check_close(as_np(out), reference(batch), F16, "fallback")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A barrier wait that nothing completes gives up, sets PKV_DEVERR_TIMEOUT, and the GPU stays usable."""
+    assert binding.device_errors() == 0
+    assert binding.selftest_wait_timeout(2_000_000) & 8
+    batch = W.make_config(1)
+    t = W.as_torch(batch, DEV)
+    out = run_step(batch, t, write=False)
+    torch.cuda.synchronize()
+    check_close(as_np(out), reference(batch), F16, "after timeout")
+    assert binding.device_errors() == 0
+
+
+# ----------------------------------------------------------------------------
+# copy-on-write: block copies and writes driven by the host block pool
+
+
+def test_copy_on_write_step_matches_oracle():
+    """Fork sequences, append tokens (copying shared blocks first), then decode each sequence."""
+    from paged_kv_cache_91_gb300.block_pool import BlockPool
+
+    rng = np.random.default_rng(61)
+    B, Hkv, H, D, dtype = 16, 4, 8, 128, F16
+    pool = BlockPool(num_blocks=96, block_size=B, seed=61)
+    seqs = []
+    for n in (23, 40, 16, 5):
+        s = pool.new_sequence()
+        pool.append_tokens(s, n)
+        seqs.append(s)
+    seqs += [pool.fork(seqs[0]), pool.fork(seqs[0]), pool.fork(seqs[1]), pool.fork(seqs[2])]
+    kc = W.round_f32_to(rng.standard_normal((96, Hkv, B, D), dtype=np.float32), dtype)
+    vc = W.round_f32_to(rng.standard_normal((96, Hkv, B, D), dtype=np.float32), dtype)
+    # one decode step: every sequence appends 1-3 tokens
+    slots, copies = [], []
+    for s in seqs:
+        sl, cp = pool.append_tokens(s, int(rng.integers(1, 4)))
+        slots += sl
+        copies += cp
+    assert len(copies) >= 3  # the forks' shared last blocks were copied
+    slots = np.array(slots, dtype=np.int64)
+    mapping = np.array(copies, dtype=np.int64).reshape(-1, 2)
+    new_k = W.round_f32_to(rng.standard_normal((len(slots), Hkv, D), dtype=np.float32), dtype)
+    new_v = W.round_f32_to(rng.standard_normal((len(slots), Hkv, D), dtype=np.float32), dtype)
+    ek, ev = oracle.copy_blocks_c(kc, vc, mapping)
+    ek, ev = oracle.write_c(ek, ev, new_k, new_v, slots, B)
+
+    def dev16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.float16).to(DEV)
+
+    tk, tv = dev16(kc), dev16(vc)
+    binding.paged_kv_copy_blocks(tk, tv, torch.from_numpy(mapping).to(DEV))
+    binding.paged_kv_write(dev16(new_k), dev16(new_v), tk, tv, torch.from_numpy(slots).to(DEV))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(as_np(tk), ek)
+    np.testing.assert_array_equal(as_np(tv), ev)
+
+    tables = BlockPool.tables(seqs)
+    ctx = np.array([s.num_tokens for s in seqs], dtype=np.int32)
+    q = W.round_f32_to(rng.standard_normal((len(seqs), H, D), dtype=np.float32), dtype)
+    out = torch.empty(len(seqs), H, D, dtype=torch.float16, device=DEV)
+    binding.paged_attention_decode(out, dev16(q), tk, tv, torch.from_numpy(tables).to(DEV),
+                                   torch.from_numpy(ctx).to(DEV), 1 / np.sqrt(D), max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    ref = oracle.decode_c(q, ek, ev, tables, ctx, 1 / np.sqrt(D), dtype)
+    check_close(as_np(out), ref, dtype, "after copy-on-write")
+    assert binding.device_errors() == 0
+
+
+@pytest.mark.parametrize("D,B", [(64, 8), (128, 32)])
+def test_copy_blocks_many_pairs_and_bad_pair(D, B):
+    rng = np.random.default_rng(62)
+    NB, Hkv = 300, 2
+    kc = rng.integers(0, 65536, size=(NB, Hkv, B, D), dtype=np.uint16)
+    vc = rng.integers(0, 65536, size=(NB, Hkv, B, D), dtype=np.uint16)
+    perm = rng.permutation(NB)
+    pairs = np.stack([perm[:100], perm[100:200]], axis=1).astype(np.int64)
+    ek, ev = oracle.copy_blocks_c(kc, vc, pairs)
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(DEV)
+
+    tk, tv = dev(kc), dev(vc)
+    bad = np.concatenate([pairs, [[NB + 5, perm[250]]]]).astype(np.int64)  # last pair names no block
+    binding.paged_kv_copy_blocks(tk, tv, torch.from_numpy(bad).to(DEV))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(as_np(tk), ek)
+    np.testing.assert_array_equal(as_np(tv), ev)
+    assert binding.device_errors() & 1
