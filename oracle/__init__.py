@@ -6,8 +6,9 @@ Python binding never import it. It shares no code with the CUDA path.
 
 Two independent implementations of the same definitions:
 
-* ``write_c`` / ``decode_c`` -- plain C (``pkv_oracle.c``), fp64, OpenMP over
-  (sequence, head) pairs; fast enough for the full-size workloads.
+* ``write_c`` / ``decode_c`` / ``copy_blocks_c`` / ``write_fp8_c`` -- plain C
+  (``pkv_oracle.c``), fp64, OpenMP over (sequence, head) pairs; fast enough for
+  the full-size workloads. E4M3 (FP8) codes: ``e4m3_encode_c`` / ``e4m3_decode_c``.
 * ``write_np`` / ``decode_np`` -- numpy, fp64, gather-then-attend; plus
   ``attention_np``, unpaged attention over contiguous K/V arrays.
 
@@ -62,7 +63,14 @@ def _load():
         lib.oracle_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64]
         lib.oracle_decode.restype = i32
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, P, i32, f64, i32, i32, i32, i32, i64, i32,
-                                      P, i64, i32]
+                                      i32, f64, f64, P, i64, i32]
+        lib.oracle_write_fp8.restype = i64
+        lib.oracle_write_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i32, ctypes.c_float,
+                                         ctypes.c_float]
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [P, P, i64]
+        lib.oracle_e4m3_decode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [P, P, i64]
         lib.oracle_copy_blocks.restype = i64
         lib.oracle_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i64]
         lib.oracle_widen.restype = f64
@@ -111,12 +119,49 @@ def copy_blocks_c(key_cache, value_cache, block_mapping):
     return kc, vc
 
 
+def e4m3_encode_c(x) -> np.ndarray:
+    """E4M3 codes of float32 values (nearest, ties to even, saturating to +-448)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e4m3_decode_c(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def write_fp8_c(key_cache, value_cache, new_key, new_value, slot_mapping, block_size, src_dtype,
+                k_scale: float, v_scale: float):
+    """The quantizing write into copies of E4M3 pools (uint8 codes)."""
+    kc = np.ascontiguousarray(key_cache, dtype=np.uint8).copy()
+    vc = np.ascontiguousarray(value_cache, dtype=np.uint8).copy()
+    k = np.ascontiguousarray(new_key, dtype=np.uint16)
+    v = np.ascontiguousarray(new_value, dtype=np.uint16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, Hkv, D = k.shape
+    rc = _load().oracle_write_fp8(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(sm), T, Hkv, D, block_size,
+                                  kc.shape[0], DTYPE_CODE[src_dtype], float(k_scale), float(v_scale))
+    if rc < 0:
+        raise ValueError(f"slot of token {-rc - 1} lies outside the pool")
+    return kc, vc
+
+
 def decode_c(query, key_cache, value_cache, block_tables, context_lens, scale, dtype,
-             pairs=None, num_threads: int = 0):
-    """fp64 decode attention; returns out [S][H][D] (rows of unselected pairs are 0)."""
+             pairs=None, num_threads: int = 0, k_scale: float = 1.0, v_scale: float = 1.0):
+    """fp64 decode attention; returns out [S][H][D] (rows of unselected pairs are 0).
+
+    A uint8 pool is an E4M3 cache whose elements are code * k_scale (keys) and
+    code * v_scale (values); 16-bit pools hold dtype bit patterns.
+    """
     q = np.ascontiguousarray(query, dtype=np.uint16)
-    kc = np.ascontiguousarray(key_cache, dtype=np.uint16)
-    vc = np.ascontiguousarray(value_cache, dtype=np.uint16)
+    fp8 = np.asarray(key_cache).dtype == np.uint8
+    cdt = np.uint8 if fp8 else np.uint16
+    kc = np.ascontiguousarray(key_cache, dtype=cdt)
+    vc = np.ascontiguousarray(value_cache, dtype=cdt)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
     S, H, D = q.shape
@@ -130,6 +175,7 @@ def decode_c(query, key_cache, value_cache, block_tables, context_lens, scale, d
         npairs = pp.shape[0]
     rc = _load().oracle_decode(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
                                _ptr(cl), S, float(scale), B, H, Hkv, D, NB, DTYPE_CODE[dtype],
+                               2 if fp8 else DTYPE_CODE[dtype], float(k_scale), float(v_scale),
                                _ptr(pp) if pp is not None else None, npairs, int(num_threads))
     if rc:
         raise ValueError("block table entry outside the pool")
@@ -152,6 +198,35 @@ def widen_np(bits: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     raise ValueError(dtype)
+
+
+def e4m3_decode_np(codes) -> np.ndarray:
+    """Exact values of E4M3 codes: 1 sign, 4 exponent (bias 7), 3 mantissa bits; S.1111.111 is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    v = np.where(e == 0, np.ldexp(m.astype(np.float64), -9), np.ldexp((8 + m).astype(np.float64), e - 10))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return s * v
+
+
+_E4M3_POS = None
+
+
+def e4m3_encode_np(x) -> np.ndarray:
+    """Nearest E4M3 code of float32 values, ties to the even mantissa, saturating to +-448."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_decode_np(np.arange(0x7F, dtype=np.uint8))  # codes 0..126, increasing values
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick = np.where(dhi < dlo, hi, np.where(dlo < dhi, lo, np.where(hi % 2 == 0, hi, lo)))
+    code = pick.astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
 
 
 def write_np(key_cache, value_cache, new_key, new_value, slot_mapping, block_size):
@@ -202,8 +277,9 @@ def attention_np(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> n
     return w @ V
 
 
-def decode_np(query, key_cache, value_cache, block_tables, context_lens, scale, dtype):
-    """fp64 decode attention, gather then attend; returns out [S][H][D]."""
+def decode_np(query, key_cache, value_cache, block_tables, context_lens, scale, dtype,
+              k_scale: float = 1.0, v_scale: float = 1.0):
+    """fp64 decode attention, gather then attend; returns out [S][H][D] (uint8 pools: E4M3 codes)."""
     query = np.asarray(query, dtype=np.uint16)
     S, H, D = query.shape
     Hkv, B = key_cache.shape[1], key_cache.shape[2]
@@ -213,7 +289,11 @@ def decode_np(query, key_cache, value_cache, block_tables, context_lens, scale, 
         ctx = int(context_lens[s])
         for h in range(H):
             g = h // group
-            K = widen_np(gather_np(key_cache, block_tables[s], ctx, g, B), dtype)
-            V = widen_np(gather_np(value_cache, block_tables[s], ctx, g, B), dtype)
+            Kc = gather_np(key_cache, block_tables[s], ctx, g, B)
+            Vc = gather_np(value_cache, block_tables[s], ctx, g, B)
+            if np.asarray(key_cache).dtype == np.uint8:
+                K, V = e4m3_decode_np(Kc) * k_scale, e4m3_decode_np(Vc) * v_scale
+            else:
+                K, V = widen_np(Kc, dtype), widen_np(Vc, dtype)
             out[s, h] = attention_np(widen_np(query[s, h], dtype), K, V, scale)
     return out

@@ -33,7 +33,9 @@
  *                     Query head h reads kv head h / (H / Hkv) (contiguous
  *                     GQA groups). A context of 0 tokens gives o = 0.
  *
- * fp16/bf16 inputs are widened to double exactly from their bit patterns.
+ * fp16/bf16 inputs are widened to double exactly from their bit patterns. An
+ * FP8 (E4M3) cache holds codes of value / scale; its elements are code * scale,
+ * computed exactly in double (oracle_write_fp8, oracle_e4m3_*).
  */
 #include <math.h>
 #include <stdint.h>
@@ -72,6 +74,84 @@ static double widen(uint16_t bits, int dtype) {
 }
 
 double oracle_widen(uint16_t bits, int dtype) { return widen(bits, dtype); }
+
+/*
+ * FP8 E4M3 (the OCP 8-bit format with 4 exponent bits): 1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; the
+ * largest finite magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the
+ * subnormals m/8 * 2^-6.
+ */
+double oracle_e4m3_decode(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value to x, ties to the even mantissa, magnitudes above 448 saturated to 448. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    double best_d = a; /* distance to code 0 (value 0) */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+void oracle_e4m3_encode_array(const float* x, uint8_t* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t* c, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}
+
+/*
+ * The quantizing cache write of an FP8 cache: code = E4M3(value / scale), the
+ * division done in fp32 (correctly rounded) and the result rounded to the
+ * nearest E4M3 value with saturation. "[vLLM] PagedAttention: ...",
+ * write_to_paged_cache(..., kv_cache_dtype, k_scale, v_scale). Returns the
+ * number of tokens written, or -(t + 1) for the first token whose slot lies
+ * outside the pool.
+ */
+long long oracle_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* key_cache, uint8_t* value_cache,
+                           const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                           int block_size, long long num_blocks, int src_dtype, float k_scale, float v_scale) {
+    long long written = 0, bad = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_blocks * block_size) {
+            if (!bad) bad = -(long long)(t + 1);
+            continue;
+        }
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                float kf = (float)widen(key[src + d], src_dtype);
+                float vf = (float)widen(value[src + d], src_dtype);
+                key_cache[dst + d] = oracle_e4m3_encode(kf / k_scale);
+                value_cache[dst + d] = oracle_e4m3_encode(vf / v_scale);
+            }
+        }
+        ++written;
+    }
+    return bad ? bad : written;
+}
 
 /*
  * Returns the number of tokens written, or -(t + 1) for the first token t
@@ -130,11 +210,18 @@ long long oracle_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const i
 }
 
 /* One (sequence, query head) pair. Returns 0, or -1 on a block id outside the pool. */
-static int decode_pair(double* out, const uint16_t* query, const uint16_t* key_cache,
-                       const uint16_t* value_cache, const int32_t* block_tables,
+/* Cache element j of a pool of 16-bit (cache_dtype 0, 1) or E4M3 (cache_dtype 2) elements, in value units. */
+static double cache_value(const void* cache, size_t j, int cache_dtype, double scale) {
+    if (cache_dtype == 2) return oracle_e4m3_decode(((const uint8_t*)cache)[j]) * scale;
+    return widen(((const uint16_t*)cache)[j], cache_dtype);
+}
+
+static int decode_pair(double* out, const uint16_t* query, const void* key_cache,
+                       const void* value_cache, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, double scale,
                        int block_size, int num_heads, int num_kv_heads, int head_dim,
-                       long long num_blocks, int dtype, int s, int h) {
+                       long long num_blocks, int dtype, int cache_dtype, double k_scale, double v_scale,
+                       int s, int h) {
     const int D = head_dim, B = block_size;
     double* o = out + ((size_t)s * num_heads + h) * D;
     int ctx = context_lens[s];
@@ -154,8 +241,8 @@ static int decode_pair(double* out, const uint16_t* query, const uint16_t* key_c
         if (phys < 0 || phys >= num_blocks) { rc = -1; break; }
         size_t base = (((size_t)phys * num_kv_heads + g) * B + (j % B)) * D;
         for (int d = 0; d < D; ++d) {
-            K[(size_t)j * D + d] = widen(key_cache[base + d], dtype);
-            V[(size_t)j * D + d] = widen(value_cache[base + d], dtype);
+            K[(size_t)j * D + d] = cache_value(key_cache, base + d, cache_dtype, k_scale);
+            V[(size_t)j * D + d] = cache_value(value_cache, base + d, cache_dtype, v_scale);
         }
     }
     if (!rc) {
@@ -193,10 +280,11 @@ static int decode_pair(double* out, const uint16_t* query, const uint16_t* key_c
  * num_threads: <= 0 uses the OpenMP default. Returns 0, or -1 if any block id
  * lies outside the pool.
  */
-int oracle_decode(double* out, const uint16_t* query, const uint16_t* key_cache,
-                  const uint16_t* value_cache, const int32_t* block_tables, int max_blocks_per_seq,
+int oracle_decode(double* out, const uint16_t* query, const void* key_cache,
+                  const void* value_cache, const int32_t* block_tables, int max_blocks_per_seq,
                   const int32_t* context_lens, int num_seqs, double scale, int block_size,
                   int num_heads, int num_kv_heads, int head_dim, long long num_blocks, int dtype,
+                  int cache_dtype, double k_scale, double v_scale,
                   const int32_t* pairs, long long npairs, int num_threads) {
     long long n = pairs ? npairs : (long long)num_seqs * num_heads;
     int rc = 0;
@@ -209,7 +297,7 @@ int oracle_decode(double* out, const uint16_t* query, const uint16_t* key_cache,
         int h = pairs ? pairs[2 * i + 1] : (int)(i % num_heads);
         rc |= decode_pair(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                           context_lens, scale, block_size, num_heads, num_kv_heads, head_dim,
-                          num_blocks, dtype, s, h);
+                          num_blocks, dtype, cache_dtype, k_scale, v_scale, s, h);
     }
     return rc ? -1 : 0;
 }
