@@ -43,6 +43,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attention: KV-read HBM GB/s (% of peak) and decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FP8_SCALE = 2.0 ** -6  # k_scale = v_scale of the FP8 runs: N(0,1) values up to 7 are not saturated
 
 
 def parse_args():
@@ -60,6 +61,9 @@ def parse_args():
                     help="tokens per KV block (the pages' block-size ablation)")
     ap.add_argument("--path", choices=["persistent", "partitioned"], default=None,
                     help="decode path (default: the library's automatic choice)")
+    ap.add_argument("--kv-dtype", choices=["auto", "fp8_e4m3"], default="auto",
+                    help="auto: the cache holds the workload's fp16/bf16 values; fp8_e4m3: E4M3 codes "
+                         "(paged_kv_write_fp8 / paged_attention_decode_fp8, k_scale = v_scale = FP8_SCALE)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
@@ -114,15 +118,21 @@ class Dist:
 # byte accounting
 
 
-def step_bytes(batch, partition_size: int):
-    """Algorithmic bytes of one decode call: KV reads plus q, out, tables and split-K partials."""
+def default_partition(fp8: bool) -> int:
+    """The library's partition size when the call passes 0 (longer for an FP8 cache)."""
+    return 1024 if fp8 else 512
+
+
+def step_bytes(batch, partition_size: int, cache_bytes: int = 2):
+    """Algorithmic bytes of one decode call: KV reads plus q, out, tables and split-K partials.
+    cache_bytes: bytes per cached K/V element (2, or 1 for an FP8 cache)."""
     import numpy as np
 
     from paged_kv_cache_91_gb300 import workloads as W
 
-    P = partition_size or 512
+    P = partition_size or default_partition(cache_bytes == 1)
     ctx = batch.context_lens.astype(np.int64)
-    kv = W.algorithmic_kv_bytes(batch)
+    kv = W.algorithmic_kv_bytes(batch) * cache_bytes // batch.elem_bytes
     S, H, D, B = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size
     qo = 2 * S * H * D * batch.elem_bytes
     tables = int(((ctx + B - 1) // B).sum()) * 4 + S * 4
@@ -135,6 +145,8 @@ def step_bytes(batch, partition_size: int):
 KERNEL_SOURCES = {
     "simt": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_f16.cu", "pkv_decode_simt_bf16.cu"),
     "mma": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_f16.cu", "pkv_decode_mma_bf16.cu"),
+    "simt_fp8": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_fp8.cu"),
+    "mma_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mma_fp8.cu"),
 }
 
 
@@ -245,42 +257,59 @@ def gpu_id_for(device) -> str:
 # CPU oracle timing (baseline leg and reference arm)
 
 
-def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1):
-    """Run the oracle over the given sequences (all heads) until budget_s; returns (seconds, reps)."""
+def oracle_fp8_pools(batch, scale: float):
+    """The batch's pools as E4M3 codes from the oracle's encoder: E4M3(fp32(x) / scale) per element."""
+    import numpy as np
+
+    import oracle
+
+    vals = oracle.widen_np(np.arange(65536, dtype=np.uint32).astype(np.uint16), batch.dtype).astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        lut = oracle.e4m3_encode_np(vals / np.float32(scale))
+    return lut[batch.key_cache], lut[batch.value_cache]
+
+
+def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1, fp8_pools=None):
+    """Run the oracle over the given sequences (all heads) until budget_s; returns (seconds, reps).
+    fp8_pools: (key codes, value codes) of an FP8 cache with k_scale = v_scale = FP8_SCALE."""
     import numpy as np
 
     import oracle
 
     pairs = np.array([(s, h) for s in seqs for h in range(batch.num_heads)], dtype=np.int32)
+    kc, vc = fp8_pools if fp8_pools is not None else (batch.key_cache, batch.value_cache)
+    sc = FP8_SCALE if fp8_pools is not None else 1.0
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.decode_c(batch.query, batch.key_cache, batch.value_cache, batch.block_tables, batch.context_lens,
-                        batch.scale, batch.dtype, pairs=pairs)
+        oracle.decode_c(batch.query, kc, vc, batch.block_tables, batch.context_lens,
+                        batch.scale, batch.dtype, pairs=pairs, k_scale=sc, v_scale=sc)
         reps += 1
         el = time.perf_counter() - t0
         if reps >= min_reps and el >= budget_s:
             return el, reps
 
 
-def sample_kv_bytes(batch, seqs):
+def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
     ctx = batch.context_lens[list(seqs)].astype("int64").sum()
-    return int(ctx) * batch.num_kv_heads * batch.head_dim * 2 * batch.elem_bytes
+    return int(ctx) * batch.num_kv_heads * batch.head_dim * 2 * cache_bytes
 
 
 # ----------------------------------------------------------------------------
 
 
-def workload_config(batch, n, partition_size, pool_bytes):
+def workload_config(batch, n, partition_size, pool_bytes, fp8=False):
     from paged_kv_cache_91_gb300 import workloads as W
 
+    extra = {"query_dtype": batch.dtype, "k_scale": FP8_SCALE, "v_scale": FP8_SCALE} if fp8 else {}
     return {
-        "workload": W.CONFIG_NAMES[n],
+        "workload": W.CONFIG_NAMES[n] + (" with an FP8 (E4M3) KV cache" if fp8 else ""),
         "num_seqs": batch.num_seqs, "num_heads": batch.num_heads, "num_kv_heads": batch.num_kv_heads,
-        "head_dim": batch.head_dim, "block_size": batch.block_size, "cache_dtype": batch.dtype,
+        "head_dim": batch.head_dim, "block_size": batch.block_size, "cache_dtype": "e4m3" if fp8 else batch.dtype,
+        **extra,
         "context_lens": {"min": int(batch.context_lens.min()), "mean": float(batch.context_lens.mean()),
                          "max": int(batch.context_lens.max())},
-        "partition_size": partition_size or 512,
+        "partition_size": partition_size or default_partition(fp8),
         "new_tokens_per_step": int((batch.slot_mapping >= 0).sum()),
         "pool_bytes": pool_bytes,
         "l2": "inputs larger than L2 (KV pool > 129 MB); no flush between steps",
@@ -297,8 +326,11 @@ def run_reference(args, dist):
 
     batch = W.make_config(args.config)
     S = batch.num_seqs
+    fp8 = args.kv_dtype == "fp8_e4m3"
+    pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
+    cb = 1 if fp8 else 2
     # size each step's sample so warm-up + timed steps take about two minutes
-    t_one, _ = time_oracle(batch, [0], 0.0)
+    t_one, _ = time_oracle(batch, [0], 0.0, fp8_pools=pools)
     per_seq = max(t_one, 1e-4)
     total_steps = args.steps + args.warmup
     nseq = int(max(1, min(S, 120.0 / (total_steps * per_seq))))
@@ -308,11 +340,11 @@ def run_reference(args, dist):
     for k in range(total_steps):
         seqs = sorted(rng.choice(S, size=nseq, replace=False).tolist())
         t0 = time.perf_counter()
-        time_oracle(batch, seqs, 0.0)
+        time_oracle(batch, seqs, 0.0, fp8_pools=pools)
         dt = time.perf_counter() - t0
         if k >= args.warmup:
             times.append(dt)
-            kv_total += sample_kv_bytes(batch, seqs)
+            kv_total += sample_kv_bytes(batch, seqs, cb)
     total = sum(times)
     value = kv_total / total / 1e9
     cores = oracle.max_threads()
@@ -321,7 +353,7 @@ def run_reference(args, dist):
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(batch, args.config, args.partition_size, int(batch.key_cache.nbytes * 2)),
+        "config": workload_config(batch, args.config, args.partition_size, int(batch.key_cache.nbytes * cb), fp8),
         "tokens_per_s": round(nseq * len(times) / total, 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -348,18 +380,46 @@ def run_ours(args, dist):
     if args.path:
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
-    ws_bytes = binding.paged_attention_workspace_size(batch.num_seqs, batch.num_heads, batch.num_kv_heads,
-                                                      batch.head_dim, batch.block_size, mcl, P)
+    fp8 = args.kv_dtype == "fp8_e4m3"
+    wsize = binding.paged_attention_workspace_size_fp8 if fp8 else binding.paged_attention_workspace_size
+    ws_bytes = wsize(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size, mcl, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    nparts = -(-mcl // (P or 512))
+    nparts = -(-mcl // (P or default_partition(fp8)))
     launches_per_step = 2 + (1 if nparts > 1 else 0)
-    kv_bytes, call_bytes = step_bytes(batch, P)
+    cache_bytes = 1 if fp8 else 2
+    kv_bytes, call_bytes = step_bytes(batch, P, cache_bytes)
+    if fp8:
+        # the FP8 pool: every slot of the 16-bit pool quantized by the library's own write (setup, untimed)
+        NB, Hkv, B, D = t["key_cache"].shape
+        kc, vc = (torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=dev) for _ in range(2))
+        all_slots = torch.arange(NB * B, dtype=torch.int64, device=dev)
+        binding.paged_kv_write_fp8(t["key_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                                   t["value_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D), kc, vc, all_slots,
+                                   FP8_SCALE, FP8_SCALE, stream=stream)
+        torch.cuda.synchronize()
+        del all_slots
+        t["key_cache"], t["value_cache"] = kc, vc
+
+    def write(nk, nv, sm):
+        if fp8:
+            binding.paged_kv_write_fp8(nk, nv, t["key_cache"], t["value_cache"], sm, FP8_SCALE, FP8_SCALE,
+                                       stream=stream)
+        else:
+            binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
+
+    def decode(q, bt, cl, o):
+        if fp8:
+            binding.paged_attention_decode_fp8(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
+                                               FP8_SCALE, FP8_SCALE, max_context_len=mcl, partition_size=P,
+                                               workspace=ws, stream=stream)
+        else:
+            binding.paged_attention_decode(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
+                                           max_context_len=mcl, partition_size=P, workspace=ws, stream=stream)
 
     def step(q, nk, nv, sm, bt, cl, o):
-        binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
-        binding.paged_attention_decode(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
-                                       max_context_len=mcl, partition_size=P, workspace=ws, stream=stream)
+        write(nk, nv, sm)
+        decode(q, bt, cl, o)
 
     args_dev = (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"],
                 t["context_lens"], out)
@@ -378,12 +438,9 @@ def run_ours(args, dist):
     t_wall0 = time.time()
     start.record(stream)
     for k in range(K):
-        binding.paged_kv_write(t["new_key"], t["new_value"], t["key_cache"], t["value_cache"], t["slot_mapping"],
-                               stream=stream)
+        write(t["new_key"], t["new_value"], t["slot_mapping"])
         ev[k][0].record(stream)
-        binding.paged_attention_decode(out, t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
-                                       t["context_lens"], batch.scale, max_context_len=mcl, partition_size=P,
-                                       workspace=ws, stream=stream)
+        decode(t["query"], t["block_tables"], t["context_lens"], out)
         ev[k][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -435,16 +492,21 @@ def run_ours(args, dist):
     value = total_kv * K / (total_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
-    workload = f"cfg{args.config}"
+    workload = f"cfg{args.config}" + ("-fp8" if fp8 else "")
     G = batch.num_heads // batch.num_kv_heads
-    traffic = ncu_traffic(workload, "mma" if 2 <= G <= 8 else "simt")
+    if fp8:
+        kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
+    else:
+        kind = "mma" if 2 <= G <= 8 else "simt"
+    traffic = ncu_traffic(workload, kind)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         import oracle
 
         seqs = list(range(batch.num_seqs))
-        el, reps = time_oracle(batch, seqs, args.cpu_seconds)
+        pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
+        el, reps = time_oracle(batch, seqs, args.cpu_seconds, fp8_pools=pools)
         cpu = {"value": round(kv_bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                "kind": "oracle",
                "sample": f"{reps} full decode pass(es) of the workload (all {batch.num_seqs} sequences x "
@@ -454,13 +516,15 @@ def run_ours(args, dist):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if batch.dtype == "f16" else "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if fp8 else ("f16" if batch.dtype == "f16" else "bf16"),
             "accumulate": "f32", "data": "synthetic (seeded N(0,1) K/V/q, block tables from a shuffled free list)",
-            "config": workload_config(batch, args.config, P, int(batch.key_cache.nbytes * 2)),
+            "config": workload_config(batch, args.config, P, int(batch.key_cache.nbytes * cache_bytes), fp8),
             "tokens_per_s": round(batch.num_seqs * dist.world * K / (total_ms / 1e3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
                             "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
-            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode kernel"
+            "roofline": {"bound": "hbm", "kernel": ("paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
+                         + " (decode kernel"
                          + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,

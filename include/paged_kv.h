@@ -21,7 +21,8 @@
  *   - Kernels check every block-table entry, slot and context length they read.
  *     A bad one is skipped or clamped (never dereferenced), and a bit is set in
  *     a per-device error word that paged_kv_device_errors reads.
- *   - fp16 and bf16 are supported. Query, caches and output share one dtype.
+ *   - fp16 and bf16 are supported. Query, caches and output share one dtype,
+ *     except in the *_fp8 calls, whose caches hold FP8 (E4M3) codes.
  *
  * KV pool layout (both key_cache and value_cache):
  *     [num_blocks][num_kv_heads][block_size][head_dim], row-major,
@@ -43,7 +44,8 @@
 extern "C" {
 #endif
 
-typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype_t;
+/* PKV_FP8_E4M3 names an FP8 cache; it is accepted only where a call says so. */
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype_t;
 
 typedef enum {
   PKV_OK = 0,
@@ -103,6 +105,7 @@ pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
  *
  *   block_mapping   [num_pairs][2] int64 (src, dst), device memory
  *   key_cache, value_cache  the pool, layout above; 16-byte aligned
+ *   dtype           the cache's element type: PKV_F16, PKV_BF16 or PKV_FP8_E4M3
  *
  * No block may be both a source and a destination in one call, and
  * destinations must be distinct (the result is otherwise undefined). A pair
@@ -270,6 +273,74 @@ pkv_status_t paged_kv_device_errors(uint32_t* flags, int32_t clear);
  * GPU fault.
  */
 pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream);
+
+/*
+ * FP8 KV cache. The pages pass kv_cache_dtype, k_scale and v_scale to the cache
+ * write ("[vLLM] PagedAttention: OS 페이징 기법으로 KV 캐시를 관리하는 방법",
+ * section "PagedAttention 커널", write_to_paged_cache) without fixing the format.
+ * Here the format is OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; largest finite value 448; S.1111.111 is NaN; no infinities).
+ * A cache element holds the code of value / scale, so its value is
+ * code * scale: k_scale for key_cache, v_scale for value_cache. Both are host
+ * floats, finite and > 0; others are rejected with PKV_ERR_INVALID_ARG.
+ * The pool layout is the one above with 1-byte elements: a (block, kv head)
+ * tile is block_size * head_dim bytes. paged_kv_copy_blocks copies such a
+ * pool with dtype PKV_FP8_E4M3.
+ */
+
+/*
+ * paged_kv_write_fp8 -- paged_kv_write into an FP8 pool (quantizing).
+ *
+ * For every token t with slot = slot_mapping[t] >= 0 and every kv head h:
+ *     key_cache[slot / block_size][h][slot % block_size][d] = E4M3(key[t][h][d] / k_scale)
+ *     (value_cache likewise with v_scale)
+ * key and value are fp16 or bf16 (dtype). The division is the correctly
+ * rounded fp32 quotient; E4M3() rounds it to the nearest E4M3 value, ties to
+ * the even code, and saturates magnitudes above 448 (infinities included) to
+ * +-448. A NaN gives a NaN code (0x7F or 0xFF). Padding, bad slots, alignment
+ * and the other arguments are as in paged_kv_write.
+ */
+pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_cache,
+                                void* value_cache, const int64_t* slot_mapping, int32_t num_tokens,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int32_t num_blocks, pkv_dtype_t dtype, float k_scale, float v_scale,
+                                cudaStream_t stream);
+
+/*
+ * paged_attention_workspace_size_fp8 -- workspace bytes of
+ * paged_attention_decode_fp8. The FP8 decode always runs on the PARTITIONED
+ * path, whatever pkv_set_decode_path chose, so this is the PARTITIONED size of
+ * paged_attention_workspace_size, except that partition_size 0 selects 1024
+ * (an FP8 tile carries half the bytes, and longer partitions measure faster).
+ */
+size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size,
+                                          int32_t max_context_len, int32_t partition_size);
+
+/*
+ * paged_attention_decode_fp8 -- paged_attention_decode over an FP8 pool.
+ *
+ * The result is that of paged_attention_decode with K_j and V_j replaced by
+ * their values code * k_scale and code * v_scale:
+ *     x_j = scale * k_scale * dot(query[s][h][:], codes of K_j)
+ *     out[s][h][:] = v_scale * sum_j softmax(x)_j * (codes of V_j)
+ * query and out are fp16 or bf16 (dtype). With head_dim 128 and up to 8 query
+ * heads per kv head (MHA included) the tensor cores compute both products in
+ * f16 with fp32 accumulation: the codes widen exactly to f16, a bf16 query is
+ * scaled per head by a power of two into f16 range, and the softmax weights are
+ * rounded to f16 (the normaliser sums the rounded weights). Other shapes run on
+ * the CUDA cores in fp32. partition_size 0 selects 1024 here. All other
+ * arguments, the split-K workspace (paged_attention_workspace_size_fp8) and the
+ * error behaviour are those of paged_attention_decode.
+ */
+pkv_status_t paged_attention_decode_fp8(void* out, const void* query, const void* key_cache,
+                                        const void* value_cache, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                        int32_t num_seqs, int32_t max_context_len, float scale,
+                                        int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                        float k_scale, float v_scale, int32_t partition_size,
+                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Static string naming a status code. */
 const char* pkv_status_string(pkv_status_t status);

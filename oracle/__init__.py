@@ -247,8 +247,8 @@ def write_np(key_cache, value_cache, new_key, new_value, slot_mapping, block_siz
 
 def copy_blocks_np(key_cache, value_cache, block_mapping):
     """The copy-on-write block copy as numpy indexing on copies of the pools."""
-    kc = np.array(key_cache, dtype=np.uint16, copy=True)
-    vc = np.array(value_cache, dtype=np.uint16, copy=True)
+    kc = np.array(key_cache, copy=True)  # 16-bit patterns or 8-bit codes, kept as they are
+    vc = np.array(value_cache, copy=True)
     bm = np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2)
     NB = kc.shape[0]
     if bm.size and ((bm < 0).any() or (bm >= NB).any()):

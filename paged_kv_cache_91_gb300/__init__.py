@@ -8,7 +8,10 @@ missing.
 from .binding import (  # noqa: F401
     PagedKVError,
     paged_attention_decode,
+    paged_attention_decode_fp8,
     paged_attention_workspace_size,
+    paged_attention_workspace_size_fp8,
     paged_kv_copy_blocks,
     paged_kv_write,
+    paged_kv_write_fp8,
 )

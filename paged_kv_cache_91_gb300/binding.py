@@ -16,8 +16,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 
-PKV_F16, PKV_BF16 = 0, 1
+PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 _DTYPE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+_FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)  # an FP8 cache: E4M3 codes
 DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT"}
 
 _lib = None
@@ -58,6 +59,13 @@ def load():
     lib.paged_kv_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.pkv_selftest_wait_timeout.restype = i32
     lib.pkv_selftest_wait_timeout.argtypes = [i64, P]
+    lib.paged_kv_write_fp8.restype = i32
+    lib.paged_kv_write_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, P]
+    lib.paged_attention_workspace_size_fp8.restype = sz
+    lib.paged_attention_workspace_size_fp8.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_decode_fp8.restype = i32
+    lib.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
+                                               f32, f32, i32, P, sz, P]
     _lib = lib
     return lib
 
@@ -87,6 +95,18 @@ def _cuda16(name: str, t: torch.Tensor) -> int:
     if not t.is_contiguous():
         raise PagedKVError(-1, f"{name} must be contiguous")
     return _DTYPE[t.dtype]
+
+
+def _cuda_fp8(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda or t.dtype not in _FP8_DTYPES or not t.is_contiguous():
+        raise PagedKVError(-1, f"{name} must be a contiguous CUDA uint8 or float8_e4m3fn tensor (E4M3 codes)")
+
+
+def _cache_dtype(name: str, t: torch.Tensor) -> int:
+    if t.dtype in _FP8_DTYPES:
+        _cuda_fp8(name, t)
+        return PKV_FP8_E4M3
+    return _cuda16(name, t)
 
 
 def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
@@ -122,8 +142,8 @@ def paged_kv_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, blo
                          stream=None) -> None:
     """Copy whole physical blocks: block_mapping [num_pairs][2] int64 (src, dst) on the device."""
     lib = load()
-    dt = _cuda16("key_cache", key_cache)
-    if _cuda16("value_cache", value_cache) != dt or value_cache.shape != key_cache.shape:
+    dt = _cache_dtype("key_cache", key_cache)
+    if _cache_dtype("value_cache", value_cache) != dt or value_cache.shape != key_cache.shape:
         raise PagedKVError(-1, "value_cache must match key_cache")
     if block_mapping.dtype != torch.int64 or not block_mapping.is_cuda or not block_mapping.is_contiguous():
         raise PagedKVError(-1, "block_mapping must be a contiguous CUDA int64 tensor")
@@ -181,6 +201,68 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
         _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt, int(partition_size),
         _ptr(workspace), wbytes, _stream(query, stream)))
+    return out
+
+
+def paged_kv_write_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                       slot_mapping: torch.Tensor, k_scale: float, v_scale: float, stream=None) -> None:
+    """Quantizing scatter: key/value [T][Hkv][D] (f16/bf16) into an E4M3 pool [NB][Hkv][B][D]
+    (uint8 or float8_e4m3fn): code = E4M3(x / k_scale), likewise for values with v_scale."""
+    lib = load()
+    dt = _cuda16("key", key)
+    if _cuda16("value", value) != dt:
+        raise PagedKVError(-1, "value dtype differs from key")
+    _cuda_fp8("key_cache", key_cache)
+    _cuda_fp8("value_cache", value_cache)
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise PagedKVError(-1, "slot_mapping must be a contiguous CUDA int64 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    T = slot_mapping.numel()
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D) or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between key/value, caches and slot_mapping")
+    _check(lib, lib.paged_kv_write_fp8(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                       _ptr(slot_mapping), T, Hkv, D, B, NB, dt, float(k_scale), float(v_scale),
+                                       _stream(key_cache, stream)))
+
+
+def paged_attention_workspace_size_fp8(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                       block_size: int, max_context_len: int, partition_size: int = 0) -> int:
+    return int(load().paged_attention_workspace_size_fp8(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                         max_context_len, partition_size))
+
+
+def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                               value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               scale: float, k_scale: float, v_scale: float, max_context_len: Optional[int] = None,
+                               partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """paged_attention_decode over an E4M3 pool whose elements are code * k_scale (K) and code * v_scale (V)."""
+    lib = load()
+    dt = _cuda16("query", query)
+    if _cuda16("out", out) != dt:
+        raise PagedKVError(-1, "out dtype differs from query")
+    _cuda_fp8("key_cache", key_cache)
+    _cuda_fp8("value_cache", value_cache)
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    S, H, D2 = query.shape
+    if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between query, out and caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise PagedKVError(-1, "block_tables must be [S][max_blocks] and context_lens [S]")
+    maxb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxb * B
+    need = int(lib.paged_attention_workspace_size_fp8(S, H, Hkv, D, B, max_context_len, partition_size))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib, lib.paged_attention_decode_fp8(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
+        _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt, float(k_scale),
+        float(v_scale), int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
     return out
 
 

@@ -19,6 +19,9 @@ namespace pkv {
 namespace {
 
 constexpr int kDefaultPartition = 512;
+// An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
+// weigh twice as much per byte: longer partitions measure faster.
+constexpr int kDefaultPartitionFp8 = 1024;
 constexpr int kMaxDevices = 64;
 
 thread_local char g_msg[512] = "";
@@ -87,6 +90,59 @@ __global__ void pkv_write_kernel(const uint4* __restrict__ key, const uint4* __r
     const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * pieces_per_row + c;
     key_cache[dst] = kv;
     value_cache[dst] = vv;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// quantizing cache write into an FP8 (E4M3) pool: one thread per 16 codes (16
+// bytes) of a (token, kv head) row, K and V. code = E4M3(x / scale): the
+// division correctly rounded in fp32, then round-to-nearest-even to E4M3 with
+// saturation to +-448 (the satfinite conversion).
+
+template <typename T>
+__device__ __forceinline__ uint4 quantize16(const uint4 (&src)[2], float scale) {
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 r = src[k / 2];
+    const uint32_t w0 = (k & 1) ? r.z : r.x, w1 = (k & 1) ? r.w : r.y;
+    const float2 a = Elem<T>::to_float2(w0), b = Elem<T>::to_float2(w1);
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale)), __NV_SATFINITE, __NV_E4M3);
+    out[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <typename T>
+__global__ void pkv_write_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                     uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                                     const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads,
+                                     int pieces_per_row, int block_size, long long num_slots, float k_scale,
+                                     float v_scale, unsigned* err) {
+  pdl_begin();
+  const long long total = (long long)num_tokens * num_kv_heads * pieces_per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int c = (int)(idx % pieces_per_row);  // 16 output codes = 32 source bytes
+    const long long r = idx / pieces_per_row;
+    const int h = (int)(r % num_kv_heads);
+    const int t = (int)(r / num_kv_heads);
+    const size_t src = (((size_t)t * num_kv_heads + h) * pieces_per_row + c) * 2;
+    const long long slot = __ldg(slot_mapping + t);
+    const uint4 kv[2] = {__ldg(key + src), __ldg(key + src + 1)};
+    const uint4 vv[2] = {__ldg(value + src), __ldg(value + src + 1)};
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (c == 0 && h == 0) atomicOr(err, PKV_DEVERR_SLOT);
+      continue;
+    }
+    const long long blk = slot / block_size, off = slot - blk * block_size;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * pieces_per_row + c;
+    key_cache[dst] = quantize16<T>(kv, k_scale);
+    value_cache[dst] = quantize16<T>(vv, v_scale);
   }
 }
 
@@ -275,16 +331,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The pool viewed as a 2D array [num_blocks * num_kv_heads * block_size][head_dim],
-// copied in boxes of 64 dims x block_size rows with the 128-byte swizzle.
+// copied with the 128-byte swizzle in boxes of 128 bytes x block_size rows: 64
+// dims of a 16-bit cache, or all 128 codes of an E4M3 cache.
 bool make_pool_map(CUtensorMap* map, const void* base, long long rows, int head_dim, int block_size,
                    pkv_dtype_t dtype) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  const bool fp8 = dtype == PKV_FP8_E4M3;
   const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, (cuuint32_t)block_size};
   const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = enc(map, dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  const CUtensorMapDataType type = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : (dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  const CUresult r = enc(map, type,
                          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -310,19 +371,21 @@ struct Plan {
   size_t pre_bytes, need;
 };
 
+// fp8: an FP8 (E4M3) cache, always on the partitioned path: the tensor-core tile
+// for head_dim 128 and any group size up to 8 (MHA included), else the CUDA cores.
 Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_context_len,
-               int partition_size) {
+               int partition_size, bool fp8) {
   Plan pl{};
   const int G = num_heads / num_kv_heads;
-  pl.mma = G >= 2 && G <= 8;
+  pl.mma = fp8 ? (G <= 8 && head_dim == 128) : (G >= 2 && G <= 8);
   pl.ng = pl.mma ? num_kv_heads : num_heads;
   pl.gc = pl.mma ? G : 1;
   const long long mb = (max_context_len + block_size - 1) / block_size;
   const long long tiles = (long long)num_seqs * pl.ng * mb;  // upper bound on the flattened tile count
   const bool stream_ok = num_seqs <= kStreamMaxSeqs && tiles < (1LL << 31);
   const int path = g_decode_path.load(std::memory_order_relaxed);
-  pl.stream = stream_ok && path == PKV_DECODE_PERSISTENT;
-  const int P = partition_size ? partition_size : kDefaultPartition;
+  pl.stream = !fp8 && stream_ok && path == PKV_DECODE_PERSISTENT;
+  const int P = partition_size ? partition_size : (fp8 ? kDefaultPartitionFp8 : kDefaultPartition);
   pl.np = max_partitions_for(max_context_len, P);
   if (pl.stream) {
     long long w = tiles < kStreamMaxWarps ? tiles : kStreamMaxWarps;
@@ -344,6 +407,159 @@ int sm_count(int dev) {
     counts[dev] = n;
   }
   return counts[dev];
+}
+
+size_t workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_context_len, int32_t partition_size, bool fp8) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
+      block_size <= 0 || max_context_len < 0 || partition_size < 0)
+    return 0;
+  return make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, partition_size, fp8)
+      .need;
+}
+
+// Both decode entry points. fp8: the caches hold E4M3 codes of value / k_scale
+// and value / v_scale.
+pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, const void* value_cache,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t max_context_len, float scale, int32_t block_size,
+                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                         pkv_dtype_t dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream, bool fp8, float k_scale, float v_scale) {
+  g_msg[0] = '\0';
+  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
+                num_kv_heads);
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (fp8 && !(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len < 0");
+  if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
+                max_context_len, (long long)max_blocks_per_seq * block_size);
+  if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
+  const int P = partition_size ? partition_size : (fp8 ? kDefaultPartitionFp8 : kDefaultPartition);
+  if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
+    return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
+                block_size, kMaxPartitionBlocks * block_size);
+  if (num_seqs > 65535 || num_heads > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
+
+  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, P, fp8);
+  if (pl.need) {
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", pl.need);
+    if (workspace_bytes < pl.need)
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, pl.need);
+    if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+
+  DecodeParams p{};
+  p.out = out;
+  p.query = query;
+  p.key_cache = static_cast<const unsigned char*>(key_cache);
+  p.value_cache = static_cast<const unsigned char*>(value_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = err;
+  p.scale_log2 = scale * 1.4426950408889634f * k_scale;
+  p.v_scale = v_scale;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.partition_size = P;
+  p.max_partitions = pl.np;
+  p.ctx_limit = max_context_len;
+
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof kmap);
+  memset(&vmap, 0, sizeof vmap);
+  if (pl.mma) {
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    const pkv_dtype_t cache_dtype = fp8 ? PKV_FP8_E4M3 : dtype;
+    if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
+        !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+  }
+
+  if (pl.stream) {
+    const int sms = sm_count(dev);
+    if (!sms) return fail(PKV_ERR_CUDA, "could not read the SM count of device %d", dev);
+    int occ = 0;
+    e = dtype == PKV_F16 ? decode_stream_occupancy_f16(head_dim, block_size, pl.mma, num_seqs, &occ)
+                         : decode_stream_occupancy_bf16(head_dim, block_size, pl.mma, num_seqs, &occ);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the persistent decode kernel");
+    if (occ < 1) occ = 1;
+    int grid = sms * occ;
+    if (grid > pl.wcap / kStreamWarps) grid = pl.wcap / kStreamWarps;
+    StreamParams sp{};
+    sp.p = p;
+    sp.num_seqs = num_seqs;
+    sp.ng = pl.ng;
+    sp.gc = pl.gc;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    sp.pre_out = reinterpret_cast<int*>(ws);
+    sp.slot_o = reinterpret_cast<float*>(ws + pl.pre_bytes);
+    sp.slot_m = sp.slot_o + (size_t)2 * pl.wcap * pl.gc * head_dim;
+    sp.slot_l = sp.slot_m + (size_t)2 * pl.wcap * pl.gc;
+    e = dtype == PKV_F16 ? decode_stream_f16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream)
+                         : decode_stream_bf16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "persistent decode kernel launch");
+    e = dtype == PKV_F16 ? stream_reduce_f16(sp, head_dim, grid * kStreamWarps, stream)
+                         : stream_reduce_bf16(sp, head_dim, grid * kStreamWarps, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+    return PKV_OK;
+  }
+
+  if (pl.need) {
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_seqs * num_heads * pl.np;
+    p.part_o = ws;
+    p.part_m = ws + rows * head_dim;
+    p.part_l = p.part_m + rows;
+  }
+  if (fp8 && pl.mma) {
+    e = dtype == PKV_F16 ? decode_mma_fp8_f16(p, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                         : decode_mma_fp8_bf16(p, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  } else if (fp8) {
+    e = dtype == PKV_F16 ? decode_simt_fp8_f16(p, head_dim, block_size, num_seqs, stream)
+                         : decode_simt_fp8_bf16(p, head_dim, block_size, num_seqs, stream);
+  } else if (pl.mma) {
+    e = dtype == PKV_F16 ? decode_mma_f16(p, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                         : decode_mma_bf16(p, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  } else {
+    e = dtype == PKV_F16 ? decode_simt_f16(p, head_dim, block_size, num_seqs, stream)
+                         : decode_simt_bf16(p, head_dim, block_size, num_seqs, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+
+  if (pl.np > 1) {
+    e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream)
+                         : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+  }
+  return PKV_OK;
 }
 
 }  // namespace
@@ -404,6 +620,43 @@ pkv_status_t paged_kv_write(const void* key, const void* value, void* key_cache,
   return PKV_OK;
 }
 
+pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_cache, void* value_cache,
+                                const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int32_t num_blocks, pkv_dtype_t dtype,
+                                float k_scale, float v_scale, cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_kv_heads <= 0 || num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (!(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key, value and caches must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+  const int pieces = head_dim / 16;  // 16 one-byte codes per 16-byte piece
+  const long long total = (long long)num_tokens * num_kv_heads * pieces;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  auto kern = dtype == PKV_F16 ? pkv_write_fp8_kernel<__half> : pkv_write_fp8_kernel<__nv_bfloat16>;
+  e = launch_kernel(kern, dim3((unsigned)blocks), dim3(threads), 0, stream, static_cast<const uint4*>(key),
+                    static_cast<const uint4*>(value), static_cast<uint4*>(key_cache),
+                    static_cast<uint4*>(value_cache), slot_mapping, num_tokens, num_kv_heads, pieces, block_size,
+                    (long long)num_blocks * block_size, k_scale, v_scale, err);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_kv_write_fp8 launch");
+  return PKV_OK;
+}
+
 int32_t pkv_set_decode_path(int32_t path) {
   if (path != PKV_DECODE_AUTO && path != PKV_DECODE_PARTITIONED && path != PKV_DECODE_PERSISTENT) return -1;
   return g_decode_path.exchange(path);
@@ -414,7 +667,8 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
                                   int32_t num_blocks, pkv_dtype_t dtype, cudaStream_t stream) {
   g_msg[0] = '\0';
   if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs < 0");
-  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
   if (num_kv_heads <= 0 || num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
   if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
   if (!supported_block_size(block_size))
@@ -429,7 +683,8 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   unsigned* err = error_word(dev);
   if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
-  const long long pieces = (long long)num_kv_heads * block_size * head_dim * 2 / 16;
+  const int elem_bytes = dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const long long pieces = (long long)num_kv_heads * block_size * head_dim * elem_bytes / 16;
   const int threads = 256;
   long long chunks = (pieces + threads * 4 - 1) / (threads * 4);  // about 4 pieces per thread
   if (chunks < 1) chunks = 1;
@@ -442,10 +697,15 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
 
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                       int32_t block_size, int32_t max_context_len, int32_t partition_size) {
-  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
-      block_size <= 0 || max_context_len < 0 || partition_size < 0)
-    return 0;
-  return make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, partition_size).need;
+  return workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, partition_size,
+                        false);
+}
+
+size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t max_context_len,
+                                          int32_t partition_size) {
+  return workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, partition_size,
+                        true);
 }
 
 pkv_status_t paged_attention_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
@@ -455,130 +715,22 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
                                     int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
                                     int32_t partition_size, void* workspace, size_t workspace_bytes,
                                     cudaStream_t stream) {
-  g_msg[0] = '\0';
-  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
-  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
-    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
-                num_kv_heads);
-  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
-    return fail(PKV_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be > 0");
-  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
-  if (!supported_block_size(block_size))
-    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
-  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
-  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len < 0");
-  if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
-    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
-                max_context_len, (long long)max_blocks_per_seq * block_size);
-  if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
-  const int P = partition_size ? partition_size : kDefaultPartition;
-  if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
-    return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
-                block_size, kMaxPartitionBlocks * block_size);
-  if (num_seqs > 65535 || num_heads > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
-  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
-    return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
-  if (num_seqs == 0) return PKV_OK;
-  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
-    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
-    return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
+  return decode_impl(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     max_context_len, scale, block_size, num_heads, num_kv_heads, head_dim, num_blocks, dtype,
+                     partition_size, workspace, workspace_bytes, stream, false, 1.f, 1.f);
+}
 
-  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, P);
-  if (pl.need) {
-    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", pl.need);
-    if (workspace_bytes < pl.need)
-      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, pl.need);
-    if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
-  }
-
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  unsigned* err = error_word(dev);
-  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
-
-  DecodeParams p{};
-  p.out = out;
-  p.query = query;
-  p.key_cache = static_cast<const unsigned char*>(key_cache);
-  p.value_cache = static_cast<const unsigned char*>(value_cache);
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.err = err;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.group = num_heads / num_kv_heads;
-  p.num_blocks = num_blocks;
-  p.partition_size = P;
-  p.max_partitions = pl.np;
-  p.ctx_limit = max_context_len;
-
-  CUtensorMap kmap, vmap;
-  memset(&kmap, 0, sizeof kmap);
-  memset(&vmap, 0, sizeof vmap);
-  if (pl.mma) {
-    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-    if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
-        !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
-      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  }
-
-  if (pl.stream) {
-    const int sms = sm_count(dev);
-    if (!sms) return fail(PKV_ERR_CUDA, "could not read the SM count of device %d", dev);
-    int occ = 0;
-    e = dtype == PKV_F16 ? decode_stream_occupancy_f16(head_dim, block_size, pl.mma, num_seqs, &occ)
-                         : decode_stream_occupancy_bf16(head_dim, block_size, pl.mma, num_seqs, &occ);
-    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the persistent decode kernel");
-    if (occ < 1) occ = 1;
-    int grid = sms * occ;
-    if (grid > pl.wcap / kStreamWarps) grid = pl.wcap / kStreamWarps;
-    StreamParams sp{};
-    sp.p = p;
-    sp.num_seqs = num_seqs;
-    sp.ng = pl.ng;
-    sp.gc = pl.gc;
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    sp.pre_out = reinterpret_cast<int*>(ws);
-    sp.slot_o = reinterpret_cast<float*>(ws + pl.pre_bytes);
-    sp.slot_m = sp.slot_o + (size_t)2 * pl.wcap * pl.gc * head_dim;
-    sp.slot_l = sp.slot_m + (size_t)2 * pl.wcap * pl.gc;
-    e = dtype == PKV_F16 ? decode_stream_f16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream)
-                         : decode_stream_bf16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "persistent decode kernel launch");
-    e = dtype == PKV_F16 ? stream_reduce_f16(sp, head_dim, grid * kStreamWarps, stream)
-                         : stream_reduce_bf16(sp, head_dim, grid * kStreamWarps, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
-    return PKV_OK;
-  }
-
-  if (pl.need) {
-    float* ws = static_cast<float*>(workspace);
-    const size_t rows = (size_t)num_seqs * num_heads * pl.np;
-    p.part_o = ws;
-    p.part_m = ws + rows * head_dim;
-    p.part_l = p.part_m + rows;
-  }
-  if (pl.mma) {
-    e = dtype == PKV_F16 ? decode_mma_f16(p, kmap, vmap, head_dim, block_size, num_seqs, stream)
-                         : decode_mma_bf16(p, kmap, vmap, head_dim, block_size, num_seqs, stream);
-  } else {
-    e = dtype == PKV_F16 ? decode_simt_f16(p, head_dim, block_size, num_seqs, stream)
-                         : decode_simt_bf16(p, head_dim, block_size, num_seqs, stream);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-
-  if (pl.np > 1) {
-    e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream)
-                         : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
-  }
-  return PKV_OK;
+pkv_status_t paged_attention_decode_fp8(void* out, const void* query, const void* key_cache,
+                                        const void* value_cache, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t max_context_len, float scale, int32_t block_size,
+                                        int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t num_blocks, pkv_dtype_t dtype, float k_scale, float v_scale,
+                                        int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+  return decode_impl(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     max_context_len, scale, block_size, num_heads, num_kv_heads, head_dim, num_blocks, dtype,
+                     partition_size, workspace, workspace_bytes, stream, true, k_scale, v_scale);
 }
 
 pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream) {

@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,7 +52,8 @@ struct DecodeParams {
   float* part_m;  // [S][H][max_partitions]
   float* part_l;  // [S][H][max_partitions]
   unsigned* err;  // per-device error word
-  float scale_log2;  // scale * log2(e): scores live in the base-2 domain
+  float scale_log2;  // scale * log2(e) (* k_scale for an FP8 cache): scores live in the base-2 domain
+  float v_scale;     // FP8 cache: value of one V code unit (1 for 16-bit caches, unused there)
   int max_blocks_per_seq;
   int num_heads;
   int num_kv_heads;
@@ -216,6 +218,29 @@ struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// cache element formats of the CUDA-core tile: C is the type of the stored K/V
+// elements. A 16-bit cache holds the inputs' bits; an E4M3 cache holds 8-bit
+// codes whose values are code * scale (the scale is applied outside the tile).
+// pair() widens the element pair in the low 2 * EB bytes of `w` (first element
+// in the lower bytes) to fp32.
+
+template <typename C>
+struct CacheFmt {
+  static constexpr int EB = 2;  // bytes per element
+  static __device__ __forceinline__ float2 pair(uint32_t w) { return Elem<C>::to_float2(w); }
+};
+
+template <>
+struct CacheFmt<__nv_fp8_e4m3> {
+  static constexpr int EB = 1;
+  // Every E4M3 value is exactly an fp16 value, so the widening is exact.
+  static __device__ __forceinline__ float2 pair(uint32_t w) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
   }
 };
 

@@ -30,20 +30,30 @@ __device__ __forceinline__ int swz_offset(int t, int piece) {
   return box * (BS * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
 }
 
-template <typename T, int D, int BS>
+template <typename T_, int D_, int BS_>
 struct MmaTile {
+  using T = T_;  // query / output type, also the cache type
+  static constexpr int D = D_;
+  static constexpr int BS = BS_;
+  static constexpr bool FP8 = false;
+  static constexpr int MIN_CTAS = PKV_DECODE_MIN_CTAS;
   static constexpr int NBOX = D / 64;       // swizzled boxes per tile (64 dims x BS rows each)
   static constexpr int BOXB = BS * 128;     // bytes of one box
   static constexpr int TILE = NBOX * BOXB;  // = BS * D * 2
   static constexpr int CH = BS >= 16 ? BS / 16 : 1;  // 16-token slices per block
   static constexpr int KT = D / 16;                  // k-steps of the score MMA / m-tiles of PV
+  using QB = uint32_t[KT][2];                        // Q^T operand registers
   static_assert(TILE == BS * D * 2, "tile bytes");
   static_assert(BOXB % 1024 == 0, "swizzle atoms need 1024-byte aligned boxes");
 
   // Q^T as the B operand of the score MMA: lane holds head n = lane / 4,
   // dims 2 (lane % 4) + {0, 1} (+ 8) of each 16-dim k-step. Heads >= G are zero.
   // `q` points at the group's first query row (G rows of D), global or shared.
-  static __device__ __forceinline__ void load_qb(uint32_t (&qb)[KT][2], const T* q, int G, int lane) {
+  // sa, sb: the score multipliers of the lane's two columns (here both sl2).
+  static __device__ __forceinline__ void load_qb(uint32_t (&qb)[KT][2], const T* q, int G, int lane, float sl2,
+                                                 float& sa, float& sb) {
+    sa = sl2;
+    sb = sl2;
     const int n_head = lane >> 2, kq = (lane & 3) * 2;
     const T* qr = q + n_head * D;
 #pragma unroll
@@ -63,8 +73,8 @@ struct MmaTile {
   // Zeroes the value rows past nvalid in shared memory (the stage then needs a
   // proxy fence before the copy engine refills it).
   static __device__ __forceinline__ void run(unsigned char* Ks, unsigned char* Vs, int nvalid,
-                                             const uint32_t (&qb)[KT][2], int lane, float sl2, float& m0,
-                                             float& m1, float& l0, float& l1, float (&acc)[KT][4]) {
+                                             const uint32_t (&qb)[KT][2], int lane, float sla, float slb,
+                                             float& m0, float& m1, float& l0, float& l1, float (&acc)[KT][4]) {
     const int mi = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix
     const int r8 = lane & 7;   // row inside that matrix
     const int r0 = lane >> 2;  // accumulator rows r0 and r0 + 8
@@ -103,10 +113,10 @@ struct MmaTile {
         const int ta = c * 16 + r0, tb = ta + 8;
         const bool va = (BS >= 16 || r0 < BS) && ta < nvalid;
         const bool vb = BS >= 16 && tb < nvalid;
-        const float x00 = va ? sacc[0] * sl2 : -INFINITY;
-        const float x01 = va ? sacc[1] * sl2 : -INFINITY;
-        const float x10 = vb ? sacc[2] * sl2 : -INFINITY;
-        const float x11 = vb ? sacc[3] * sl2 : -INFINITY;
+        const float x00 = va ? sacc[0] * sla : -INFINITY;
+        const float x01 = va ? sacc[1] * slb : -INFINITY;
+        const float x10 = vb ? sacc[2] * sla : -INFINITY;
+        const float x11 = vb ? sacc[3] * slb : -INFINITY;
         float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -151,6 +161,22 @@ struct MmaTile {
     }
   }
 
+  // The running sums are complete after every tile here.
+  static __device__ __forceinline__ void finish(float&, float&) {}
+
+  // The accumulators as red[head][dim] (head = column, dims in natural order).
+  static __device__ __forceinline__ void store_acc(float* red, const float (&acc)[KT][4], int lane) {
+    const int j0 = (lane & 3) * 2, r0 = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      const int d0 = mt * 16 + r0;
+      red[j0 * D + d0] = acc[mt][0];
+      red[(j0 + 1) * D + d0] = acc[mt][1];
+      red[j0 * D + d0 + 8] = acc[mt][2];
+      red[(j0 + 1) * D + d0 + 8] = acc[mt][3];
+    }
+  }
+
   // Issue the tensor-map copies of one (block, kv head) tile pair into a stage.
   static __device__ __forceinline__ void issue_tiles(unsigned char* st, const CUtensorMap* kmap,
                                                      const CUtensorMap* vmap, int y, uint64_t* bar) {
@@ -162,9 +188,9 @@ struct MmaTile {
   }
 };
 
-template <int D, int BS, int NW, int SPW>
+template <int D, int BS, int NW, int SPW, int TILE_BYTES = BS * D * 2>
 struct MmaShape {
-  static constexpr int TILE = BS * D * 2;
+  static constexpr int TILE = TILE_BYTES;
   static constexpr int STAGE = 2 * TILE;  // K tile + V tile
   static constexpr int RING = NW * SPW * STAGE;
   static constexpr int BARS = RING;
@@ -174,13 +200,15 @@ struct MmaShape {
   static_assert(RED_PER_WARP <= SPW * STAGE, "reduction scratch reuses the warp's ring");
 };
 
-template <typename T, int D, int BS, int NW, int SPW>
-__global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
+// Tile: MmaTile (16-bit cache) or MmaTileE4M3 (FP8 cache, pkv_decode_mma_fp8.cuh).
+template <typename Tile, int NW, int SPW>
+__global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
     pkv_decode_gqa_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
-  using Sh = MmaShape<D, BS, NW, SPW>;
-  using Tile = MmaTile<T, D, BS>;
+  using T = typename Tile::T;
+  constexpr int D = Tile::D, BS = Tile::BS;
+  using Sh = MmaShape<D, BS, NW, SPW, Tile::TILE>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -253,8 +281,9 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
   for (int i = 0; i < nfirst; ++i) issue(i);
   int issued = nfirst;
 
-  uint32_t qb[Tile::KT][2];
-  Tile::load_qb(qb, reinterpret_cast<const T*>(p.query) + row0 * D, G, lane);
+  typename Tile::QB qb;
+  float sla, slb;  // score multipliers of this lane's two columns
+  Tile::load_qb(qb, reinterpret_cast<const T*>(p.query) + row0 * D, G, lane, p.scale_log2, sla, slb);
 
   // running state of this lane's two heads (columns j0 = 2 (lane % 4), j0 + 1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -275,7 +304,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
       unsigned char* Ks = ring + k * Sh::STAGE;
       const int lb = warp + NW * i;
       const int nvalid = min(BS, tok1 - (blk0 + lb) * BS);
-      Tile::run(Ks, Ks + Sh::TILE, nvalid, qb, lane, p.scale_log2, m0, m1, l0, l1, acc);
+      Tile::run(Ks, Ks + Sh::TILE, nvalid, qb, lane, sla, slb, m0, m1, l0, l1, acc);
       if (nvalid < BS) zeroed |= 1u << k;
     }
     __syncwarp();
@@ -295,19 +324,14 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
     for (int mt = 0; mt < Tile::KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   }
 
+  Tile::finish(l0, l1);
+
   // merge the warps: each warp writes [head][D] accumulators, m, l into its own ring slice
   float* red = reinterpret_cast<float*>(ring);
   float* red_m = red + 8 * D;
   float* red_l = red_m + 8;
-  const int j0 = (lane & 3) * 2, r0 = lane >> 2;
-#pragma unroll
-  for (int mt = 0; mt < Tile::KT; ++mt) {
-    const int d0 = mt * 16 + r0;
-    red[j0 * D + d0] = acc[mt][0];
-    red[(j0 + 1) * D + d0] = acc[mt][1];
-    red[j0 * D + d0 + 8] = acc[mt][2];
-    red[(j0 + 1) * D + d0 + 8] = acc[mt][3];
-  }
+  const int j0 = (lane & 3) * 2;
+  Tile::store_acc(red, acc, lane);
   if (lane < 4) {
     red_m[j0] = m0;
     red_m[j0 + 1] = m1;
@@ -330,6 +354,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
       o += rw[g * D + d] * f;
     }
     o = L > 0.f ? o / L : 0.f;
+    if constexpr (Tile::FP8) o *= p.v_scale * Tile::UNIT;  // V codes in MMA units -> values
     const size_t row = row0 + g;
     if (direct) {
       reinterpret_cast<T*>(p.out)[row * D + d] = Elem<T>::from_float(o);
@@ -347,20 +372,20 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS)
 #define PKV_MMA_RING_BYTES (64 * 1024)  // ring bytes per CTA (build-time tuning knob)
 #endif
 
-template <int D, int BS>
+template <int STAGE_BYTES, int RING_BYTES = PKV_MMA_RING_BYTES>
 constexpr int mma_stages() {
-  constexpr int stage = 2 * BS * D * 2;
-  constexpr int spw = (PKV_MMA_RING_BYTES) / (kDecodeWarps * stage);
+  constexpr int spw = RING_BYTES / (kDecodeWarps * STAGE_BYTES);
   return spw < 1 ? 1 : (spw > 6 ? 6 : spw);
 }
 
-template <typename T, int D, int BS>
+// Tile: MmaTile<T, D, BS> or MmaTileE4M3<T, D, BS>; RING_BYTES: ring bytes per CTA.
+template <typename Tile, int RING_BYTES = PKV_MMA_RING_BYTES>
 cudaError_t launch_decode_gqa_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   int num_seqs, cudaStream_t stream) {
   constexpr int NW = kDecodeWarps;
-  constexpr int SPW = mma_stages<D, BS>();
-  using Sh = MmaShape<D, BS, NW, SPW>;
-  auto kern = pkv_decode_gqa_mma_kernel<T, D, BS, NW, SPW>;
+  constexpr int SPW = mma_stages<2 * Tile::TILE, RING_BYTES>();
+  using Sh = MmaShape<Tile::D, Tile::BS, NW, SPW, Tile::TILE>;
+  auto kern = pkv_decode_gqa_mma_kernel<Tile, NW, SPW>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -21,56 +21,85 @@
 
 namespace pkv {
 
-template <int D, int BS>
+template <int D, int BS, int EB = 2>
 struct SimtTileShape {
   static constexpr int TPC = BS < 16 ? BS : 16;  // tokens per score chunk
   static constexpr int CPB = BS / TPC;           // chunks per block
   static constexpr int LPT = 32 / TPC;           // lanes per token in the score pass
   static constexpr int DPL = D / LPT;            // head dims per lane in the score pass
-  static constexpr int NCH = DPL / 8;            // 16-byte pieces per lane in the score pass
+  static constexpr int EPP = 16 / EB;            // elements per 16-byte piece
+  static constexpr int NCH = DPL / EPP;          // 16-byte pieces per lane in the score pass
   static constexpr int DPV = D / 32;             // head dims per lane in the value pass
-  static constexpr int TILE = BS * D * 2;        // bytes of one (block, kv head) tile
-  static_assert(NCH == 2 || NCH == 4 || NCH == 8, "score-pass piece count");
+  static constexpr int ROWB = D * EB;            // bytes of one cached row
+  static constexpr int TILE = BS * ROWB;         // bytes of one (block, kv head) tile
+  static_assert(NCH == 1 || NCH == 2 || NCH == 4 || NCH == 8, "score-pass piece count");
   static_assert(DPV == 2 || DPV == 4, "value-pass width");
 };
 
-// Start piece of each lane in the score pass. Rows of a tile are 128 or 256
-// bytes apart, so without a rotation the lanes of one shared-memory phase hit
-// the same 16-byte bank group; these rotations make every phase conflict-free.
-template <int LPT, int NCH>
-__device__ __forceinline__ int qk_rotation(int lane) {
+// Start piece of each lane in the score pass. Lane (t, pt) reads row t at byte
+// pt * NCH * 16 + piece * 16. A warp's 16-byte loads are served 8 lanes at a
+// time, and the 8 lanes must hit 8 different 16-byte bank groups; rows are 64,
+// 128 or 256 bytes apart, so without a rotation several lanes of one group land
+// in the same bank group. rotation_conflict_free() checks every case below.
+template <int ROWB, int LPT, int NCH>
+__host__ __device__ constexpr int qk_rotation(int lane) {
   const int t = lane / LPT, pt = lane % LPT;
-  if constexpr (NCH >= 8) {
-    return lane & 7;
-  } else if constexpr (NCH == 4 && LPT == 2) {
-    return t & 3;
-  } else if constexpr (NCH == 4) {
-    return ((pt >> 1) + 2 * t) & 3;
-  } else {
-    return t & 1;
-  }
+  if (NCH == 1) return 0;
+  if (NCH >= 8) return lane & 7;
+  if (NCH == 4 && LPT == 2) return t & 3;
+  if (NCH == 4) return ((pt >> 1) + 2 * t) & 3;
+  if (ROWB == 64) return (t >> 1) & 1;  // NCH == 2, two lanes per 64-byte row
+  return t & 1;                          // NCH == 2, four lanes per 128-byte row
 }
 
-template <typename T, int D, int BS>
+template <int ROWB, int LPT, int NCH>
+constexpr bool rotation_conflict_free() {
+  for (int phase = 0; phase < 4; ++phase) {
+    for (int i = 0; i < NCH; ++i) {
+      unsigned used = 0;
+      for (int k = 0; k < 8; ++k) {
+        const int lane = phase * 8 + k;
+        const int piece = (i + qk_rotation<ROWB, LPT, NCH>(lane)) & (NCH - 1);
+        const int addr = (lane / LPT) * ROWB + (lane % LPT) * NCH * 16 + piece * 16;
+        const unsigned bit = 1u << ((addr / 16) % 8);
+        if (used & bit) return false;
+        used |= bit;
+      }
+    }
+  }
+  return true;
+}
+
+// T: query/output type; C: cache element type (T itself, or __nv_fp8_e4m3).
+template <typename T, typename C, int D, int BS>
 struct SimtTile {
-  using Sh = SimtTileShape<D, BS>;
+  using Fmt = CacheFmt<C>;
+  static constexpr int EB = Fmt::EB;
+  using Sh = SimtTileShape<D, BS, EB>;
+  static_assert(rotation_conflict_free<Sh::ROWB, Sh::LPT, Sh::NCH>(), "score-pass bank conflicts");
+  static constexpr int PAIR = 2 * EB;  // bytes of one element pair
+
+  static __device__ __forceinline__ int rotation(int lane) { return qk_rotation<Sh::ROWB, Sh::LPT, Sh::NCH>(lane); }
 
   // This lane's slice of one query row for the score pass, scaled into the
   // base-2 domain and stored in rotated piece order. `q` is the row's first
   // element, in global or shared memory, 16-byte aligned.
   static __device__ __forceinline__ void load_q(float (&qreg)[Sh::DPL], const T* q, int lane, float scale_log2) {
     const int pt = lane % Sh::LPT;
-    const int rot = qk_rotation<Sh::LPT, Sh::NCH>(lane);
+    const int rot = rotation(lane);
 #pragma unroll
     for (int i = 0; i < Sh::NCH; ++i) {
       const int piece = (i + rot) & (Sh::NCH - 1);
-      const uint4 raw = *reinterpret_cast<const uint4*>(q + pt * Sh::DPL + piece * 8);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = Elem<T>::to_float2(w[e]);
-        qreg[i * 8 + 2 * e] = f.x * scale_log2;
-        qreg[i * 8 + 2 * e + 1] = f.y * scale_log2;
+      for (int k = 0; k < Sh::EPP / 8; ++k) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(q + pt * Sh::DPL + piece * Sh::EPP + k * 8);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = Elem<T>::to_float2(w[e]);
+          qreg[i * Sh::EPP + k * 8 + 2 * e] = f.x * scale_log2;
+          qreg[i * Sh::EPP + k * 8 + 2 * e + 1] = f.y * scale_log2;
+        }
       }
     }
   }
@@ -81,29 +110,26 @@ struct SimtTile {
                                              const float (&qreg)[Sh::DPL], int lane, float& m, float& l,
                                              float (&acc)[Sh::DPV]) {
     const int tl = lane / Sh::LPT, pt = lane % Sh::LPT;
-    const int rot = qk_rotation<Sh::LPT, Sh::NCH>(lane);
+    const int rot = rotation(lane);
 #pragma unroll
     for (int c = 0; c < Sh::CPB; ++c) {
       if (c * Sh::TPC < nvalid) {
         // scores of this chunk's tokens: LPT lanes per token, fp32 accumulation
-        const unsigned char* krow = Ks + (c * Sh::TPC + tl) * (D * 2) + pt * (Sh::DPL * 2);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        const unsigned char* krow = Ks + (c * Sh::TPC + tl) * Sh::ROWB + pt * (Sh::NCH * 16);
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i2 = 0; i2 < Sh::NCH; ++i2) {
           const int piece = (i2 + rot) & (Sh::NCH - 1);
           const uint4 raw = *reinterpret_cast<const uint4*>(krow + piece * 16);
-          const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
-          const float2 f2 = Elem<T>::to_float2(raw.z), f3 = Elem<T>::to_float2(raw.w);
-          a0 = fmaf(qreg[i2 * 8 + 0], f0.x, a0);
-          a1 = fmaf(qreg[i2 * 8 + 1], f0.y, a1);
-          a2 = fmaf(qreg[i2 * 8 + 2], f1.x, a2);
-          a3 = fmaf(qreg[i2 * 8 + 3], f1.y, a3);
-          a0 = fmaf(qreg[i2 * 8 + 4], f2.x, a0);
-          a1 = fmaf(qreg[i2 * 8 + 5], f2.y, a1);
-          a2 = fmaf(qreg[i2 * 8 + 6], f3.x, a2);
-          a3 = fmaf(qreg[i2 * 8 + 7], f3.y, a3);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < Sh::EPP / 2; ++j) {  // element pairs of the piece
+            const float2 f = Fmt::pair(w[j * PAIR / 4] >> (8 * ((j * PAIR) % 4)));
+            a[(2 * j) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j], f.x, a[(2 * j) & 3]);
+            a[(2 * j + 1) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j + 1], f.y, a[(2 * j + 1) & 3]);
+          }
         }
-        float sc = (a0 + a1) + (a2 + a3);
+        float sc = (a[0] + a[1]) + (a[2] + a[3]);
 #pragma unroll
         for (int o = Sh::LPT / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
         const int nv = min(Sh::TPC, nvalid - c * Sh::TPC);
@@ -128,15 +154,15 @@ struct SimtTile {
         // weighted values: lane owns DPV consecutive head dims. A full chunk runs
         // without per-token branches so its loads can all be in flight at once;
         // a partial chunk never reads rows past the context.
-        const unsigned char* vrow = Vs + (c * Sh::TPC) * (D * 2) + lane * (Sh::DPV * 2);
+        const unsigned char* vrow = Vs + (c * Sh::TPC) * Sh::ROWB + lane * (Sh::DPV * EB);
         if (nv == Sh::TPC) {
 #pragma unroll
-          for (int tt = 0; tt < Sh::TPC; ++tt) pv_row(acc, __shfl_sync(kFull, pr, tt * Sh::LPT), vrow + tt * (D * 2));
+          for (int tt = 0; tt < Sh::TPC; ++tt) pv_row(acc, __shfl_sync(kFull, pr, tt * Sh::LPT), vrow + tt * Sh::ROWB);
         } else {
 #pragma unroll
           for (int tt = 0; tt < Sh::TPC; ++tt) {
             const float w = __shfl_sync(kFull, pr, tt * Sh::LPT);
-            if (tt < nv) pv_row(acc, w, vrow + tt * (D * 2));
+            if (tt < nv) pv_row(acc, w, vrow + tt * Sh::ROWB);
           }
         }
       }
@@ -145,36 +171,40 @@ struct SimtTile {
 
   // acc[e] += w * V[row][lane dims e]
   static __device__ __forceinline__ void pv_row(float (&acc)[Sh::DPV], float w, const unsigned char* v) {
-    if constexpr (Sh::DPV == 4) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(v);
-      const float2 f0 = Elem<T>::to_float2(raw.x), f1 = Elem<T>::to_float2(raw.y);
-      acc[0] = fmaf(w, f0.x, acc[0]);
-      acc[1] = fmaf(w, f0.y, acc[1]);
-      acc[2] = fmaf(w, f1.x, acc[2]);
-      acc[3] = fmaf(w, f1.y, acc[3]);
+    constexpr int BYTES = Sh::DPV * EB;  // 8, 4 or 2
+    uint32_t raw[2];
+    if constexpr (BYTES == 8) {
+      const uint2 r = *reinterpret_cast<const uint2*>(v);
+      raw[0] = r.x;
+      raw[1] = r.y;
+    } else if constexpr (BYTES == 4) {
+      raw[0] = *reinterpret_cast<const uint32_t*>(v);
     } else {
-      const uint32_t raw = *reinterpret_cast<const uint32_t*>(v);
-      const float2 f0 = Elem<T>::to_float2(raw);
-      acc[0] = fmaf(w, f0.x, acc[0]);
-      acc[1] = fmaf(w, f0.y, acc[1]);
+      raw[0] = *reinterpret_cast<const uint16_t*>(v);
+    }
+#pragma unroll
+    for (int j = 0; j < Sh::DPV / 2; ++j) {
+      const float2 f = Fmt::pair(raw[j * PAIR / 4] >> (8 * ((j * PAIR) % 4)));
+      acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
+      acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
     }
   }
 };
 
-template <int D, int BS, int NW, int SPW>
-struct SimtShape : SimtTileShape<D, BS> {
-  static constexpr int STAGE = 2 * SimtTileShape<D, BS>::TILE;  // K tile + V tile
+template <int D, int BS, int NW, int SPW, int EB = 2>
+struct SimtShape : SimtTileShape<D, BS, EB> {
+  static constexpr int STAGE = 2 * SimtTileShape<D, BS, EB>::TILE;  // K tile + V tile
   static constexpr int RING = NW * SPW * STAGE;
   static constexpr int BARS = RING;  // mbarriers follow the ring
   static constexpr int RED = BARS + ((NW * SPW * 8 + 15) / 16) * 16;
   static constexpr int SMEM = RED + NW * (D + 2) * 4;
 };
 
-template <typename T, int D, int BS, int NW, int SPW>
+template <typename T, typename C, int D, int BS, int NW, int SPW>
 __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_kernel(const DecodeParams p) {
   pdl_begin();
-  using Sh = SimtShape<D, BS, NW, SPW>;
-  using Tile = SimtTile<T, D, BS>;
+  using Tile = SimtTile<T, C, D, BS>;
+  using Sh = SimtShape<D, BS, NW, SPW, Tile::EB>;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int part = PKV_GRID_HEAD_FASTEST ? blockIdx.y : blockIdx.x;
@@ -305,7 +335,8 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_
     f[w] = red_m[w] == -INFINITY ? 0.f : fast_exp2(red_m[w] - M);
     L += red_l[w] * f[w];
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float inv = L > 0.f ? 1.f / L : 0.f;
+  if constexpr (Tile::EB == 1) inv *= p.v_scale;  // V codes -> values
   for (int d = threadIdx.x; d < D; d += NW * 32) {
     float o = 0.f;
 #pragma unroll
@@ -328,19 +359,21 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_
 #endif
 
 // Stages per warp: about PKV_SIMT_RING_BYTES of ring per CTA, 1 to 6 stages.
-template <int D, int BS>
+template <int D, int BS, int EB = 2>
 constexpr int simt_stages() {
-  constexpr int stage = 2 * BS * D * 2;
+  constexpr int stage = 2 * BS * D * EB;
   constexpr int spw = (PKV_SIMT_RING_BYTES) / (kDecodeWarps * stage);
   return spw < 1 ? 1 : (spw > 6 ? 6 : spw);
 }
 
-template <typename T, int D, int BS>
+// C: cache element type (T for a 16-bit cache, __nv_fp8_e4m3 for an FP8 cache).
+template <typename T, int D, int BS, typename C = T>
 cudaError_t launch_decode_simt(const DecodeParams& p, int num_seqs, cudaStream_t stream) {
   constexpr int NW = kDecodeWarps;
-  constexpr int SPW = simt_stages<D, BS>();
-  using Sh = SimtShape<D, BS, NW, SPW>;
-  auto kern = pkv_decode_simt_kernel<T, D, BS, NW, SPW>;
+  constexpr int EB = CacheFmt<C>::EB;
+  constexpr int SPW = simt_stages<D, BS, EB>();
+  using Sh = SimtShape<D, BS, NW, SPW, EB>;
+  auto kern = pkv_decode_simt_kernel<T, C, D, BS, NW, SPW>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                              const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
   using Sh = StreamShape<D, BS, NW, SPW, MMA>;
-  using ST = SimtTile<T, D, BS>;
+  using ST = SimtTile<T, T, D, BS>;
   using MT = MmaTile<T, D, BS>;
   const DecodeParams& p = sp.p;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -266,7 +266,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if constexpr (MMA) {
 #pragma unroll
         for (int mt = 0; mt < MT::KT; ++mt) acc_m[mt][0] = acc_m[mt][1] = acc_m[mt][2] = acc_m[mt][3] = 0.f;
-        MT::load_qb(qb, qs, gc, lane);
+        float sl_unused0, sl_unused1;
+        MT::load_qb(qb, qs, gc, lane, p.scale_log2, sl_unused0, sl_unused1);
       } else {
 #pragma unroll
         for (int e = 0; e < ST::Sh::DPV; ++e) acc_s[e] = 0.f;
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (phys >= 0) {
       const int nvalid = flags & 0xff;
       if constexpr (MMA) {
-        MT::run(st, st + Sh::TILE, nvalid, qb, lane, p.scale_log2, m, m1, l, l1, acc_m);
+        MT::run(st, st + Sh::TILE, nvalid, qb, lane, p.scale_log2, p.scale_log2, m, m1, l, l1, acc_m);
         if (nvalid < BS) zeroed |= 1u << k;
       } else {
         ST::run(st, st + Sh::TILE, nvalid, qreg, lane, m, l, acc_s);

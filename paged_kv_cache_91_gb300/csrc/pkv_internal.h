@@ -14,6 +14,18 @@ cudaError_t decode_simt_f16(const DecodeParams& p, int head_dim, int block_size,
 cudaError_t decode_simt_bf16(const DecodeParams& p, int head_dim, int block_size, int num_seqs,
                              cudaStream_t stream);
 
+// CUDA-core decode over an FP8 (E4M3) cache; T is the query/output type.
+cudaError_t decode_simt_fp8_f16(const DecodeParams& p, int head_dim, int block_size, int num_seqs,
+                                cudaStream_t stream);
+cudaError_t decode_simt_fp8_bf16(const DecodeParams& p, int head_dim, int block_size, int num_seqs,
+                                 cudaStream_t stream);
+
+// Tensor-core decode over an FP8 (E4M3) cache (head_dim 128, group <= 8, MHA included).
+cudaError_t decode_mma_fp8_f16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+cudaError_t decode_mma_fp8_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+
 // Tensor-core grouped-query decode (2 <= group <= 8; one CTA per kv head).
 cudaError_t decode_mma_f16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int block_size, int num_seqs, cudaStream_t stream);

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("paged_kv_write", "paged_attention_decode", "paged_attention_workspace_size",
               "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message", "pkv_set_decode_path",
-              "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks"):
+              "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
+              "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8"):
         assert n in names
 
 
@@ -163,3 +164,65 @@ def test_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
                 assert "liboracle" not in src and "pkv_oracle" not in src, f
+
+
+def test_fp8_workspace_is_the_partitioned_size_on_every_path(lib):
+    ws8 = lib.paged_attention_workspace_size_fp8
+    prev = lib.pkv_set_decode_path(2)  # persistent: the FP8 decode ignores it
+    try:
+        assert ws8(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
+        assert ws8(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 8 * 130 * 4  # 0 selects 1024 for FP8
+        assert ws8(256, 32, 8, 128, 16, 1024, 0) == 0
+        assert ws8(64, 40, 40, 128, 16, 512, 512) == 0
+        assert ws8(0, 40, 40, 128, 16, 4096, 0) == 0
+    finally:
+        lib.pkv_set_decode_path(prev)
+
+
+def decode_fp8(lib, **kw):
+    a = dict(out=fake(1), query=fake(2), key_cache=fake(3), value_cache=fake(4), block_tables=fake(5),
+             max_blocks_per_seq=8, context_lens=fake(6), num_seqs=2, max_context_len=128, scale=0.125,
+             block_size=16, num_heads=4, num_kv_heads=4, head_dim=64, num_blocks=16, dtype=0,
+             k_scale=0.5, v_scale=0.25, partition_size=0, workspace=None, workspace_bytes=0, stream=None)
+    a.update(kw)
+    return lib.paged_attention_decode_fp8(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k_scale=0.0), INVALID),
+    (dict(v_scale=-1.0), INVALID),
+    (dict(k_scale=float("inf")), INVALID),
+    (dict(v_scale=float("nan")), INVALID),
+    (dict(dtype=2), INVALID),                        # the query cannot be FP8
+    (dict(head_dim=96), UNSUPPORTED),
+    (dict(out=None), INVALID),
+    (dict(max_blocks_per_seq=65, max_context_len=1025), WORKSPACE),  # > 1024 (the FP8 default partition)
+])
+def test_decode_fp8_rejects_on_host(lib, kw, status):
+    assert decode_fp8(lib, **kw) == status
+    assert lib.pkv_last_error_message() != b""
+
+
+def write_fp8(lib, **kw):
+    a = dict(key=fake(1), value=fake(2), key_cache=fake(3), value_cache=fake(4), slot_mapping=fake(5),
+             num_tokens=4, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8, dtype=1, k_scale=1.0,
+             v_scale=1.0, stream=None)
+    a.update(kw)
+    return lib.paged_kv_write_fp8(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k_scale=0.0), INVALID),
+    (dict(v_scale=float("inf")), INVALID),
+    (dict(dtype=2), INVALID),
+    (dict(key=None), INVALID),
+    (dict(block_size=4), UNSUPPORTED),
+    (dict(value_cache=P(0x40001)), INVALID),
+])
+def test_write_fp8_rejects_on_host(lib, kw, status):
+    assert write_fp8(lib, **kw) == status
+
+
+def test_fp8_zero_work_is_a_noop(lib):
+    assert write_fp8(lib, num_tokens=0, key=None) == OK
+    assert decode_fp8(lib, num_seqs=0, out=None) == OK
