@@ -11,6 +11,12 @@ Two independent implementations of the same definitions:
   the full-size workloads. E4M3 (FP8) codes: ``e4m3_encode_c`` / ``e4m3_decode_c``.
 * ``write_np`` / ``decode_np`` -- numpy, fp64, gather-then-attend; plus
   ``attention_np``, unpaged attention over contiguous K/V arrays.
+* ``multi_query_c`` / ``multi_query_np`` -- several query tokens per sequence
+  (packed by ``query_start_loc``): query token i of a sequence with q_len
+  query tokens sits at position ctx - q_len + i and attends positions up to
+  its own (a_ij over j <= i: "vLLM: LLM 서빙 메모리 최적화의 교과서", 01 Problem
+  Definition; chunked prefill and speculative verification: "Sparse
+  Computation and Memory Management for Efficient LLM Inference").
 
 Decode computes, for each sequence s and query head h with kv head
 g = h // (H / Hkv) and the first ctx_s cached tokens gathered through the
@@ -76,6 +82,9 @@ def _load():
         lib.oracle_widen.restype = f64
         lib.oracle_widen.argtypes = [ctypes.c_uint16, i32]
         lib.oracle_max_threads.restype = i32
+        lib.oracle_multi_query.restype = i32
+        lib.oracle_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, f64, i32, i32, i32, i32, i64, i32,
+                                           i32, f64, f64, i32]
         _lib = lib
     return _lib
 
@@ -296,4 +305,55 @@ def decode_np(query, key_cache, value_cache, block_tables, context_lens, scale, 
             else:
                 K, V = widen_np(Kc, dtype), widen_np(Vc, dtype)
             out[s, h] = attention_np(widen_np(query[s, h], dtype), K, V, scale)
+    return out
+
+
+def multi_query_c(query, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale, dtype,
+                  num_threads: int = 0, k_scale: float = 1.0, v_scale: float = 1.0):
+    """fp64 multi-query attention; query [T][H][D] bits packed by query_start_loc [S+1]; returns out [T][H][D]."""
+    q = np.ascontiguousarray(query, dtype=np.uint16)
+    fp8 = np.asarray(key_cache).dtype == np.uint8
+    cdt = np.uint8 if fp8 else np.uint16
+    kc = np.ascontiguousarray(key_cache, dtype=cdt)
+    vc = np.ascontiguousarray(value_cache, dtype=cdt)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    T, H, D = q.shape
+    NB, Hkv, B, D2 = kc.shape
+    S = cl.shape[0]
+    assert D == D2 and vc.shape == kc.shape and bt.shape[0] == S and qsl.shape == (S + 1,)
+    assert qsl[0] == 0 and qsl[-1] == T and (np.diff(qsl) >= 0).all()
+    out = np.zeros((T, H, D), dtype=np.float64)
+    rc = _load().oracle_multi_query(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl),
+                                    _ptr(qsl), S, float(scale), B, H, Hkv, D, NB, DTYPE_CODE[dtype],
+                                    2 if fp8 else DTYPE_CODE[dtype], float(k_scale), float(v_scale),
+                                    int(num_threads))
+    if rc == -1:
+        raise ValueError("block table entry outside the pool")
+    if rc == -2:
+        raise ValueError("a sequence has more query tokens than context tokens")
+    return out
+
+
+def multi_query_np(query, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale, dtype):
+    """fp64 multi-query attention, gather then attend per query token over its causal prefix."""
+    query = np.asarray(query, dtype=np.uint16)
+    T, H, D = query.shape
+    Hkv, B = key_cache.shape[1], key_cache.shape[2]
+    group = H // Hkv
+    out = np.zeros((T, H, D), dtype=np.float64)
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    for s in range(len(context_lens)):
+        ctx = int(context_lens[s])
+        q0, q_len = int(qsl[s]), int(qsl[s + 1] - qsl[s])
+        if q_len > ctx:
+            raise ValueError("a sequence has more query tokens than context tokens")
+        for h in range(H):
+            g = h // group
+            K = widen_np(gather_np(key_cache, block_tables[s], ctx, g, B), dtype)
+            V = widen_np(gather_np(value_cache, block_tables[s], ctx, g, B), dtype)
+            for i in range(q_len):
+                n = ctx - q_len + i + 1
+                out[q0 + i, h] = attention_np(widen_np(query[q0 + i, h], dtype), K[:n], V[:n], scale)
     return out

@@ -33,6 +33,19 @@
  *                     Query head h reads kv head h / (H / Hkv) (contiguous
  *                     GQA groups). A context of 0 tokens gives o = 0.
  *
+ *   oracle_multi_query -- several query tokens per sequence (a chunked-prefill
+ *                     chunk or the tokens a speculative step verifies:
+ *                     "Sparse Computation and Memory Management for Efficient
+ *                     LLM Inference", the chunked prefill paragraph and
+ *                     Speculative Decoding). Sequence s has q_len =
+ *                     query_start_loc[s+1] - query_start_loc[s] query tokens;
+ *                     they are its last q_len context positions, and query
+ *                     token i (position p = ctx - q_len + i) attends the
+ *                     positions j <= p, as a_ij and o_i are defined over
+ *                     j <= i in "vLLM: LLM 서빙 메모리 최적화의 교과서", 01
+ *                     Problem Definition. Each output row is oracle_decode's
+ *                     formula over the first p + 1 cached tokens.
+ *
  * fp16/bf16 inputs are widened to double exactly from their bit patterns. An
  * FP8 (E4M3) cache holds codes of value / scale; its elements are code * scale,
  * computed exactly in double (oracle_write_fp8, oracle_e4m3_*).
@@ -300,6 +313,97 @@ int oracle_decode(double* out, const uint16_t* query, const void* key_cache,
                           num_blocks, dtype, cache_dtype, k_scale, v_scale, s, h);
     }
     return rc ? -1 : 0;
+}
+
+/*
+ * One (sequence, query head) pair of the multi-query case: all q_len query
+ * rows of the sequence. Returns 0, -1 on a block id outside the pool, or -2 if
+ * q_len is negative or larger than the context.
+ */
+static int mq_pair(double* out, const uint16_t* query, const void* key_cache, const void* value_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                   const int32_t* query_start_loc, double scale, int block_size, int num_heads,
+                   int num_kv_heads, int head_dim, long long num_blocks, int dtype, int cache_dtype,
+                   double k_scale, double v_scale, int s, int h) {
+    const int D = head_dim, B = block_size;
+    const int ctx = context_lens[s];
+    const int q0 = query_start_loc[s], q_len = query_start_loc[s + 1] - q0;
+    if (q_len < 0 || q_len > ctx) return -2;
+    if (q_len == 0) return 0;
+    const int group = num_heads / num_kv_heads;
+    const int g = h / group;
+
+    /* gather the sequence's K and V rows into contiguous arrays */
+    double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+    double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+    double* x = (double*)malloc(sizeof(double) * (size_t)ctx);
+    double* q = (double*)malloc(sizeof(double) * (size_t)D);
+    int rc = 0;
+    for (int j = 0; j < ctx && !rc; ++j) {
+        long long phys = block_tables[(size_t)s * max_blocks_per_seq + j / B];
+        if (phys < 0 || phys >= num_blocks) { rc = -1; break; }
+        size_t base = (((size_t)phys * num_kv_heads + g) * B + (j % B)) * D;
+        for (int d = 0; d < D; ++d) {
+            K[(size_t)j * D + d] = cache_value(key_cache, base + d, cache_dtype, k_scale);
+            V[(size_t)j * D + d] = cache_value(value_cache, base + d, cache_dtype, v_scale);
+        }
+    }
+    for (int i = 0; i < q_len && !rc; ++i) {
+        const size_t row = (size_t)(q0 + i) * num_heads + h;
+        double* o = out + row * D;
+        const int n = ctx - q_len + i + 1; /* tokens at positions 0 .. ctx - q_len + i */
+        for (int d = 0; d < D; ++d) {
+            o[d] = 0.0;
+            q[d] = widen(query[row * D + d], dtype);
+        }
+        double mx = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += q[d] * K[(size_t)j * D + d];
+            x[j] = scale * acc;
+            if (x[j] > mx) mx = x[j];
+        }
+        double den = 0.0;
+        for (int j = 0; j < n; ++j) {
+            x[j] = exp(x[j] - mx);
+            den += x[j];
+        }
+        for (int j = 0; j < n; ++j) {
+            double w = x[j] / den;
+            for (int d = 0; d < D; ++d) o[d] += w * V[(size_t)j * D + d];
+        }
+    }
+    free(K);
+    free(V);
+    free(x);
+    free(q);
+    return rc;
+}
+
+/*
+ * out: [query_start_loc[num_seqs]][H][D] doubles; query likewise (bits).
+ * query_start_loc: [num_seqs + 1] int32, non-decreasing, starting at 0.
+ * Returns 0, -1 if a block id lies outside the pool, -2 on a bad q_len.
+ */
+int oracle_multi_query(double* out, const uint16_t* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                       const int32_t* query_start_loc, int num_seqs, double scale, int block_size,
+                       int num_heads, int num_kv_heads, int head_dim, long long num_blocks, int dtype,
+                       int cache_dtype, double k_scale, double v_scale, int num_threads) {
+    long long n = (long long)num_seqs * num_heads;
+    int rc1 = 0, rc2 = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc1, rc2)
+#endif
+    for (long long i = 0; i < n; ++i) {
+        int r = mq_pair(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start_loc, scale, block_size, num_heads, num_kv_heads, head_dim, num_blocks,
+                        dtype, cache_dtype, k_scale, v_scale, (int)(i / num_heads), (int)(i % num_heads));
+        if (r == -1) rc1 = 1;
+        if (r == -2) rc2 = 1;
+    }
+    return rc1 ? -1 : (rc2 ? -2 : 0);
 }
 
 int oracle_max_threads(void) {
