@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--kv-dtype", choices=["auto", "fp8_e4m3"], default="auto",
                     help="auto: the cache holds the workload's fp16/bf16 values; fp8_e4m3: E4M3 codes "
                          "(paged_kv_write_fp8 / paged_attention_decode_fp8, k_scale = v_scale = FP8_SCALE)")
+    ap.add_argument("--query-len", type=int, default=None,
+                    help="multi-query step: each sequence's last N context tokens are written and attend causally "
+                         "(paged_attention_multi_query; speculative verification / chunked prefill)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
@@ -134,11 +137,13 @@ def step_bytes(batch, partition_size: int, cache_bytes: int = 2):
     ctx = batch.context_lens.astype(np.int64)
     kv = W.algorithmic_kv_bytes(batch) * cache_bytes // batch.elem_bytes
     S, H, D, B = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size
-    qo = 2 * S * H * D * batch.elem_bytes
+    # query rows per sequence: 1 in decode, q_len in the multi-query form
+    qlen = np.ones(S, np.int64) if batch.query_start_loc is None else np.diff(batch.query_start_loc).astype(np.int64)
+    qo = 2 * int(qlen.sum()) * H * D * batch.elem_bytes
     tables = int(((ctx + B - 1) // B).sum()) * 4 + S * 4
     nparts = (ctx + P - 1) // P
     split = nparts > 1
-    partials = int((nparts[split] * H).sum()) * (D + 2) * 4 * 2
+    partials = int((nparts[split] * qlen[split] * H).sum()) * (D + 2) * 4 * 2
     return kv, kv + qo + tables + partials
 
 
@@ -147,6 +152,7 @@ KERNEL_SOURCES = {
     "mma": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_f16.cu", "pkv_decode_mma_bf16.cu"),
     "simt_fp8": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_fp8.cu"),
     "mma_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mma_fp8.cu"),
+    "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_decode_mq.cu"),
 }
 
 
@@ -290,6 +296,21 @@ def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1, fp8_pools=None)
             return el, reps
 
 
+def time_oracle_mq(batch, budget_s: float):
+    """Run the multi-query oracle over the whole batch until budget_s; returns (seconds, reps)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.multi_query_c(batch.query, batch.key_cache, batch.value_cache, batch.block_tables,
+                             batch.context_lens, batch.query_start_loc, batch.scale, batch.dtype)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el, reps
+
+
 def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
     ctx = batch.context_lens[list(seqs)].astype("int64").sum()
     return int(ctx) * batch.num_kv_heads * batch.head_dim * 2 * cache_bytes
@@ -299,11 +320,19 @@ def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
 
 
 def workload_config(batch, n, partition_size, pool_bytes, fp8=False):
+    import numpy as np
+
     from paged_kv_cache_91_gb300 import workloads as W
 
     extra = {"query_dtype": batch.dtype, "k_scale": FP8_SCALE, "v_scale": FP8_SCALE} if fp8 else {}
+    if batch.query_start_loc is not None:
+        ql = np.diff(batch.query_start_loc)
+        extra.update({"query_tokens_per_step": int(ql.sum()), "query_len": {"min": int(ql.min()), "max": int(ql.max())},
+                      "attention": "multi-query, causal within each sequence's last query_len positions"})
     return {
-        "workload": W.CONFIG_NAMES[n] + (" with an FP8 (E4M3) KV cache" if fp8 else ""),
+        "workload": W.CONFIG_NAMES[n] + (" with an FP8 (E4M3) KV cache" if fp8 else "")
+        + ("" if batch.query_start_loc is None else
+           f", {int(np.diff(batch.query_start_loc).max())} query tokens per sequence"),
         "num_seqs": batch.num_seqs, "num_heads": batch.num_heads, "num_kv_heads": batch.num_kv_heads,
         "head_dim": batch.head_dim, "block_size": batch.block_size, "cache_dtype": "e4m3" if fp8 else batch.dtype,
         **extra,
@@ -372,17 +401,29 @@ def run_ours(args, dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     binding.load()
-    batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size)
+    batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size,
+                          query_len=args.query_len)
     P = args.partition_size
     t = W.as_torch(batch, dev)
+    mq = args.query_len is not None
+    if mq and args.kv_dtype != "auto":
+        raise SystemExit("--query-len runs on 16-bit caches only")
+    max_query_len = int(np.diff(batch.query_start_loc).max()) if mq else 1
+    n_query_rows = int(batch.query_start_loc[-1]) if mq else batch.num_seqs  # query tokens per step
     out = torch.empty_like(t["query"])
     mcl = batch.max_context_len
     if args.path:
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
     fp8 = args.kv_dtype == "fp8_e4m3"
-    wsize = binding.paged_attention_workspace_size_fp8 if fp8 else binding.paged_attention_workspace_size
-    ws_bytes = wsize(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size, mcl, P)
+    if mq:
+        ws_bytes = binding.paged_attention_multi_query_workspace_size(
+            int(batch.query_start_loc[-1]), batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+            mcl, P)
+    else:
+        wsize = binding.paged_attention_workspace_size_fp8 if fp8 else binding.paged_attention_workspace_size
+        ws_bytes = wsize(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+                         mcl, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     nparts = -(-mcl // (P or default_partition(fp8)))
@@ -408,8 +449,12 @@ def run_ours(args, dist):
         else:
             binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
 
-    def decode(q, bt, cl, o):
-        if fp8:
+    def decode(q, bt, cl, o, qsl=None):
+        if mq:
+            binding.paged_attention_multi_query(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
+                                                max_query_len=max_query_len, max_context_len=mcl, partition_size=P,
+                                                workspace=ws, stream=stream)
+        elif fp8:
             binding.paged_attention_decode_fp8(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
                                                FP8_SCALE, FP8_SCALE, max_context_len=mcl, partition_size=P,
                                                workspace=ws, stream=stream)
@@ -417,12 +462,12 @@ def run_ours(args, dist):
             binding.paged_attention_decode(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
                                            max_context_len=mcl, partition_size=P, workspace=ws, stream=stream)
 
-    def step(q, nk, nv, sm, bt, cl, o):
+    def step(q, nk, nv, sm, bt, cl, o, qsl=None):
         write(nk, nv, sm)
-        decode(q, bt, cl, o)
+        decode(q, bt, cl, o, qsl)
 
     args_dev = (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"],
-                t["context_lens"], out)
+                t["context_lens"], out, t.get("query_start_loc"))
     sampler = ClockSampler(gpu_id_for(dev))
     for _ in range(args.warmup):
         step(*args_dev)
@@ -440,7 +485,7 @@ def run_ours(args, dist):
     for k in range(K):
         write(t["new_key"], t["new_value"], t["slot_mapping"])
         ev[k][0].record(stream)
-        decode(t["query"], t["block_tables"], t["context_lens"], out)
+        decode(t["query"], t["block_tables"], t["context_lens"], out, t.get("query_start_loc"))
         ev[k][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -456,7 +501,8 @@ def run_ours(args, dist):
     e2e = None
     if not args.no_e2e:
         host = {k: t[k].cpu().pin_memory() for k in ("query", "new_key", "new_value", "slot_mapping",
-                                                      "block_tables", "context_lens")}
+                                                      "block_tables", "context_lens")
+                + (("query_start_loc",) if mq else ())}
         dbuf = {k: torch.empty_like(t[k]) for k in host}
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -466,7 +512,7 @@ def run_ours(args, dist):
             for k, v in host.items():
                 dbuf[k].copy_(v, non_blocking=True)
             step(dbuf["query"], dbuf["new_key"], dbuf["new_value"], dbuf["slot_mapping"], dbuf["block_tables"],
-                 dbuf["context_lens"], out)
+                 dbuf["context_lens"], out, dbuf.get("query_start_loc"))
             out_h.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -492,9 +538,11 @@ def run_ours(args, dist):
     value = total_kv * K / (total_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
-    workload = f"cfg{args.config}" + ("-fp8" if fp8 else "")
+    workload = f"cfg{args.config}" + ("-fp8" if fp8 else "") + (f"-q{args.query_len}" if mq else "")
     G = batch.num_heads // batch.num_kv_heads
-    if fp8:
+    if mq:
+        kind = "mq"
+    elif fp8:
         kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
     else:
         kind = "mma" if 2 <= G <= 8 else "simt"
@@ -505,11 +553,16 @@ def run_ours(args, dist):
         import oracle
 
         seqs = list(range(batch.num_seqs))
-        pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
-        el, reps = time_oracle(batch, seqs, args.cpu_seconds, fp8_pools=pools)
+        if mq:
+            el, reps = time_oracle_mq(batch, args.cpu_seconds)
+            what = "multi-query"
+        else:
+            pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
+            el, reps = time_oracle(batch, seqs, args.cpu_seconds, fp8_pools=pools)
+            what = "decode"
         cpu = {"value": round(kv_bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                "kind": "oracle",
-               "sample": f"{reps} full decode pass(es) of the workload (all {batch.num_seqs} sequences x "
+               "sample": f"{reps} full {what} pass(es) of the workload (all {batch.num_seqs} sequences x "
                          f"{batch.num_heads} heads), fp64, {el:.1f} s"}
 
     if dist.rank == 0:
@@ -520,11 +573,12 @@ def run_ours(args, dist):
             "dtype": "e4m3" if fp8 else ("f16" if batch.dtype == "f16" else "bf16"),
             "accumulate": "f32", "data": "synthetic (seeded N(0,1) K/V/q, block tables from a shuffled free list)",
             "config": workload_config(batch, args.config, P, int(batch.key_cache.nbytes * cache_bytes), fp8),
-            "tokens_per_s": round(batch.num_seqs * dist.world * K / (total_ms / 1e3), 1),
+            "tokens_per_s": round(n_query_rows * dist.world * K / (total_ms / 1e3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
                             "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
-            "roofline": {"bound": "hbm", "kernel": ("paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
-                         + " (decode kernel"
+            "roofline": {"bound": "hbm", "kernel": ("paged_attention_multi_query" if mq else
+                                                    "paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
+                         + (" (multi-query kernel" if mq else " (decode kernel")
                          + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -62,6 +62,9 @@ typedef enum {
                                   max_blocks_per_seq * block_size (clamped)               */
 #define PKV_DEVERR_SLOT 4u     /* a slot_mapping entry >= num_blocks * block_size        */
 #define PKV_DEVERR_TIMEOUT 8u  /* a wait for a bulk copy gave up after its time limit   */
+#define PKV_DEVERR_QUERY 16u   /* query_start_loc gives a sequence a negative number of
+                                  query tokens, more than max_query_len or its context,
+                                  or rows outside [0, num_query_tokens)                  */
 
 /*
  * paged_kv_write -- store the step's new keys and values in the paged pool.
@@ -273,6 +276,56 @@ pkv_status_t paged_kv_device_errors(uint32_t* flags, int32_t clear);
  * GPU fault.
  */
 pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream);
+
+/*
+ * paged_attention_multi_query -- attention of several query tokens per
+ * sequence over the paged pool: a chunked-prefill chunk batched with decode
+ * tokens, or the tokens a speculative step verifies.
+ *
+ * Source: "Sparse Computation and Memory Management for Efficient LLM
+ * Inference", the chunked prefill paragraph (prefill chunks share a step with
+ * decode tokens) and Speculative Decoding; the causal rule is a_ij and o_i
+ * over j <= i, "vLLM: LLM 서빙 메모리 최적화의 교과서", 01 Problem Definition.
+ *
+ * Sequence s has q_len = query_start_loc[s+1] - query_start_loc[s] query
+ * tokens, rows query_start_loc[s] .. + q_len - 1 of query and out. They are its
+ * last q_len context positions (their keys and values are already in the pool,
+ * written by paged_kv_write), so query token i sits at position
+ * p = context_lens[s] - q_len + i and, for every query head h,
+ *     out[query_start_loc[s] + i][h][:] = sum_{j <= p} softmax_j(x) * V_j,
+ *     x_j = scale * dot(query[query_start_loc[s] + i][h][:], K_j)
+ * with K_j, V_j as in paged_attention_decode. q_len = 1 everywhere is exactly
+ * paged_attention_decode; q_len = context_lens[s] is causal self-attention over
+ * the whole prompt.
+ *
+ *   out, query        [num_query_tokens][num_heads][head_dim], contiguous, 16-byte aligned
+ *   query_start_loc   [num_seqs + 1] int32, device memory: 0, then non-decreasing
+ *   num_query_tokens  host-side: query_start_loc[num_seqs] (rows of query and out)
+ *   max_query_len     host-side bound on every q_len; sizes the launch; <= max_context_len
+ *   partition_size    0 = 512, as in paged_attention_decode
+ *   workspace         paged_attention_multi_query_workspace_size(...) bytes
+ * Everything else is as in paged_attention_decode (the decode-path choice does
+ * not apply: this call always runs partitioned, on the tensor cores, for every
+ * group size). A sequence whose query_start_loc entries are out of order, give
+ * it more than max_query_len or context_lens[s] tokens, or reach past
+ * num_query_tokens is skipped (its rows are not written) and sets
+ * PKV_DEVERR_QUERY.
+ */
+size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int32_t num_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t block_size, int32_t max_context_len,
+                                                  int32_t partition_size);
+
+pkv_status_t paged_attention_multi_query(void* out, const void* query, const void* key_cache,
+                                         const void* value_cache, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                         const int32_t* query_start_loc, int32_t num_seqs,
+                                         int32_t num_query_tokens, int32_t max_query_len,
+                                         int32_t max_context_len, float scale, int32_t block_size,
+                                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, pkv_dtype_t dtype,
+                                         int32_t partition_size, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * FP8 KV cache. The pages pass kv_cache_dtype, k_scale and v_scale to the cache

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 _DTYPE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)  # an FP8 cache: E4M3 codes
-DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT"}
+DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT", 16: "QUERY"}
 
 _lib = None
 
@@ -63,6 +63,11 @@ def load():
     lib.paged_kv_write_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, P]
     lib.paged_attention_workspace_size_fp8.restype = sz
     lib.paged_attention_workspace_size_fp8.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_multi_query_workspace_size.restype = sz
+    lib.paged_attention_multi_query_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_multi_query.restype = i32
+    lib.paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32, i32,
+                                                i32, i32, i32, i32, P, sz, P]
     lib.paged_attention_decode_fp8.restype = i32
     lib.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
                                                f32, f32, i32, P, sz, P]
@@ -263,6 +268,57 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
         _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt, float(k_scale),
         float(v_scale), int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
+    return out
+
+
+def paged_attention_multi_query_workspace_size(num_query_tokens: int, num_heads: int, num_kv_heads: int,
+                                               head_dim: int, block_size: int, max_context_len: int,
+                                               partition_size: int = 0) -> int:
+    return int(load().paged_attention_multi_query_workspace_size(num_query_tokens, num_heads, num_kv_heads,
+                                                                 head_dim, block_size, max_context_len,
+                                                                 partition_size))
+
+
+def paged_attention_multi_query(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                query_start_loc: torch.Tensor, scale: float, max_query_len: Optional[int] = None,
+                                max_context_len: Optional[int] = None, partition_size: int = 0,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of several query tokens per sequence (query/out [T][H][D], packed by
+    query_start_loc [S+1] int32): sequence s's q_len tokens are its last q_len context positions.
+
+    ``max_query_len`` bounds every q_len on the host; when omitted it is read from
+    query_start_loc, which synchronises the stream.
+    """
+    lib = load()
+    dt = _cuda16("query", query)
+    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
+        if _cuda16(n, t) != dt:
+            raise PagedKVError(-1, f"{n} dtype differs from query")
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                 ("query_start_loc", query_start_loc)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    T, H, D2 = query.shape
+    S = context_lens.shape[0]
+    if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between query, out and caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start_loc.shape != (S + 1,):
+        raise PagedKVError(-1, "block_tables must be [S][max_blocks] and query_start_loc [S + 1]")
+    maxb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = maxb * B
+    if max_query_len is None:
+        max_query_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
+    need = int(lib.paged_attention_multi_query_workspace_size(T, H, Hkv, D, B, max_context_len, partition_size))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib, lib.paged_attention_multi_query(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
+        _ptr(context_lens), _ptr(query_start_loc), S, T, int(max_query_len), int(max_context_len), float(scale),
+        B, H, Hkv, D, NB, dt, int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
     return out
 
 

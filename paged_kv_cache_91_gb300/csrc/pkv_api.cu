@@ -12,6 +12,7 @@
 
 #include "paged_kv.h"
 #include "pkv_common.cuh"
+#include "pkv_decode_mq.cuh"
 #include "pkv_decode_stream.cuh"
 #include "pkv_internal.h"
 
@@ -149,8 +150,11 @@ __global__ void pkv_write_fp8_kernel(const uint4* __restrict__ key, const uint4*
 // ---------------------------------------------------------------------------
 // split-K reduce: merge the partitions' (m_p, l_p, o_p) of one (seq, head) by
 // log-sum-exp: out = sum_p w_p o_p / sum_p w_p with w_p = l_p 2^(m_p - max m).
-// One warp per (seq, head) row, kReduceRows rows per CTA; lane p holds the
-// weight of partition p (p < 32 per round) and each lane merges D/32 dims.
+// One warp per output row, kReduceRows rows per CTA; lane p holds the weight
+// of partition p (p < 32 per round) and each lane merges D/32 dims. An output
+// row is (seq, head) in decode, and (query token, head) in the multi-query
+// case (qsl != nullptr), whose query token's sequence is found by binary
+// search in query_start_loc.
 
 constexpr int kReduceRows = 4;
 constexpr int kReduceEarly = 4;  // partitions whose partial outputs are fetched with the first loads
@@ -159,13 +163,28 @@ template <typename T, int D>
 __global__ void __launch_bounds__(32 * kReduceRows)
     pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o, const float* __restrict__ part_m,
                       const float* __restrict__ part_l, const int32_t* __restrict__ context_lens, int num_seqs,
-                      int num_heads, int partition_size, int max_partitions, int ctx_limit) {
+                      int num_heads, int partition_size, int max_partitions, int ctx_limit, const MqParams mq) {
   pdl_begin();
   constexpr int DPL = D / 32;  // dims per lane: 4 (float4) or 2 (float2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;  // = s * num_heads + h
-  if (row >= (size_t)num_seqs * num_heads) return;
-  const int s = (int)(row / num_heads);
+  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;  // (seq or query token) * num_heads + h
+  const size_t nrows = (size_t)(mq.query_start_loc ? mq.num_query_tokens : num_seqs) * num_heads;
+  if (row >= nrows) return;
+  int s = (int)(row / num_heads);
+  if (mq.query_start_loc) {
+    // the sequence whose query rows contain this one (the last s with query_start_loc[s] <= qrow)
+    const int qrow = s;
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mq.query_start_loc[mid] <= qrow) lo = mid; else hi = mid - 1;
+    }
+    s = lo;
+    const int c = context_lens[s];
+    int q0 = 0;
+    const int n = mq_query_len(mq, s, c < 0 ? 0 : (c > ctx_limit ? ctx_limit : c), q0);
+    if (n < 0 || qrow < q0 || qrow >= q0 + n) return;  // reported by the attention kernel; row not written
+  }
   const size_t base = row * max_partitions;
   // One round of loads: the context length, this lane's partition (m, l), and the
   // partial outputs of the first partitions. All are in bounds whatever the
@@ -257,17 +276,20 @@ __global__ void __launch_bounds__(32 * kReduceRows)
   }
 }
 
+// mq.query_start_loc == nullptr: decode rows (num_seqs * num_heads).
 template <typename T>
-cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cudaStream_t stream) {
-  const size_t rows = (size_t)num_seqs * p.num_heads;
+cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cudaStream_t stream,
+                          const MqParams& mq = MqParams{}) {
+  const size_t rows = (size_t)(mq.query_start_loc ? mq.num_query_tokens : num_seqs) * p.num_heads;
   const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
   T* out = static_cast<T*>(p.out);
   const float *po = p.part_o, *pm = p.part_m, *pl = p.part_l;
   if (head_dim == 128)
     return launch_kernel(pkv_reduce_kernel<T, 128>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
-                         p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
+                         p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit,
+                         mq);
   return launch_kernel(pkv_reduce_kernel<T, 64>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
-                       p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
+                       p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit, mq);
 }
 
 // ---------------------------------------------------------------------------
@@ -731,6 +753,128 @@ pkv_status_t paged_attention_decode_fp8(void* out, const void* query, const void
   return decode_impl(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      max_context_len, scale, block_size, num_heads, num_kv_heads, head_dim, num_blocks, dtype,
                      partition_size, workspace, workspace_bytes, stream, true, k_scale, v_scale);
+}
+
+size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim, int32_t block_size, int32_t max_context_len,
+                                                  int32_t partition_size) {
+  if (num_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
+      block_size <= 0 || max_context_len < 0 || partition_size < 0)
+    return 0;
+  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int np = max_partitions_for(max_context_len, P);
+  return np > 1 ? (size_t)num_query_tokens * num_heads * np * (head_dim + 2) * sizeof(float) : 0;
+}
+
+pkv_status_t paged_attention_multi_query(void* out, const void* query, const void* key_cache,
+                                         const void* value_cache, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                         const int32_t* query_start_loc, int32_t num_seqs, int32_t num_query_tokens,
+                                         int32_t max_query_len, int32_t max_context_len, float scale,
+                                         int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs, num_query_tokens and max_query_len must be >= 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
+                num_kv_heads);
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len < 0");
+  if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
+                max_context_len, (long long)max_blocks_per_seq * block_size);
+  if (max_query_len > max_context_len)
+    return fail(PKV_ERR_INVALID_ARG, "max_query_len %d exceeds max_context_len %d", max_query_len, max_context_len);
+  if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
+  const int P = partition_size ? partition_size : kDefaultPartition;
+  if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
+    return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
+                block_size, kMaxPartitionBlocks * block_size);
+  const int G = num_heads / num_kv_heads;
+  const long long row_tiles = ((long long)max_query_len * G + 7) / 8;
+  if (num_seqs > 65535 || (long long)num_kv_heads * row_tiles > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_kv_heads * ceil(max_query_len * group / 8) must be <= 65535");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
+  if ((long long)num_query_tokens * num_heads >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "num_query_tokens * num_heads must be < 2^31");
+  if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PKV_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens || !query_start_loc)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
+  const int np = max_partitions_for(max_context_len, P);
+  const size_t need = paged_attention_multi_query_workspace_size(num_query_tokens, num_heads, num_kv_heads, head_dim,
+                                                                 block_size, max_context_len, partition_size);
+  if (need) {
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", need);
+    if (workspace_bytes < need)
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+    if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+
+  DecodeParams p{};
+  p.out = out;
+  p.query = query;
+  p.key_cache = static_cast<const unsigned char*>(key_cache);
+  p.value_cache = static_cast<const unsigned char*>(value_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = err;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.v_scale = 1.f;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = G;
+  p.num_blocks = num_blocks;
+  p.partition_size = P;
+  p.max_partitions = np;
+  p.ctx_limit = max_context_len;
+  if (need) {
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_query_tokens * num_heads * np;
+    p.part_o = ws;
+    p.part_m = ws + rows * head_dim;
+    p.part_l = p.part_m + rows;
+  }
+  MqParams mq{};
+  mq.query_start_loc = query_start_loc;
+  mq.num_query_tokens = num_query_tokens;
+  mq.max_query_len = max_query_len;
+  mq.row_tiles = (int)row_tiles;
+
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof kmap);
+  memset(&vmap, 0, sizeof vmap);
+  const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+  if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
+      !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "multi-query kernel launch");
+  if (np > 1) {
+    e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream, mq)
+                         : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream, mq);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+  }
+  return PKV_OK;
 }
 
 pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream) {

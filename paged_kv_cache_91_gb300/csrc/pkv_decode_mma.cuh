@@ -54,11 +54,16 @@ struct MmaTile {
                                                  float& sa, float& sb) {
     sa = sl2;
     sb = sl2;
-    const int n_head = lane >> 2, kq = (lane & 3) * 2;
-    const T* qr = q + n_head * D;
+    load_qb_row(qb, (lane >> 2) < G ? q + (lane >> 2) * D : nullptr, lane);
+  }
+
+  // The same operand with column n = lane / 4 taken from the query row `qr`
+  // (nullptr: a zero column).
+  static __device__ __forceinline__ void load_qb_row(uint32_t (&qb)[KT][2], const T* qr, int lane) {
+    const int kq = (lane & 3) * 2;
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
-      if (n_head < G) {
+      if (qr) {
         qb[kk][0] = *reinterpret_cast<const uint32_t*>(qr + kk * 16 + kq);
         qb[kk][1] = *reinterpret_cast<const uint32_t*>(qr + kk * 16 + 8 + kq);
       } else {
@@ -70,11 +75,15 @@ struct MmaTile {
 
   // Fold one (block, kv head) tile into the lane's running state for its two
   // heads (columns j0 = 2 (lane % 4), j0 + 1): tokens 0 .. nvalid-1 take part.
+  // CAUSAL: besides, column j0 sees only tokens whose position tok_base + t is
+  // below lim0 (lim1 for j0 + 1); a column may then see no token of a tile.
   // Zeroes the value rows past nvalid in shared memory (the stage then needs a
   // proxy fence before the copy engine refills it).
+  template <bool CAUSAL = false>
   static __device__ __forceinline__ void run(unsigned char* Ks, unsigned char* Vs, int nvalid,
                                              const uint32_t (&qb)[KT][2], int lane, float sla, float slb,
-                                             float& m0, float& m1, float& l0, float& l1, float (&acc)[KT][4]) {
+                                             float& m0, float& m1, float& l0, float& l1, float (&acc)[KT][4],
+                                             int tok_base = 0, int lim0 = 0, int lim1 = 0) {
     const int mi = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix
     const int r8 = lane & 7;   // row inside that matrix
     const int r0 = lane >> 2;  // accumulator rows r0 and r0 + 8
@@ -113,10 +122,17 @@ struct MmaTile {
         const int ta = c * 16 + r0, tb = ta + 8;
         const bool va = (BS >= 16 || r0 < BS) && ta < nvalid;
         const bool vb = BS >= 16 && tb < nvalid;
-        const float x00 = va ? sacc[0] * sla : -INFINITY;
-        const float x01 = va ? sacc[1] * slb : -INFINITY;
-        const float x10 = vb ? sacc[2] * sla : -INFINITY;
-        const float x11 = vb ? sacc[3] * slb : -INFINITY;
+        bool va0 = va, va1 = va, vb0 = vb, vb1 = vb;
+        if constexpr (CAUSAL) {
+          va0 = va && tok_base + ta < lim0;
+          va1 = va && tok_base + ta < lim1;
+          vb0 = vb && tok_base + tb < lim0;
+          vb1 = vb && tok_base + tb < lim1;
+        }
+        const float x00 = va0 ? sacc[0] * sla : -INFINITY;
+        const float x01 = va1 ? sacc[1] * slb : -INFINITY;
+        const float x10 = vb0 ? sacc[2] * sla : -INFINITY;
+        const float x11 = vb1 ? sacc[3] * slb : -INFINITY;
         float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -124,9 +140,12 @@ struct MmaTile {
           mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
         }
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - mn0), fast_exp2(x01 - mn1));
-        const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - mn0), fast_exp2(x11 - mn1));
+        // a column that has seen no token yet keeps m = -inf; exponentiate against 0 there
+        const float ms0 = CAUSAL && mn0 == -INFINITY ? 0.f : mn0;
+        const float ms1 = CAUSAL && mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+        const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - ms0), fast_exp2(x01 - ms1));
+        const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - ms0), fast_exp2(x11 - ms1));
         const float2 fa = Elem<T>::to_float2(pa), fb = Elem<T>::to_float2(pb);
         float rs0 = fa.x + fb.x, rs1 = fa.y + fb.y;
 #pragma unroll

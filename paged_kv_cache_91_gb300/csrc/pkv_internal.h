@@ -32,6 +32,13 @@ cudaError_t decode_mma_f16(const DecodeParams& p, const CUtensorMap& kmap, const
 cudaError_t decode_mma_bf16(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             int head_dim, int block_size, int num_seqs, cudaStream_t stream);
 
+// Multi-query attention (several causal query tokens per sequence; pkv_decode_mq.cuh).
+struct MqParams;
+cudaError_t decode_mq_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
+                          const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+cudaError_t decode_mq_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, cudaStream_t stream);
+
 // Persistent equal-work decode (pkv_decode_stream.cuh): CTAs per SM, launch, reduce.
 struct StreamParams;
 cudaError_t decode_stream_occupancy_f16(int head_dim, int block_size, bool mma, int num_seqs, int* ctas);

@@ -10,7 +10,9 @@ Shapes follow the pages' vocabulary ("KV Cache와 PagedAttention 완전 해부",
 §5단계; "Sparse Computation and Memory Management ...", Block-level Attention
 Formulation):
 
-  query        [S][H][D]            16-bit bit patterns (uint16)
+  query        [S][H][D]            16-bit bit patterns (uint16); with several
+                                    query tokens per sequence [T][H][D], packed
+                                    by query_start_loc [S+1] int32
   key_cache    [NB][Hkv][B][D]      one contiguous B*D tile per (block, kv head)
   value_cache  [NB][Hkv][B][D]
   block_tables [S][max_blocks]      int32, logical block -> physical block, -1 past the end
@@ -88,6 +90,7 @@ class DecodeBatch:
     new_value: np.ndarray
     partition_size: int = 512
     meta: dict = field(default_factory=dict)
+    query_start_loc: np.ndarray | None = None  # [S+1] int32 when sequences have several query tokens
 
     @property
     def num_seqs(self) -> int:
@@ -160,7 +163,7 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
                 pool_factor: float = 1.0, shared_prefix_tokens: int = 0,
                 key_outlier_frac: float = 0.0, key_outlier_scale: float = 8.0,
                 partition_size: int = 512, name: str = "custom",
-                threads: int | None = None) -> DecodeBatch:
+                threads: int | None = None, query_lens=None) -> DecodeBatch:
     """Build a seeded decode batch.
 
     Physical blocks come from a free list that is a seeded permutation of the
@@ -173,6 +176,12 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
     The step's new token of sequence s is its last context position ctx_s - 1;
     its K/V are already in the pool, and ``new_key``/``new_value`` hold a copy
     so a test can clear the slot and have the cache write restore it.
+
+    With ``query_lens`` (q_s <= ctx_s tokens per sequence) the step's new
+    tokens are each sequence's last q_s context positions, in order: a
+    chunked-prefill chunk or the tokens a speculative step verifies. Then
+    ``query`` is [sum q_s][H][D], packed by ``query_start_loc``, and
+    ``slot_mapping`` / ``new_key`` / ``new_value`` have one row per new token.
     """
     if dtype not in DTYPES:
         raise ValueError(dtype)
@@ -210,7 +219,16 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
 
     H, Hkv, D = num_heads, num_kv_heads, head_dim
     qrng = np.random.default_rng([seed, _S_QUERY])
-    query = round_f32_to(qrng.standard_normal((S, H, D), dtype=np.float32), dtype)
+    if query_lens is None:
+        qlen = (ctx > 0).astype(np.int64)
+        qsl = None
+        query = round_f32_to(qrng.standard_normal((S, H, D), dtype=np.float32), dtype)
+    else:
+        qlen = np.asarray(query_lens, dtype=np.int64)
+        if qlen.shape != ctx.shape or (qlen < 0).any() or (qlen > ctx).any():
+            raise ValueError("query_lens must give 0 <= q_s <= ctx_s per sequence")
+        qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+        query = round_f32_to(qrng.standard_normal((int(qsl[-1]), H, D), dtype=np.float32), dtype)
 
     threads = threads or max(1, min(32, os.cpu_count() or 1))
     shape = (num_blocks, Hkv, B, D)
@@ -227,18 +245,21 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
     kc[bi, :, oi, :] = CANARY[dtype]
     vc[bi, :, oi, :] = CANARY[dtype]
 
-    slot_mapping = np.full(S, -1, dtype=np.int64)
-    new_key = np.zeros((S, Hkv, D), dtype=np.uint16)
-    new_value = np.zeros((S, Hkv, D), dtype=np.uint16)
+    # one row per new token: sequence s's last qlen[s] positions (decode: row s, or -1 when ctx = 0)
+    rows = S if qsl is None else int(qsl[-1])
+    slot_mapping = np.full(rows, -1, dtype=np.int64)
+    new_key = np.zeros((rows, Hkv, D), dtype=np.uint16)
+    new_value = np.zeros((rows, Hkv, D), dtype=np.uint16)
     for s in range(S):
-        c = int(ctx[s])
-        if c == 0:
-            continue
-        phys = int(tables[s, (c - 1) // B])
-        off = (c - 1) % B
-        slot_mapping[s] = phys * B + off
-        new_key[s] = kc[phys, :, off, :]
-        new_value[s] = vc[phys, :, off, :]
+        c, n = int(ctx[s]), int(qlen[s])
+        r0 = s if qsl is None else int(qsl[s])
+        for i in range(n):
+            p = c - n + i
+            phys = int(tables[s, p // B])
+            off = p % B
+            slot_mapping[r0 + i] = phys * B + off
+            new_key[r0 + i] = kc[phys, :, off, :]
+            new_value[r0 + i] = vc[phys, :, off, :]
     live = slot_mapping[slot_mapping >= 0]
     if len(np.unique(live)) != len(live):
         raise ValueError("two sequences write the same slot")
@@ -249,7 +270,8 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
         block_tables=tables, context_lens=ctx.astype(np.int32), slot_mapping=slot_mapping,
         new_key=new_key, new_value=new_value, partition_size=partition_size,
         meta=dict(seed=seed, pool_factor=pool_factor, shared_prefix_tokens=shared_prefix_tokens,
-                  key_outlier_frac=key_outlier_frac, needed_blocks=needed))
+                  key_outlier_frac=key_outlier_frac, needed_blocks=needed),
+        query_start_loc=qsl)
 
 
 # ----------------------------------------------------------------------------
@@ -282,17 +304,20 @@ def config_context_lens(n: int) -> np.ndarray:
 
 
 def make_config(n: int, threads: int | None = None, max_seqs: int | None = None,
-                block_size: int = 16) -> DecodeBatch:
+                block_size: int = 16, query_len: int | None = None) -> DecodeBatch:
     """Workload n (1..5) at full size, or its first ``max_seqs`` sequences.
 
     ``block_size`` other than 16 gives the same contexts paged in blocks of 8 or
     32 tokens (the pages' block-size ablation; 16 is the default they report best).
+    ``query_len`` makes each sequence's last min(query_len, ctx) tokens the step's
+    query tokens (the multi-query form) instead of one decode token.
     """
     ctx = config_context_lens(n)
     if max_seqs is not None:
         ctx = ctx[:max_seqs]
     seed = 1000 + n
-    common = dict(seed=seed, context_lens=ctx, block_size=block_size, name=f"cfg{n}", threads=threads)
+    common = dict(seed=seed, context_lens=ctx, block_size=block_size, name=f"cfg{n}", threads=threads,
+                  query_lens=None if query_len is None else np.minimum(ctx, query_len))
     if n == 1:
         return build_batch(num_heads=4, num_kv_heads=4, head_dim=64, dtype=F16, num_blocks=16, **common)
     if n == 2:
@@ -357,4 +382,6 @@ def as_torch(batch: DecodeBatch, device):
         block_tables=torch.from_numpy(batch.block_tables).to(device),
         context_lens=torch.from_numpy(batch.context_lens).to(device),
         slot_mapping=torch.from_numpy(batch.slot_mapping).to(device),
+        **({} if batch.query_start_loc is None
+           else {"query_start_loc": torch.from_numpy(batch.query_start_loc).to(device)}),
     )

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     for n in ("paged_kv_write", "paged_attention_decode", "paged_attention_workspace_size",
               "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message", "pkv_set_decode_path",
               "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
-              "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8"):
+              "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
+              "paged_attention_multi_query", "paged_attention_multi_query_workspace_size"):
         assert n in names
 
 
@@ -226,3 +227,45 @@ def test_write_fp8_rejects_on_host(lib, kw, status):
 def test_fp8_zero_work_is_a_noop(lib):
     assert write_fp8(lib, num_tokens=0, key=None) == OK
     assert decode_fp8(lib, num_seqs=0, out=None) == OK
+
+
+def test_multi_query_workspace_size(lib):
+    ws = lib.paged_attention_multi_query_workspace_size
+    assert ws(100, 32, 8, 128, 16, 512, 512) == 0  # one partition
+    assert ws(100, 32, 8, 128, 16, 513, 0) == 100 * 32 * 2 * 130 * 4
+    assert ws(7, 4, 4, 64, 16, 2048, 256) == 7 * 4 * 8 * 66 * 4
+    assert ws(-1, 4, 4, 64, 16, 2048, 256) == 0
+
+
+def multi_query(lib, **kw):
+    a = dict(out=fake(1), query=fake(2), key_cache=fake(3), value_cache=fake(4), block_tables=fake(5),
+             max_blocks_per_seq=8, context_lens=fake(6), query_start_loc=fake(7), num_seqs=2, num_query_tokens=5,
+             max_query_len=4, max_context_len=128, scale=0.125, block_size=16, num_heads=8, num_kv_heads=2,
+             head_dim=64, num_blocks=16, dtype=0, partition_size=0, workspace=None, workspace_bytes=0, stream=None)
+    a.update(kw)
+    return lib.paged_attention_multi_query(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(query_start_loc=None), INVALID),
+    (dict(num_query_tokens=-1), INVALID),
+    (dict(max_query_len=-3), INVALID),
+    (dict(max_query_len=129), INVALID),                # more query tokens than the context can hold
+    (dict(num_heads=7), INVALID),
+    (dict(head_dim=80), UNSUPPORTED),
+    (dict(dtype=2), INVALID),
+    (dict(max_context_len=129), INVALID),
+    (dict(partition_size=20), UNSUPPORTED),
+    (dict(num_kv_heads=1, num_heads=64, max_query_len=128, max_blocks_per_seq=64, max_context_len=1024,
+          num_query_tokens=1 << 26), UNSUPPORTED),  # too many rows
+    (dict(max_blocks_per_seq=64, max_context_len=1024), WORKSPACE),
+])
+def test_multi_query_rejects_on_host(lib, kw, status):
+    assert multi_query(lib, **kw) == status
+    assert lib.pkv_last_error_message() != b""
+
+
+def test_multi_query_nothing_to_do_is_a_noop(lib):
+    assert multi_query(lib, num_seqs=0, out=None) == OK
+    assert multi_query(lib, num_query_tokens=0, out=None) == OK
+    assert multi_query(lib, max_query_len=0, out=None) == OK
