@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--query-len", type=int, default=None,
                     help="multi-query step: each sequence's last N context tokens are written and attend causally "
                          "(paged_attention_multi_query; speculative verification / chunked prefill)")
+    ap.add_argument("--mq-tile", choices=["auto", "columns", "rows"], default="auto",
+                    help="multi-query tile (default: the library's choice by rows per kv head)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
@@ -177,6 +179,21 @@ def ncu_traffic(workload: str, kind: str):
     if not entry or entry.get("kernel_hash") != kernel_hash(kind):
         return None
     return entry.get("dram_bytes_per_call")
+
+
+# Layers of the models the workloads are shaped after ("KV Cache와 PagedAttention 완전 해부": Qwen3-4B has 36
+# layers (§2단계); the LLaMA-2-13B example has 40 (§3단계)).
+MODEL_LAYERS = {2: ("LLaMA-2-13B", 40), 3: ("Qwen3-4B", 36), 4: ("Qwen3-4B-shaped heads", 36),
+                5: ("LLaMA-2-13B", 40)}
+
+
+def model_extrapolation(config: int, tokens_per_s_one_layer: float):
+    """Tokens/s of a model of L such layers if attention were the whole step (labelled as such)."""
+    if config not in MODEL_LAYERS:
+        return None
+    name, layers = MODEL_LAYERS[config]
+    return {"model": name, "layers": layers, "value": round(tokens_per_s_one_layer / layers, 1),
+            "note": "attention only: one layer's measured step time x layers; no projections, MLP or sampling"}
 
 
 def hbm_peak():
@@ -412,6 +429,8 @@ def run_ours(args, dist):
     n_query_rows = int(batch.query_start_loc[-1]) if mq else batch.num_seqs  # query tokens per step
     out = torch.empty_like(t["query"])
     mcl = batch.max_context_len
+    binding.set_multi_query_tile({"auto": binding.MQ_TILE_AUTO, "columns": binding.MQ_TILE_COLUMNS,
+                                  "rows": binding.MQ_TILE_ROWS}[args.mq_tile])
     if args.path:
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
@@ -477,12 +496,14 @@ def run_ours(args, dist):
     # --- device-resident timed region
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     dist.barrier()
     t_wall0 = time.time()
     start.record(stream)
     for k in range(K):
+        ev_w[k].record(stream)
         write(t["new_key"], t["new_value"], t["slot_mapping"])
         ev[k][0].record(stream)
         decode(t["query"], t["block_tables"], t["context_lens"], out, t.get("query_start_loc"))
@@ -493,6 +514,7 @@ def run_ours(args, dist):
     t_wall1 = time.time()
     total_ms = start.elapsed_time(end)
     decode_ms = [a.elapsed_time(b) for a, b in ev]
+    write_ms = [w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)]
     total_ms = dist.max(total_ms)
     dec_avg_ms = statistics.fmean(decode_ms)
     errors = binding.device_errors(clear=True)
@@ -583,6 +605,9 @@ def run_ours(args, dist):
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_call": call_bytes, "avg_call_ms": round(dec_avg_ms, 4)},
+            "write_call_ms": round(statistics.fmean(write_ms), 4),
+            "attention_only_model_tokens_per_s": model_extrapolation(args.config, n_query_rows * dist.world * K
+                                                                     / (total_ms / 1e3)),
             "gpu_launches": K * launches_per_step,
             "clocks": clocks,
             "device_errors": errors,

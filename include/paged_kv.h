@@ -311,6 +311,27 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  * num_query_tokens is skipped (its rows are not written) and sets
  * PKV_DEVERR_QUERY.
  */
+/*
+ * Multi-query tiles (pkv_set_multi_query_tile). Both compute the same result.
+ *   PKV_MQ_TILE_COLUMNS  8 (query token, head) rows of one kv head per CTA, in
+ *                        the n = 8 dimension of the MMA, the CTA's warps
+ *                        splitting the context's blocks. Reads no padding rows
+ *                        when a kv head has few rows (e.g. speculative
+ *                        verification of a few tokens).
+ *   PKV_MQ_TILE_ROWS     64 rows per CTA, 16 per warp in the MMA's M dimension,
+ *                        the warps sharing each K/V tile. Reads the context
+ *                        8 times less often for long chunks.
+ *   PKV_MQ_TILE_AUTO     ROWS when max_query_len * (num_heads / num_kv_heads)
+ *                        >= 64, else COLUMNS (default).
+ */
+#define PKV_MQ_TILE_AUTO 0
+#define PKV_MQ_TILE_COLUMNS 1
+#define PKV_MQ_TILE_ROWS 2
+
+/* Choose the multi-query tile for later calls in this process (PKV_MQ_TILE_*).
+ * Returns the previous choice, or -1 for an unknown value (nothing changes). */
+int32_t pkv_set_multi_query_tile(int32_t tile);
+
 size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int32_t num_heads,
                                                   int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t block_size, int32_t max_context_len,

@@ -65,6 +65,8 @@ def load():
     lib.paged_attention_workspace_size_fp8.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.paged_attention_multi_query_workspace_size.restype = sz
     lib.paged_attention_multi_query_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pkv_set_multi_query_tile.restype = i32
+    lib.pkv_set_multi_query_tile.argtypes = [i32]
     lib.paged_attention_multi_query.restype = i32
     lib.paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32, i32,
                                                 i32, i32, i32, i32, P, sz, P]
@@ -269,6 +271,17 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
         _ptr(context_lens), S, int(max_context_len), float(scale), B, H, Hkv, D, NB, dt, float(k_scale),
         float(v_scale), int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
     return out
+
+
+MQ_TILE_AUTO, MQ_TILE_COLUMNS, MQ_TILE_ROWS = 0, 1, 2
+
+
+def set_multi_query_tile(tile: int) -> int:
+    """Choose the multi-query tile for later calls (MQ_TILE_*); returns the previous choice."""
+    prev = int(load().pkv_set_multi_query_tile(int(tile)))
+    if prev < 0:
+        raise PagedKVError(-1, f"unknown multi-query tile {tile}")
+    return prev
 
 
 def paged_attention_multi_query_workspace_size(num_query_tokens: int, num_heads: int, num_kv_heads: int,

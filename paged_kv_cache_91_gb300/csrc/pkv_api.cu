@@ -20,6 +20,9 @@ namespace pkv {
 namespace {
 
 constexpr int kDefaultPartition = 512;
+#ifndef PKV_MQ_WIDE_MIN_ROWS
+#define PKV_MQ_WIDE_MIN_ROWS 64  // multi-query rows per kv head from which the wide tile runs (build-time knob)
+#endif
 // An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
 // weigh twice as much per byte: longer partitions measure faster.
 constexpr int kDefaultPartitionFp8 = 1024;
@@ -380,6 +383,7 @@ int max_partitions_for(int max_context_len, int partition_size) {
 }
 
 std::atomic<int> g_decode_path{PKV_DECODE_AUTO};
+std::atomic<int> g_mq_tile{PKV_MQ_TILE_AUTO};
 
 size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
@@ -679,6 +683,11 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
   return PKV_OK;
 }
 
+int32_t pkv_set_multi_query_tile(int32_t tile) {
+  if (tile != PKV_MQ_TILE_AUTO && tile != PKV_MQ_TILE_COLUMNS && tile != PKV_MQ_TILE_ROWS) return -1;
+  return g_mq_tile.exchange(tile);
+}
+
 int32_t pkv_set_decode_path(int32_t path) {
   if (path != PKV_DECODE_AUTO && path != PKV_DECODE_PARTITIONED && path != PKV_DECODE_PERSISTENT) return -1;
   return g_decode_path.exchange(path);
@@ -800,9 +809,16 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
                 block_size, kMaxPartitionBlocks * block_size);
   const int G = num_heads / num_kv_heads;
-  const long long row_tiles = ((long long)max_query_len * G + 7) / 8;
+  // Many rows per kv head go to the wide tile (64 rows per CTA, query rows in
+  // the MMA's M), a few to the 8-column tile, which reads no padding rows.
+  const int tile = g_mq_tile.load(std::memory_order_relaxed);
+  const bool wide = tile == PKV_MQ_TILE_ROWS ||
+                    (tile == PKV_MQ_TILE_AUTO && (long long)max_query_len * G >= PKV_MQ_WIDE_MIN_ROWS);
+  const int rows_per_tile = wide ? 64 : 8;
+  const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
   if (num_seqs > 65535 || (long long)num_kv_heads * row_tiles > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_kv_heads * ceil(max_query_len * group / 8) must be <= 65535");
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_kv_heads * ceil(max_query_len * group / %d) must be <= 65535",
+                rows_per_tile);
   if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
     return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
   if ((long long)num_query_tokens * num_heads >= (1LL << 31))
@@ -866,8 +882,8 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
       !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream)
-                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream)
+                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream);
   if (e != cudaSuccess) return cuda_fail(e, "multi-query kernel launch");
   if (np > 1) {
     e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream, mq)

@@ -1,6 +1,7 @@
-// Multi-query paged attention (tensor-core tile), f16 and bf16 instantiations.
+// Multi-query paged attention (8-column tile and the wide 64-row tile), f16 and bf16 instantiations.
 #include "pkv_decode_mq.cuh"
 #include "pkv_internal.h"
+#include "pkv_mq_wide.cuh"
 
 namespace pkv {
 
@@ -8,7 +9,19 @@ namespace {
 
 template <typename T>
 cudaError_t dispatch(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                     int head_dim, int block_size, int num_seqs, cudaStream_t stream) {
+                     int head_dim, int block_size, int num_seqs, bool wide, cudaStream_t stream) {
+  if (wide) {
+    if (head_dim == 128) {
+      if (block_size == 16) return launch_mq_wide<T, 128, 16>(p, mq, kmap, vmap, num_seqs, stream);
+      if (block_size == 8) return launch_mq_wide<T, 128, 8>(p, mq, kmap, vmap, num_seqs, stream);
+      if (block_size == 32) return launch_mq_wide<T, 128, 32>(p, mq, kmap, vmap, num_seqs, stream);
+    } else if (head_dim == 64) {
+      if (block_size == 16) return launch_mq_wide<T, 64, 16>(p, mq, kmap, vmap, num_seqs, stream);
+      if (block_size == 8) return launch_mq_wide<T, 64, 8>(p, mq, kmap, vmap, num_seqs, stream);
+      if (block_size == 32) return launch_mq_wide<T, 64, 32>(p, mq, kmap, vmap, num_seqs, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (head_dim == 128) {
     if (block_size == 16) return launch_mq_mma<MmaTile<T, 128, 16>>(p, mq, kmap, vmap, num_seqs, stream);
     if (block_size == 8) return launch_mq_mma<MmaTile<T, 128, 8>>(p, mq, kmap, vmap, num_seqs, stream);
@@ -24,13 +37,15 @@ cudaError_t dispatch(const DecodeParams& p, const MqParams& mq, const CUtensorMa
 }  // namespace
 
 cudaError_t decode_mq_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                          const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, cudaStream_t stream) {
-  return dispatch<__half>(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+                          const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, bool wide,
+                          cudaStream_t stream) {
+  return dispatch<__half>(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream);
 }
 
 cudaError_t decode_mq_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, cudaStream_t stream) {
-  return dispatch<__nv_bfloat16>(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, bool wide,
+                           cudaStream_t stream) {
+  return dispatch<__nv_bfloat16>(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream);
 }
 
 }  // namespace pkv

@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
               "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message", "pkv_set_decode_path",
               "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
               "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
-              "paged_attention_multi_query", "paged_attention_multi_query_workspace_size"):
+              "paged_attention_multi_query", "paged_attention_multi_query_workspace_size",
+              "pkv_set_multi_query_tile"):
         assert n in names
 
 
@@ -269,3 +270,13 @@ def test_multi_query_nothing_to_do_is_a_noop(lib):
     assert multi_query(lib, num_seqs=0, out=None) == OK
     assert multi_query(lib, num_query_tokens=0, out=None) == OK
     assert multi_query(lib, max_query_len=0, out=None) == OK
+
+
+def test_multi_query_tile_switch(lib):
+    prev = lib.pkv_set_multi_query_tile(2)
+    try:
+        assert lib.pkv_set_multi_query_tile(1) == 2
+        assert lib.pkv_set_multi_query_tile(9) == -1
+        assert lib.pkv_set_multi_query_tile(0) == 1
+    finally:
+        lib.pkv_set_multi_query_tile(prev)

@@ -21,10 +21,14 @@ RTOL = 1e-2
 DEV = "cuda:0"
 
 
-@pytest.fixture(autouse=True)
-def clean_errors(cuda_lib):
+@pytest.fixture(autouse=True, params=["columns", "rows"])
+def mq_tile(request, cuda_lib):
+    """Every test runs on both multi-query tiles (they must give the same results)."""
+    prev = binding.set_multi_query_tile(binding.MQ_TILE_COLUMNS if request.param == "columns"
+                                        else binding.MQ_TILE_ROWS)
     binding.device_errors(clear=True)
-    yield
+    yield request.param
+    binding.set_multi_query_tile(prev)
 
 
 def as_bits(t: torch.Tensor) -> np.ndarray:
