@@ -123,8 +123,10 @@ class Dist:
 # byte accounting
 
 
-def default_partition(fp8: bool) -> int:
-    """The library's partition size when the call passes 0 (longer for an FP8 cache)."""
+def default_partition(fp8: bool, mq: bool = False, block_size: int = 16) -> int:
+    """The library's partition size when the call passes 0 (longer for an FP8 cache and for multi-query)."""
+    if mq:
+        return min(2048, 128 * block_size)
     return 1024 if fp8 else 512
 
 
@@ -135,7 +137,7 @@ def step_bytes(batch, partition_size: int, cache_bytes: int = 2):
 
     from paged_kv_cache_91_gb300 import workloads as W
 
-    P = partition_size or default_partition(cache_bytes == 1)
+    P = partition_size or default_partition(cache_bytes == 1, batch.query_start_loc is not None, batch.block_size)
     ctx = batch.context_lens.astype(np.int64)
     kv = W.algorithmic_kv_bytes(batch) * cache_bytes // batch.elem_bytes
     S, H, D, B = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size
@@ -154,7 +156,7 @@ KERNEL_SOURCES = {
     "mma": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_f16.cu", "pkv_decode_mma_bf16.cu"),
     "simt_fp8": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_fp8.cu"),
     "mma_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mma_fp8.cu"),
-    "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_decode_mq.cu"),
+    "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_mq_wide.cuh", "pkv_decode_mq.cu"),
 }
 
 
@@ -355,7 +357,8 @@ def workload_config(batch, n, partition_size, pool_bytes, fp8=False):
         **extra,
         "context_lens": {"min": int(batch.context_lens.min()), "mean": float(batch.context_lens.mean()),
                          "max": int(batch.context_lens.max())},
-        "partition_size": partition_size or default_partition(fp8),
+        "partition_size": partition_size or default_partition(fp8, batch.query_start_loc is not None,
+                                                              batch.block_size),
         "new_tokens_per_step": int((batch.slot_mapping >= 0).sum()),
         "pool_bytes": pool_bytes,
         "l2": "inputs larger than L2 (KV pool > 129 MB); no flush between steps",
@@ -445,7 +448,7 @@ def run_ours(args, dist):
                          mcl, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    nparts = -(-mcl // (P or default_partition(fp8)))
+    nparts = -(-mcl // (P or default_partition(fp8, mq, batch.block_size)))
     launches_per_step = 2 + (1 if nparts > 1 else 0)
     cache_bytes = 1 if fp8 else 2
     kv_bytes, call_bytes = step_bytes(batch, P, cache_bytes)

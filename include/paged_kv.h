@@ -302,7 +302,9 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *   query_start_loc   [num_seqs + 1] int32, device memory: 0, then non-decreasing
  *   num_query_tokens  host-side: query_start_loc[num_seqs] (rows of query and out)
  *   max_query_len     host-side bound on every q_len; sizes the launch; <= max_context_len
- *   partition_size    0 = 512, as in paged_attention_decode
+ *   partition_size    0 = 2048 tokens, capped at 128 blocks (every query row
+ *                     writes a partial per partition, so long partitions are
+ *                     fastest here); else as in paged_attention_decode
  *   workspace         paged_attention_multi_query_workspace_size(...) bytes
  * Everything else is as in paged_attention_decode (the decode-path choice does
  * not apply: this call always runs partitioned, on the tensor cores, for every

@@ -26,6 +26,13 @@ constexpr int kDefaultPartition = 512;
 // An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
 // weigh twice as much per byte: longer partitions measure faster.
 constexpr int kDefaultPartitionFp8 = 1024;
+// Multi-query: every query row writes D + 2 partial floats per partition, so
+// few long partitions measure fastest (capped at kMaxPartitionBlocks blocks).
+constexpr int kDefaultPartitionMq = 2048;
+int mq_default_partition(int block_size) {
+  const int cap = kMaxPartitionBlocks * block_size;
+  return kDefaultPartitionMq < cap ? kDefaultPartitionMq : cap;
+}
 constexpr int kMaxDevices = 64;
 
 thread_local char g_msg[512] = "";
@@ -770,7 +777,7 @@ size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int3
   if (num_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
       block_size <= 0 || max_context_len < 0 || partition_size < 0)
     return 0;
-  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int P = partition_size ? partition_size : mq_default_partition(block_size);
   const int np = max_partitions_for(max_context_len, P);
   return np > 1 ? (size_t)num_query_tokens * num_heads * np * (head_dim + 2) * sizeof(float) : 0;
 }
@@ -804,7 +811,7 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   if (max_query_len > max_context_len)
     return fail(PKV_ERR_INVALID_ARG, "max_query_len %d exceeds max_context_len %d", max_query_len, max_context_len);
   if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
-  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int P = partition_size ? partition_size : mq_default_partition(block_size);
   if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
                 block_size, kMaxPartitionBlocks * block_size);

@@ -36,8 +36,12 @@ struct MqWideShape {
   static_assert(TILE % 1024 == 0 || BS * 128 % 1024 == 0, "swizzle atoms need 1024-byte aligned boxes");
 };
 
+#ifndef PKV_MQ_WIDE_MIN_CTAS
+#define PKV_MQ_WIDE_MIN_CTAS 3  // __launch_bounds__ minimum CTAs per SM (build-time tuning knob)
+#endif
+
 template <typename T, int D, int BS, int NW, int ST>
-__global__ void __launch_bounds__(NW * 32, 2)
+__global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
     pkv_mq_wide_kernel(const DecodeParams p, const MqParams mq, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
@@ -192,16 +196,28 @@ __global__ void __launch_bounds__(NW * 32, 2)
         if (c * 16 < nvalid) {
           const int nv = min(16, nvalid - c * 16);  // valid tokens of this 16-token chunk
           // S = Q . K^T for 16 tokens (n-tile 0: tokens 0-7, n-tile 1: 8-15)
+          // (four accumulation chains: even and odd k-steps of each n-tile)
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
           {
+            float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
             const int tk = (mi >> 1) * 8 + r8;
             const int t = BS >= 16 ? c * 16 + tk : (tk & (BS - 1));
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
               uint32_t b[4];
               ldmatrix_x4(b, Ks + swz_offset<BS>(t, 2 * kk + (mi & 1)));
-              Mma<T>::run(s0, qa[kk], b[0], b[1]);
-              Mma<T>::run(s1, qa[kk], b[2], b[3]);
+              if (kk & 1) {
+                Mma<T>::run(s2, qa[kk], b[0], b[1]);
+                Mma<T>::run(s3, qa[kk], b[2], b[3]);
+              } else {
+                Mma<T>::run(s0, qa[kk], b[0], b[1]);
+                Mma<T>::run(s1, qa[kk], b[2], b[3]);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              s0[e] += s2[e];
+              s1[e] += s3[e];
             }
           }
           // masks: chunk token u at position base + c*16 + u sees row A iff u < nv and position < limA

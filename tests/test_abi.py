@@ -233,7 +233,9 @@ def test_fp8_zero_work_is_a_noop(lib):
 def test_multi_query_workspace_size(lib):
     ws = lib.paged_attention_multi_query_workspace_size
     assert ws(100, 32, 8, 128, 16, 512, 512) == 0  # one partition
-    assert ws(100, 32, 8, 128, 16, 513, 0) == 100 * 32 * 2 * 130 * 4
+    assert ws(100, 32, 8, 128, 16, 513, 512) == 100 * 32 * 2 * 130 * 4
+    assert ws(100, 32, 8, 128, 16, 2048, 0) == 0  # 0 selects 2048 tokens
+    assert ws(100, 32, 8, 128, 8, 2048, 0) == 100 * 32 * 2 * 130 * 4  # capped at 128 blocks of 8
     assert ws(7, 4, 4, 64, 16, 2048, 256) == 7 * 4 * 8 * 66 * 4
     assert ws(-1, 4, 4, 64, 16, 2048, 256) == 0
 
@@ -259,7 +261,7 @@ def multi_query(lib, **kw):
     (dict(partition_size=20), UNSUPPORTED),
     (dict(num_kv_heads=1, num_heads=64, max_query_len=128, max_blocks_per_seq=64, max_context_len=1024,
           num_query_tokens=1 << 26), UNSUPPORTED),  # too many rows
-    (dict(max_blocks_per_seq=64, max_context_len=1024), WORKSPACE),
+    (dict(max_blocks_per_seq=200, max_context_len=3000), WORKSPACE),
 ])
 def test_multi_query_rejects_on_host(lib, kw, status):
     assert multi_query(lib, **kw) == status
