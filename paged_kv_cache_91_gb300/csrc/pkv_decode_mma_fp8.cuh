@@ -8,26 +8,24 @@
 // 16 x 16 x 8 multiply-add step per instruction, where the CUDA cores would
 // spend one instruction per element and head.
 //
-// Widening. Every E4M3 value times 2^-8 is exactly an f16 value with the bit
-// pattern sign << 15 | (code & 0x7f) << 7 (E4M3's exponent bias is 7, f16's 15,
-// and E4M3 subnormals land on f16 subnormals). With two codes in the low bytes
-// of the two 16-bit halves of a word u, the f16 pair is (u + (u & 0x00800080))
-// << 7: a byte permute, a mask and an add-shift, where the conversion
-// instruction would occupy the integer pipe four times as long. The 2^-8 of K
-// goes into the score multiplier, that of V into the output multiplier.
+// Widening. Every E4M3 value is exactly an f16 value. One conversion
+// instruction widens the two codes of a 16-bit half of a register into an f16
+// pair; applied to the two halves of a loaded word it costs about one
+// integer-pipe instruction per pair, half of what an integer bit rearrangement
+// or the conversion intrinsic's repacking costs (measured on this GPU).
 //
 // Layout. The tile arrives through a 2D tensor map as BS rows of 128 bytes
 // (D = 128 codes) with the 128-byte swizzle: 16-byte chunk c of row t sits at
 // chunk position c ^ (t % 8). Lane (g = lane / 4, qd = lane % 4) uses only whole
 // 16-byte chunks, each one conflict-free load, by choosing which head dim sits
 // at which MMA position:
-//   score MMA, k-step j: positions 2qd, 2qd+1 are dims 32qd + 4j + 0, + 2 and
-//     positions 2qd+8, 2qd+9 are dims 32qd + 4j + 1, + 3 (the even and odd bytes
-//     of one word), so the lane reads bytes 32qd .. 32qd+31 of token rows g and
-//     g + 8; Q^T uses the same dim order.
+//   score MMA, k-step j: positions 2qd, 2qd+1 are dims 32qd + 4j + 0, + 1 and
+//     positions 2qd+8, 2qd+9 are dims 32qd + 4j + 2, + 3 (the two halves of one
+//     word), so the lane reads bytes 32qd .. 32qd+31 of token rows g and g + 8;
+//     Q^T uses the same dim order.
 //   PV MMA, m-tile i: row g is dim 16g + 2i, row g + 8 is dim 16g + 2i + 1, so
 //     the lane needs chunk g of token rows 2qd, 2qd+1, 2qd+8, 2qd+9; a byte
-//     permute pairs the two token rows of each A-fragment word.
+//     permute pairs the two token rows of each dim in a 16-bit half.
 // Every dim still meets every other factor once, so S and O are unchanged.
 //
 // The MMA multiplies f16 by f16. An f16 query is used as it is. A bf16 query is
@@ -50,10 +48,12 @@ namespace pkv {
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
 
-// f16x2 of 2^-8 times the E4M3 values of the codes in bytes 0 and 2 of u (bytes
-// 1 and 3 are ignored).
-__device__ __forceinline__ uint32_t e4m3_even_to_f16x2(uint32_t u) {
-  return ((u & 0x007f007fu) + ((u & 0x00800080u) << 1)) << 7;
+// The E4M3 codes of w as two f16 pairs: lo = (byte 0, byte 1), hi = (byte 2,
+// byte 3), the first code of each pair in the low half. Exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 template <typename T_, int D_, int BS_>
@@ -62,7 +62,7 @@ struct MmaTileE4M3 {
   static constexpr int D = D_;
   static constexpr int BS = BS_;
   static constexpr bool FP8 = true;
-  static constexpr float UNIT = 256.f;  // K and V enter the MMAs as value * 2^-8
+  static constexpr float UNIT = 1.f;  // K and V enter the MMAs at their code values
   static constexpr int MIN_CTAS = PKV_MMA_FP8_MIN_CTAS;  // resident CTAs per SM the registers must allow
   static_assert(D == 128, "one 128-byte swizzle span per cached row");
   static constexpr int TILE = BS * D;                // bytes of one (block, kv head) tile
@@ -75,9 +75,9 @@ struct MmaTileE4M3 {
   static __device__ __forceinline__ int off(int t, int c) { return t * 128 + ((c ^ (t & 7)) << 4); }
 
   // Q^T as the B operand: lane (head g = lane / 4, quad qd) holds, for k-step j,
-  // dims 32qd + 4j + {0, 2} (qb[j][0]) and + {1, 3} (qb[j][1]) of head g in
-  // f16. sa, sb: sl2 * 2^8 * 2^-k of the lane's columns (heads 2qd, 2qd + 1).
-  // Heads >= G are zero.
+  // dims 32qd + 4j + {0, 1} (qb[j][0]) and + {2, 3} (qb[j][1]) of head g in
+  // f16. sa, sb: sl2 * 2^-k of the lane's columns (heads 2qd, 2qd + 1). Heads
+  // >= G are zero.
   static __device__ __forceinline__ void load_qb(QB& qb, const T* q, int G, int lane, float sl2, float& sa,
                                                  float& sb) {
     const int g = lane >> 2, qd = lane & 3;
@@ -121,8 +121,8 @@ struct MmaTileE4M3 {
     // w[2j] holds dims 4j, 4j+1 and w[2j+1] dims 4j+2, 4j+3 (relative to 32qd)
 #pragma unroll
     for (int j = 0; j < KT; ++j) {
-      qb[j][0] = prmt(w[2 * j], w[2 * j + 1], 0x5410);  // dims 4j, 4j+2
-      qb[j][1] = prmt(w[2 * j], w[2 * j + 1], 0x7632);  // dims 4j+1, 4j+3
+      qb[j][0] = w[2 * j];
+      qb[j][1] = w[2 * j + 1];
     }
     sa = sl2 * UNIT * __shfl_sync(kFull, inv, (2 * qd) * 4);
     sb = sl2 * UNIT * __shfl_sync(kFull, inv, (2 * qd + 1) * 4);
@@ -130,7 +130,7 @@ struct MmaTileE4M3 {
 
   // Fold one (block, kv head) tile into the lane's running state for its two
   // heads (columns 2 (lane % 4) and + 1): tokens 0 .. nvalid-1 take part. acc is
-  // in units of 2^-8 V. Zeroes the value rows past nvalid in shared memory (the
+  // in V's code units. Zeroes the value rows past nvalid in shared memory (the
   // stage then needs a proxy fence before the copy engine refills it).
   static __device__ __forceinline__ void run(unsigned char* Ks, unsigned char* Vs, int nvalid, const QB& qb,
                                              int lane, float sla, float slb, float& m0, float& m1, float& l0,
@@ -158,8 +158,9 @@ struct MmaTileE4M3 {
         float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < KT; ++j) {
-          const uint32_t a[4] = {e4m3_even_to_f16x2(wa[j]), e4m3_even_to_f16x2(wb[j]),
-                                 e4m3_even_to_f16x2(wa[j] >> 8), e4m3_even_to_f16x2(wb[j] >> 8)};
+          uint32_t a[4];  // rows g, g + 8 at positions 2qd.. (dims +0, +1) and 2qd+8.. (dims +2, +3)
+          e4m3x4_to_f16x2(wa[j], a[0], a[2]);
+          e4m3x4_to_f16x2(wb[j], a[1], a[3]);
           if (j & 1) {
             Mma<__half>::run(sacc2, a, qb[j][0], qb[j][1]);
           } else {
@@ -217,17 +218,18 @@ struct MmaTileE4M3 {
         const uint32_t x8[4] = {X8.x, X8.y, X8.z, X8.w}, x9[4] = {X9.x, X9.y, X9.z, X9.w};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          // byte b of word w is dim 16g + 4w + b. q.. = [r.b0, r.b1, r'.b0, r'.b1]
-          // and r.. = [r.b2, r.b3, r'.b2, r'.b3] for the token rows (r, r'): the even
-          // bytes pair the two rows at one dim, the odd bytes at the next dim
-          const uint32_t q01 = prmt(x0[w], x1[w], 0x5410), r01 = prmt(x0[w], x1[w], 0x7632);
-          const uint32_t q89 = prmt(x8[w], x9[w], 0x5410), r89 = prmt(x8[w], x9[w], 0x7632);
+          // byte b of word w is dim 16g + 4w + b. For the token rows (r, r'):
+          // lo = [r.b0, r'.b0, r.b1, r'.b1] and hi = [r.b2, r'.b2, r.b3, r'.b3], so
+          // each 16-bit half pairs the two rows at one dim
+          const uint32_t lo01 = prmt(x0[w], x1[w], 0x5140), hi01 = prmt(x0[w], x1[w], 0x7362);
+          const uint32_t lo89 = prmt(x8[w], x9[w], 0x5140), hi89 = prmt(x8[w], x9[w], 0x7362);
           // m-tile 2w: dims 16g + 4w (row g) and + 1 (row g + 8); m-tile 2w + 1: + 2 and + 3
-          const uint32_t ae[4] = {e4m3_even_to_f16x2(q01), e4m3_even_to_f16x2(q01 >> 8), e4m3_even_to_f16x2(q89),
-                                  e4m3_even_to_f16x2(q89 >> 8)};
+          uint32_t ae[4], ao[4];
+          e4m3x4_to_f16x2(lo01, ae[0], ae[1]);
+          e4m3x4_to_f16x2(lo89, ae[2], ae[3]);
+          e4m3x4_to_f16x2(hi01, ao[0], ao[1]);
+          e4m3x4_to_f16x2(hi89, ao[2], ao[3]);
           Mma<__half>::run(acc[2 * w], ae, b0, b1);
-          const uint32_t ao[4] = {e4m3_even_to_f16x2(r01), e4m3_even_to_f16x2(r01 >> 8), e4m3_even_to_f16x2(r89),
-                                  e4m3_even_to_f16x2(r89 >> 8)};
           Mma<__half>::run(acc[2 * w + 1], ao, b0, b1);
         }
       }
