@@ -242,6 +242,16 @@ struct CacheFmt<__nv_fp8_e4m3> {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
     return __half22float2(*reinterpret_cast<const __half2*>(&h));
   }
+  // The four codes of w as two pairs: lo = (byte 0, byte 1), hi = (byte 2, byte 3).
+  // One conversion instruction per 16-bit half of the register.
+  static __device__ __forceinline__ void quad(uint32_t w, float2& lo, float2& hi) {
+    uint32_t a, b;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(a), "=r"(b)
+        : "r"(w));
+    lo = __half22float2(*reinterpret_cast<const __half2*>(&a));
+    hi = __half22float2(*reinterpret_cast<const __half2*>(&b));
+  }
 };
 
 // ---------------------------------------------------------------------------

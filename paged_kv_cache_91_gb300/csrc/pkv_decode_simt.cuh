@@ -124,7 +124,16 @@ struct SimtTile {
           const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int j = 0; j < Sh::EPP / 2; ++j) {  // element pairs of the piece
-            const float2 f = Fmt::pair(w[j * PAIR / 4] >> (8 * ((j * PAIR) % 4)));
+            float2 f;
+            if constexpr (EB == 1) {
+              if (j & 1) continue;  // pairs j, j + 1 come from one word
+              float2 f2;
+              Fmt::quad(w[j / 2], f, f2);
+              a[(2 * j + 2) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j + 2], f2.x, a[(2 * j + 2) & 3]);
+              a[(2 * j + 3) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j + 3], f2.y, a[(2 * j + 3) & 3]);
+            } else {
+              f = Fmt::pair(w[j]);
+            }
             a[(2 * j) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j], f.x, a[(2 * j) & 3]);
             a[(2 * j + 1) & 3] = fmaf(qreg[i2 * Sh::EPP + 2 * j + 1], f.y, a[(2 * j + 1) & 3]);
           }
@@ -182,11 +191,20 @@ struct SimtTile {
     } else {
       raw[0] = *reinterpret_cast<const uint16_t*>(v);
     }
+    if constexpr (EB == 1 && Sh::DPV == 4) {
+      float2 f0, f1;
+      Fmt::quad(raw[0], f0, f1);
+      acc[0] = fmaf(w, f0.x, acc[0]);
+      acc[1] = fmaf(w, f0.y, acc[1]);
+      acc[2] = fmaf(w, f1.x, acc[2]);
+      acc[3] = fmaf(w, f1.y, acc[3]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < Sh::DPV / 2; ++j) {
-      const float2 f = Fmt::pair(raw[j * PAIR / 4] >> (8 * ((j * PAIR) % 4)));
-      acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
-      acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
+      for (int j = 0; j < Sh::DPV / 2; ++j) {
+        const float2 f = Fmt::pair(raw[j * PAIR / 4] >> (8 * ((j * PAIR) % 4)));
+        acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
+        acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
+      }
     }
   }
 };
