@@ -67,7 +67,7 @@ def parse_args():
     ap.add_argument("--query-len", type=int, default=None,
                     help="multi-query step: each sequence's last N context tokens are written and attend causally "
                          "(paged_attention_multi_query; speculative verification / chunked prefill)")
-    ap.add_argument("--mq-tile", choices=["auto", "columns", "rows"], default="auto",
+    ap.add_argument("--mq-tile", choices=["auto", "columns", "rows", "tensor"], default="auto",
                     help="multi-query tile (default: the library's choice by rows per kv head)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -156,7 +156,8 @@ KERNEL_SOURCES = {
     "mma": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_f16.cu", "pkv_decode_mma_bf16.cu"),
     "simt_fp8": ("pkv_common.cuh", "pkv_decode_simt.cuh", "pkv_decode_simt_fp8.cu"),
     "mma_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mma_fp8.cu"),
-    "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_mq_wide.cuh", "pkv_decode_mq.cu"),
+    "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_mq_wide.cuh", "pkv_mq_tc.cuh",
+           "pkv_tcgen05.cuh", "pkv_decode_mq.cu"),
 }
 
 
@@ -338,6 +339,21 @@ def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
 # ----------------------------------------------------------------------------
 
 
+def mq_summary(batch, tile_arg, call_ms):
+    """The multi-query tile that ran and the rate of its attention arithmetic (causal QK and PV, 4 flops per
+    (row, visible position, dim))."""
+    import numpy as np
+
+    ql = np.diff(batch.query_start_loc).astype(np.int64)
+    ctx = batch.context_lens.astype(np.int64)
+    vis = (ql * (ctx - ql) + ql * (ql + 1) // 2).sum()  # positions seen, summed over query tokens
+    flops = 4.0 * batch.head_dim * batch.num_heads * float(vis)
+    rows_per_kv_head = int(ql.max()) * (batch.num_heads // batch.num_kv_heads)
+    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head >= 64 else "columns")
+    return {"tile": tile, "rows_per_kv_head": rows_per_kv_head, "attention_gflop_per_call": round(flops / 1e9, 2),
+            "attention_tflops": round(flops / (call_ms * 1e-3) / 1e12, 1)}
+
+
 def workload_config(batch, n, partition_size, pool_bytes, fp8=False):
     import numpy as np
 
@@ -433,7 +449,7 @@ def run_ours(args, dist):
     out = torch.empty_like(t["query"])
     mcl = batch.max_context_len
     binding.set_multi_query_tile({"auto": binding.MQ_TILE_AUTO, "columns": binding.MQ_TILE_COLUMNS,
-                                  "rows": binding.MQ_TILE_ROWS}[args.mq_tile])
+                                  "rows": binding.MQ_TILE_ROWS, "tensor": binding.MQ_TILE_TENSOR}[args.mq_tile])
     if args.path:
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
@@ -617,6 +633,8 @@ def run_ours(args, dist):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if mq:
+            line["multi_query"] = mq_summary(batch, args.mq_tile, dec_avg_ms)
         print(json.dumps(line), flush=True)
 
 

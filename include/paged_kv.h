@@ -65,6 +65,8 @@ typedef enum {
 #define PKV_DEVERR_QUERY 16u   /* query_start_loc gives a sequence a negative number of
                                   query tokens, more than max_query_len or its context,
                                   or rows outside [0, num_query_tokens)                  */
+#define PKV_DEVERR_LAYOUT 32u  /* a kernel found its shared memory misaligned for the
+                                  tensor-core operand layout and wrote nothing           */
 
 /*
  * paged_kv_write -- store the step's new keys and values in the paged pool.
@@ -323,12 +325,16 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *   PKV_MQ_TILE_ROWS     64 rows per CTA, 16 per warp in the MMA's M dimension,
  *                        the warps sharing each K/V tile. Reads the context
  *                        8 times less often for long chunks.
- *   PKV_MQ_TILE_AUTO     ROWS when max_query_len * (num_heads / num_kv_heads)
+ *   PKV_MQ_TILE_TENSOR   128 rows per CTA on the fifth-generation tensor cores
+ *                        (tcgen05): scores and outputs accumulate in tensor
+ *                        memory, one thread per row runs the softmax.
+ *   PKV_MQ_TILE_AUTO     TENSOR when max_query_len * (num_heads / num_kv_heads)
  *                        >= 64, else COLUMNS (default).
  */
 #define PKV_MQ_TILE_AUTO 0
 #define PKV_MQ_TILE_COLUMNS 1
 #define PKV_MQ_TILE_ROWS 2
+#define PKV_MQ_TILE_TENSOR 3
 
 /* Choose the multi-query tile for later calls in this process (PKV_MQ_TILE_*).
  * Returns the previous choice, or -1 for an unknown value (nothing changes). */

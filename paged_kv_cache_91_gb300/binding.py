@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 _DTYPE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)  # an FP8 cache: E4M3 codes
-DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT", 16: "QUERY"}
+DEVERR_BITS = {1: "BLOCK_ID", 2: "CONTEXT", 4: "SLOT", 8: "TIMEOUT", 16: "QUERY", 32: "LAYOUT"}
 
 _lib = None
 
@@ -273,7 +273,7 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
     return out
 
 
-MQ_TILE_AUTO, MQ_TILE_COLUMNS, MQ_TILE_ROWS = 0, 1, 2
+MQ_TILE_AUTO, MQ_TILE_COLUMNS, MQ_TILE_ROWS, MQ_TILE_TENSOR = 0, 1, 2, 3
 
 
 def set_multi_query_tile(tile: int) -> int:

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kDefaultPartition = 512;
 #ifndef PKV_MQ_WIDE_MIN_ROWS
-#define PKV_MQ_WIDE_MIN_ROWS 64  // multi-query rows per kv head from which the wide tile runs (build-time knob)
+#define PKV_MQ_WIDE_MIN_ROWS 64  // multi-query rows per kv head from which the tensor-memory tile runs (build-time knob)
 #endif
 // An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
 // weigh twice as much per byte: longer partitions measure faster.
@@ -384,6 +384,27 @@ bool make_pool_map(CUtensorMap* map, const void* base, long long rows, int head_
   return r == CUDA_SUCCESS;
 }
 
+// The pool as seen by the tensor-memory multi-query tile (head_dim 128): one
+// copy per (block, kv head) tile of block_size rows, landing as 8-row atoms of
+// 2 KB, each holding its rows' columns 0..63 (1 KB, 128-byte swizzled) then
+// columns 64..127. Dimensions, innermost first: 64 columns, 8 rows of an atom
+// (row stride), the two column halves (128 bytes apart), the atoms (8 rows
+// apart).
+bool make_pool_map_tc(CUtensorMap* map, const void* base, long long rows, int block_size, pkv_dtype_t dtype) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+  const cuuint64_t strides[3] = {256, 128, 2048};
+  const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(block_size / 8)};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapDataType type =
+      dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = enc(map, type, 4, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int max_partitions_for(int max_context_len, int partition_size) {
   const int n = (max_context_len + partition_size - 1) / partition_size;
   return n < 1 ? 1 : n;
@@ -691,7 +712,9 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
 }
 
 int32_t pkv_set_multi_query_tile(int32_t tile) {
-  if (tile != PKV_MQ_TILE_AUTO && tile != PKV_MQ_TILE_COLUMNS && tile != PKV_MQ_TILE_ROWS) return -1;
+  if (tile != PKV_MQ_TILE_AUTO && tile != PKV_MQ_TILE_COLUMNS && tile != PKV_MQ_TILE_ROWS &&
+      tile != PKV_MQ_TILE_TENSOR)
+    return -1;
   return g_mq_tile.exchange(tile);
 }
 
@@ -816,12 +839,12 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
                 block_size, kMaxPartitionBlocks * block_size);
   const int G = num_heads / num_kv_heads;
-  // Many rows per kv head go to the wide tile (64 rows per CTA, query rows in
-  // the MMA's M), a few to the 8-column tile, which reads no padding rows.
-  const int tile = g_mq_tile.load(std::memory_order_relaxed);
-  const bool wide = tile == PKV_MQ_TILE_ROWS ||
-                    (tile == PKV_MQ_TILE_AUTO && (long long)max_query_len * G >= PKV_MQ_WIDE_MIN_ROWS);
-  const int rows_per_tile = wide ? 64 : 8;
+  // Many rows per kv head go to a tile with query rows in the MMA's M, a few
+  // to the 8-column tile, which reads no padding rows.
+  int tile = g_mq_tile.load(std::memory_order_relaxed);
+  if (tile == PKV_MQ_TILE_AUTO)
+    tile = (long long)max_query_len * G >= PKV_MQ_WIDE_MIN_ROWS ? PKV_MQ_TILE_TENSOR : PKV_MQ_TILE_COLUMNS;
+  const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128 : tile == PKV_MQ_TILE_ROWS ? 64 : 8;
   const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
   if (num_seqs > 65535 || (long long)num_kv_heads * row_tiles > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_kv_heads * ceil(max_query_len * group / %d) must be <= 65535",
@@ -886,11 +909,14 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   memset(&kmap, 0, sizeof kmap);
   memset(&vmap, 0, sizeof vmap);
   const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-  if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
-      !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
+  const bool tc_map = tile == PKV_MQ_TILE_TENSOR && head_dim == 128;
+  if (tc_map ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
+                   !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
+             : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
+                   !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream)
-                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, wide, stream);
+  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
+                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);
   if (e != cudaSuccess) return cuda_fail(e, "multi-query kernel launch");
   if (np > 1) {
     e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream, mq)

@@ -36,10 +36,10 @@ cudaError_t decode_mma_bf16(const DecodeParams& p, const CUtensorMap& kmap, cons
 struct MqParams;
 // wide: the 64-row tile (query rows in the MMA's M dimension) instead of the 8-column one.
 cudaError_t decode_mq_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                          const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, bool wide,
+                          const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                           cudaStream_t stream);
 cudaError_t decode_mq_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, bool wide,
+                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                            cudaStream_t stream);
 
 // Persistent equal-work decode (pkv_decode_stream.cuh): CTAs per SM, launch, reduce.

@@ -1,0 +1,521 @@
+// Multi-query paged attention on the fifth-generation tensor cores (tcgen05):
+// 128 query rows per CTA in the MMA's M dimension, scores and outputs
+// accumulated in tensor memory.
+//
+// Same computation as the other multi-query tiles (pkv_decode_mq.cuh): the
+// R = q_len * G (query token, head) rows of a (sequence, kv head), row r being
+// query token r / G at position ctx - q_len + r / G and attending the positions
+// up to its own ("vLLM: LLM 서빙 메모리 최적화의 교과서", 01 Problem Definition:
+// a_ij over j <= i; the blocked form o_i = sum_j V_j A_ij^T of "Efficient
+// Memory Management for LLM Serving with PagedAttention", §4.1 Eq. (4)). A
+// CTA takes 128 rows of one (partition, kv head, sequence) and walks the
+// partition in tiles of 64 tokens (64 / block_size pool blocks):
+//   S_j = Q . K_j^T      M 128, N 64,  K = head_dim   -> tensor memory (fp32)
+//   P_j = exp2(S_j * scale * log2 e - m_ref)          one thread per row,
+//                                                      16-bit, over S_j's columns
+//   O  += P_j . V_j      M 128, N = head_dim, K 64    A from tensor memory
+//
+// Roles (6 warps): warp 0 copies K tiles into a three-slot ring and V tiles
+// into a two-slot ring; one thread of warp 1 issues every MMA; warps 2..5 each
+// own 32 rows (their tensor-memory lane quarter) for the softmax, write P_j
+// back into tensor memory where S_j was, and finally normalise and store O. A
+// K slot is refilled as soon as its S MMA has completed, a V slot (and the S/P
+// buffer) once its PV has. S/P is double-buffered in tensor memory, so S_{j+1}
+// is usually ready when the softmax of tile j ends, and the softmax never
+// waits for the previous PV except to rescale O. The running max is a lazily
+// moved reference: O's row is rescaled only when a score exceeds the reference
+// by more than 2^8, which keeps P within the 16-bit range. Two CTAs share an
+// SM, so one CTA's start and end overlap the other's streaming.
+//
+// Every wait is bounded: a copy or MMA that does not complete makes the CTA
+// stop, set PKV_DEVERR_TIMEOUT and write an empty result.
+#pragma once
+
+#include <type_traits>
+
+#include "pkv_decode_mq.cuh"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+
+template <typename T, int D, int BS>
+struct MqTcShape {
+  static constexpr int ROWS = 128;                // query rows per CTA (M)
+  static constexpr int NT = 64;                   // tokens per K/V tile
+  static constexpr int NBT = NT / BS;             // pool blocks per tile
+  static constexpr int DH = D / 64;               // 128-byte halves of a 16-bit row
+  // A K or V tile in shared memory: 8-token atoms of DH x 1024 bytes (atom
+  // stride ATOM), each holding the 128-byte rows of its 8 tokens for columns
+  // 0..63, then (head_dim 128) for columns 64..127 -- the layout one copy of a
+  // whole pool block lands in (see make_pool_map_tc on the host).
+  static constexpr int ATOM = DH * 1024;
+  static constexpr int TILE = NT / 8 * ATOM;
+  static constexpr int KST = 3, VST = 2;          // K and V ring slots
+  static constexpr int OFF_K = DH * ROWS * 128;   // after Q
+  static constexpr int OFF_V = OFF_K + KST * TILE;
+  static constexpr int OFF_BARS = OFF_V + VST * TILE;
+  // k_full[3], k_empty[3], v_full[2], pv_done[2] (PV_j done: V slot and S/P buffer j % 2 free),
+  // s_full[2], p_full[2] (per S/P buffer: no row can reach tile j + 2 before PV_j), fin, q_full
+  static constexpr int NBARS = 16;
+  static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;  // tensor-memory base, abort flag
+  static constexpr int SMEM_USED = OFF_MISC + 8;
+  // The operands need 1024-byte aligned atoms; the dynamic shared memory of a
+  // CTA without static shared variables starts 1024-aligned (checked at run
+  // time), so no slack is reserved. At most two CTAs per SM: their tensor
+  // memory (2 x 256 columns) is then always free.
+  static constexpr int SMEM_MIN = 233472 / 3 + 1024;
+  static constexpr int SMEM = SMEM_USED > SMEM_MIN ? SMEM_USED : SMEM_MIN;
+  static constexpr int TMEM_COLS = 256;           // O at columns [0, D), S/P buffers at 128 and 192
+  static constexpr int S_COL = 128;
+  static constexpr int IDS = (kMaxPartitionBlocks + 31) / 32;
+  static constexpr int THREADS = 192;
+  static_assert(BS * 128 % 1024 == 0, "a block's rows must fill whole 1024-byte swizzle atoms");
+  static_assert(NT % BS == 0 && NBT <= 32, "tile of whole blocks");
+  static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
+};
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for `parity` on `bar`; false if another role gave up (`abort` set) or
+// the wait passed the cycle limit (then `abort` is set here).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+template <typename T, int D, int BS>
+__global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3 warps per SM quarter)
+    pkv_mq_tc_kernel(const DecodeParams p, const MqParams mq, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap) {
+  pdl_begin();
+  using Sh = MqTcShape<T, D, BS>;
+  constexpr int NT = Sh::NT, NBT = Sh::NBT, DH = Sh::DH;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int KST = Sh::KST;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + Sh::OFF_BARS);
+  uint64_t* k_empty = k_full + 3;
+  uint64_t* v_full = k_full + 6;
+  uint64_t* pv_done = k_full + 8;
+  uint64_t* s_full = k_full + 10;
+  uint64_t* p_full = k_full + 12;
+  uint64_t* fin = k_full + 14;
+  uint64_t* q_full = k_full + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned char* Qs = smem;
+  auto k_slot = [&](int j) { return smem + Sh::OFF_K + (j % KST) * Sh::TILE; };
+  auto v_slot = [&](int j) { return smem + Sh::OFF_V + (j & 1) * Sh::TILE; };
+
+  const int part = blockIdx.x;
+  const int kvh = blockIdx.y / mq.row_tiles, rt = blockIdx.y % mq.row_tiles;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const bool reporter = part == 0 && blockIdx.y == 0 && threadIdx.x == 0;
+  if (smem_u32(smem) & 1023u) {  // not expected on any supported GPU; nothing is written
+    if (threadIdx.x == 0) atomicOr(p.err, PKV_DEVERR_LAYOUT);
+    return;
+  }
+  const int ctx = clamp_context(p, s, reporter);
+  int q0 = 0;
+  const int q_len = mq_query_len(mq, s, ctx, q0);
+  if (q_len < 0) {
+    if (reporter) atomicOr(p.err, PKV_DEVERR_QUERY);
+    return;
+  }
+  const int R = q_len * G;
+  const int row0 = rt * Sh::ROWS;
+  if (row0 >= R) return;
+  const int P = p.partition_size;
+  const int tok0 = part * P;
+  if (tok0 >= ctx) return;
+  const int lim_cta = ctx - q_len + (min(row0 + Sh::ROWS, R) - 1) / G + 1;  // the CTA's last row's limit
+  const int tok1 = min(min(tok0 + P, ctx), lim_cta);
+  const bool direct = ctx <= P;
+  const int ntile = tok1 > tok0 ? (tok1 - tok0 + NT - 1) / NT : 0;
+  const int blk0 = tok0 / BS;
+
+  // softmax rows: warps 2..5, thread row = 32 (warp % 4) + lane (its tensor-memory lane)
+  const bool srole = warp >= 2;
+  const int row = 32 * (warp & 3) + lane;
+  const int r = row0 + row;
+  const bool active = srole && r < R;
+  const size_t orow = active ? (size_t)(q0 + r / G) * p.num_heads + kvh * G + r % G : 0;  // output row
+
+  if (ntile == 0) {  // no visible token in this partition: an empty partial (ctx > P here)
+    if (active) {
+      for (int d = 0; d < D; d += 4)
+        *reinterpret_cast<float4*>(p.part_o + (orow * p.max_partitions + part) * D + d) = make_float4(0, 0, 0, 0);
+      p.part_m[orow * p.max_partitions + part] = -INFINITY;
+      p.part_l[orow * p.max_partitions + part] = 0.f;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    for (int k = 0; k < 12; ++k) mbar_init(k_full + k, 1);
+    mbar_init(p_full, 128);
+    mbar_init(p_full + 1, 128);
+    mbar_init(fin, 1);
+    mbar_init(q_full, 128);
+    fence_mbar_init();
+    *abort = 0;
+  }
+  if (warp == 1) tc::alloc(tmem_slot, Sh::TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- producer: K tile j and V tile j into slot j % 2 of their rings
+    int ids[Sh::IDS];  // lane l: block ids l, l + 32, ... of the partition; -1 for a bad id
+    const int nblk = (tok1 - tok0 + BS - 1) / BS;
+#pragma unroll
+    for (int u = 0; u < Sh::IDS; ++u) {
+      const int b = lane + 32 * u;
+      ids[u] = -1;
+      if (b < nblk) {
+        const int v = p.block_tables[(size_t)s * p.max_blocks_per_seq + blk0 + b];
+        if ((unsigned)v < (unsigned)p.num_blocks) {
+          ids[u] = v;
+        } else {
+          atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+        }
+      }
+    }
+    // Copy whichever slot frees first: K tile nk once S_{nk-3} is done, V tile
+    // nv (never ahead of K) once PV_{nv-2} is done.
+    int nk = 0, nv = 0;
+    unsigned zeroed = 0;  // V slots whose tail rows the rows zeroed (generic stores)
+    long long t_last = clock64();
+    while (nv < ntile) {
+      int which = -1;  // 0: K tile nk, 1: V tile nv
+      if (lane == 0) {
+        if (nk < ntile && (nk < KST || mbar_test_wait(k_empty + nk % KST, ((nk / KST) - 1) & 1)))
+          which = 0;
+        else if (nv < nk && (nv < 2 || mbar_test_wait(pv_done + (nv & 1), ((nv >> 1) - 1) & 1)))
+          which = 1;
+        else if (*abort || clock64() - t_last > kWaitLimitCycles)
+          which = 2;
+      }
+      which = __shfl_sync(kFull, which, 0);
+      if (which == 2) {
+        if (lane == 0) *abort = 1;
+        break;
+      }
+      if (which < 0) {
+        __nanosleep(64);  // leave the issue slots to the rows' warp on this SM quarter
+        continue;
+      }
+      const int j = which ? nv : nk;
+      int phys = -1;  // lane i < NBT: block j * NBT + i of the partition
+#pragma unroll
+      for (int u = 0; u < Sh::IDS; ++u) {
+        const int b = j * NBT + (lane & (NBT - 1));
+        const int x = __shfl_sync(kFull, ids[u], b & 31);
+        if ((b >> 5) == u) phys = x;
+      }
+      if (lane >= NBT || j * NBT + lane >= nblk) phys = -1;
+      const unsigned mask = __ballot_sync(kFull, phys >= 0);
+      uint64_t* bar = which ? v_full + (j & 1) : k_full + j % KST;
+      if (lane == 0) {
+        if (which && ((zeroed >> (j & 1)) & 1u)) fence_proxy_async_smem();  // the rows' zeros precede the copies
+        mbar_arrive_expect_tx(bar, __popc(mask) * DH * BS * 128);
+        t_last = clock64();
+      }
+      if (which) {  // the rows zero this tile's V tail (the same test as theirs)
+        const bool z = mask != (1u << NBT) - 1u || tok0 + j * NT + NT > ctx;
+        zeroed = (zeroed & ~(1u << (j & 1))) | ((z ? 1u : 0u) << (j & 1));
+      }
+      __syncwarp();
+      if (phys >= 0) {
+        const int y = (phys * p.num_kv_heads + kvh) * BS;
+        unsigned char* dst = (which ? v_slot(j) : k_slot(j)) + lane * (BS / 8) * Sh::ATOM;
+        if constexpr (DH == 2)
+          tc::tma_load_4d(dst, which ? &vmap : &kmap, 0, 0, 0, y / 8, bar);  // the block's BS rows, both halves
+        else
+          tma_load_2d(dst, which ? &vmap : &kmap, 0, y, bar);
+      }
+      if (which) ++nv; else ++nk;
+    }
+    // no copy may still be landing when the CTA leaves
+    if (lane == 0) {
+      for (int j = nk > KST ? nk - KST : 0; j < nk; ++j) mbar_wait(k_full + j % KST, (j / KST) & 1);
+      for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) mbar_wait(v_full + (j & 1), (j >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue (one thread)
+    if (lane == 0) {
+      constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+      constexpr uint32_t IDESC_S = tc::idesc_f16(BF, Sh::ROWS, NT, false, false);
+      constexpr uint32_t IDESC_O = tc::idesc_f16(BF, Sh::ROWS, D, false, true);
+      const uint32_t q_addr = smem_u32(Qs);
+      auto issue_s = [&](int j) {  // S_j = Q . K_j^T into S/P buffer j % 2, then K slot j % 3 is free
+        const uint32_t k_addr = smem_u32(k_slot(j));
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t a = tc::desc_sw128(q_addr + (k / 4) * (Sh::ROWS * 128) + (k % 4) * 32, 16, 1024);
+          const uint64_t b = tc::desc_sw128(k_addr + (k / 4) * 1024 + (k % 4) * 32, 16, Sh::ATOM);
+          tc::mma_f16(tbase + Sh::S_COL + (j & 1) * NT, a, b, IDESC_S, k > 0);
+        }
+        tc::commit(s_full + (j & 1));
+        tc::commit(k_empty + j % KST);
+      };
+      auto issue_pv = [&](int j) {  // O += P_j . V_j, then V slot j % 2 and S/P buffer j % 2 are free
+        const uint32_t v_addr = smem_u32(v_slot(j));
+#pragma unroll
+        for (int k = 0; k < NT / 16; ++k) {
+          const uint64_t b = tc::desc_sw128(v_addr + k * 2 * Sh::ATOM, 1024, Sh::ATOM);
+          tc::mma_f16_ta(tbase, tbase + Sh::S_COL + (j & 1) * NT + k * 8, b, IDESC_O, j > 0 || k > 0);
+        }
+        tc::commit(pv_done + (j & 1));
+      };
+      // Issue whichever is ready: S_ns once K_ns has landed and PV_{ns-2} (the
+      // last reader of its buffer) is done; PV_npv once P_npv is written and
+      // V_npv has landed.
+      int ns = 0, npv = 0;
+      bool q_in = false;  // the rows have written Q
+      long long t_last = clock64();
+      while (npv < ntile) {
+        bool progressed = false;
+        if (!q_in) q_in = mbar_test_wait(q_full, 0);
+        if (q_in && ns < ntile && mbar_test_wait(k_full + ns % KST, (ns / KST) & 1) &&
+            (ns < 2 || mbar_test_wait(pv_done + (ns & 1), ((ns >> 1) - 1) & 1))) {
+          tc::fence_after_sync();
+          issue_s(ns++);
+          progressed = true;
+        } else if (npv < ns && mbar_test_wait(p_full + (npv & 1), (npv >> 1) & 1) &&
+                   mbar_test_wait(v_full + (npv & 1), (npv >> 1) & 1)) {
+          tc::fence_after_sync();
+          issue_pv(npv++);
+          progressed = true;
+        }
+        if (progressed) {
+          t_last = clock64();
+        } else if (__nanosleep(32), *abort) {
+          break;
+        } else if (clock64() - t_last > kWaitLimitCycles) {
+          *abort = 1;
+          break;
+        }
+      }
+      tc::commit(fin);  // every MMA issued above has completed once this arrives
+      mbar_wait(fin, 0);
+    }
+    __syncwarp();
+  } else if (srole) {
+    // ---- softmax rows
+    {  // Q rows into the A operand layout (zeros past R), while the producer starts the copies
+      const uint4* src = active ? reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.query) + orow * D)
+                                : nullptr;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = active ? src[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Qs + (c / 8) * (Sh::ROWS * 128) + tc::sw128(row, c % 8)) = v;
+      }
+      fence_proxy_async_smem();  // generic stores, read by the S MMAs
+      mbar_arrive(q_full);
+    }
+    const int lim = active ? ctx - q_len + r / G + 1 : 0;  // this row sees positions < lim
+    const int vis = min(lim, tok1);
+    const float sl2 = p.scale_log2;
+    const uint32_t all = (1u << NBT) - 1u;
+    // which blocks of each tile were fetched: the same test as the producer's
+    int ids[Sh::IDS];
+    const int nblk = (tok1 - tok0 + BS - 1) / BS;
+#pragma unroll
+    for (int u = 0; u < Sh::IDS; ++u) {
+      const int b = lane + 32 * u;
+      ids[u] = 0;
+      if (b < nblk) ids[u] = (unsigned)p.block_tables[(size_t)s * p.max_blocks_per_seq + blk0 + b] < (unsigned)p.num_blocks;
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntile; ++j) {
+      const int tb = tok0 + j * NT;
+      // (tensor-memory accesses are warp-wide: a warp leaves the loop as a whole)
+      ok = tc_wait(s_full + (j & 1), (j >> 1) & 1, abort);
+      if (!__all_sync(kFull, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t sr[2][32];
+      tc::ld32(tc::taddr(tbase, 32 * (warp & 3), Sh::S_COL + (j & 1) * NT), sr[0]);
+      tc::ld32(tc::taddr(tbase, 32 * (warp & 3), Sh::S_COL + (j & 1) * NT + 32), sr[1]);
+      tc::wait_ld();
+      int fetched = 0;
+#pragma unroll
+      for (int u = 0; u < Sh::IDS; ++u) {
+        const int b = j * NBT + (lane & (NBT - 1));
+        const int x = __shfl_sync(kFull, ids[u], b & 31);
+        if ((b >> 5) == u) fetched = x;
+      }
+      const uint32_t mask = __ballot_sync(kFull, lane < NBT && fetched) & all;
+      const int nv = vis - tb;  // leading tokens of the tile this row may see
+      float x[NT];
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent max chains
+      if (nv >= NT && mask == all) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          x[t] = __uint_as_float(sr[t >> 5][t & 31]) * sl2;
+          mq[t & 3] = fmaxf(mq[t & 3], x[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const bool see = t < nv && ((mask >> (t / BS)) & 1u);
+          x[t] = see ? __uint_as_float(sr[t >> 5][t & 31]) * sl2 : -INFINITY;
+          mq[t & 3] = fmaxf(mq[t & 3], x[t]);
+        }
+      }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const bool move = mx > m_ref + 8.f;
+      const bool resc = j > 0 && move && m_ref != -INFINITY;  // O's row holds terms to rescale
+      const float f = resc ? fast_exp2(m_ref - mx) : 1.f;
+      if (move) m_ref = mx;
+      // P row as 16-bit pairs (exp2(-inf) = 0 for masked tokens; a row that has
+      // seen nothing yet keeps m_ref = -inf and gets zeros)
+      uint32_t pw[NT / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      if (m_ref != -INFINITY) {
+#pragma unroll
+        for (int u = 0; u < NT / 2; ++u) {
+          const float a = fast_exp2(x[2 * u] - m_ref), b = fast_exp2(x[2 * u + 1] - m_ref);
+          ls[u & 3] += a + b;
+          pw[u] = Elem<T>::pack2(a, b);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < NT / 2; ++u) pw[u] = 0u;
+      }
+      if (__any_sync(kFull, resc)) {  // the whole warp moves its rows' O (factor 1 for rows that keep theirs)
+        ok = tc_wait(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort);  // once PV_{j-1} is done
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::ld32(tc::taddr(tbase, 32 * (warp & 3), c * 32), o);
+          tc::wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * f);
+          tc::st32(tc::taddr(tbase, 32 * (warp & 3), c * 32), o);
+        }
+        tc::wait_st();
+      }
+      l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      tc::st32(tc::taddr(tbase, 32 * (warp & 3), Sh::S_COL + (j & 1) * NT), pw);  // P_j over S_j
+      tc::wait_st();
+      // V rows past the context, or of blocks not fetched, may hold anything (NaN):
+      // zero them once V_j has landed, since P = 0 times NaN is NaN in the MMA
+      if (mask != all || tb + NT > ctx) {
+        ok = tc_wait(v_full + (j & 1), (j >> 1) & 1, abort);
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+        unsigned char* vs = v_slot(j);
+        for (int i = threadIdx.x - 64; i < NT * 8 * DH; i += 128) {
+          const int t = i / (8 * DH), c = i % (8 * DH);
+          if (!((mask >> (t / BS)) & 1u) || tb + t >= ctx)
+            *reinterpret_cast<uint4*>(vs + (t / 8) * Sh::ATOM + (c / 8) * 1024 + tc::sw128(t % 8, c % 8)) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // the zeros precede the PV's reads
+      }
+      tc::fence_before_sync();
+      mbar_arrive(p_full + (j & 1));
+    }
+    // epilogue: O / l
+    if (ok) ok = tc_wait(pv_done + ((ntile - 1) & 1), ((ntile - 1) >> 1) & 1, abort);
+    tc::fence_after_sync();
+    ok = ok && !*abort;
+    const float inv = ok && l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tc::ld32(tc::taddr(tbase, 32 * (warp & 3), c * 32), o);
+      tc::wait_ld();
+      if (!active) continue;
+      if (direct) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + orow * D + c * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = Elem<T>::pack2(__uint_as_float(o[8 * u + 2 * e]) * inv, __uint_as_float(o[8 * u + 2 * e + 1]) * inv);
+          dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.part_o + (orow * p.max_partitions + part) * D + c * 32);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)  // partials are normalised by their own l (inv = 0 after a failure)
+          dst[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                               __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+      }
+    }
+    if (active && !direct) {
+      p.part_m[orow * p.max_partitions + part] = ok ? m_ref : -INFINITY;
+      p.part_l[orow * p.max_partitions + part] = ok ? l : 0.f;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::dealloc(tbase, Sh::TMEM_COLS);
+  }
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_mq_tc(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
+                         const CUtensorMap& vmap, int num_seqs, cudaStream_t stream) {
+  using Sh = MqTcShape<T, D, BS>;
+  auto kern = pkv_mq_tc_kernel<T, D, BS>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+    if (e != cudaSuccess) return e;
+    // two CTAs need nearly all of the SM's shared memory: ask for the largest carveout
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const dim3 grid(p.max_partitions, p.num_kv_heads * mq.row_tiles, num_seqs);
+  return launch_kernel(kern, grid, dim3(Sh::THREADS), Sh::SMEM, stream, p, mq, kmap, vmap);
+}
+
+}  // namespace pkv

@@ -279,6 +279,7 @@ def test_multi_query_tile_switch(lib):
     try:
         assert lib.pkv_set_multi_query_tile(1) == 2
         assert lib.pkv_set_multi_query_tile(9) == -1
-        assert lib.pkv_set_multi_query_tile(0) == 1
+        assert lib.pkv_set_multi_query_tile(3) == 1  # the tensor-memory tile
+        assert lib.pkv_set_multi_query_tile(0) == 3
     finally:
         lib.pkv_set_multi_query_tile(prev)

@@ -21,11 +21,13 @@ RTOL = 1e-2
 DEV = "cuda:0"
 
 
-@pytest.fixture(autouse=True, params=["columns", "rows"])
+TILES = {"columns": binding.MQ_TILE_COLUMNS, "rows": binding.MQ_TILE_ROWS, "tensor": binding.MQ_TILE_TENSOR}
+
+
+@pytest.fixture(autouse=True, params=list(TILES))
 def mq_tile(request, cuda_lib):
-    """Every test runs on both multi-query tiles (they must give the same results)."""
-    prev = binding.set_multi_query_tile(binding.MQ_TILE_COLUMNS if request.param == "columns"
-                                        else binding.MQ_TILE_ROWS)
+    """Every test runs on each multi-query tile (they must give the same results)."""
+    prev = binding.set_multi_query_tile(TILES[request.param])
     binding.device_errors(clear=True)
     yield request.param
     binding.set_multi_query_tile(prev)
