@@ -384,8 +384,8 @@ bool make_pool_map(CUtensorMap* map, const void* base, long long rows, int head_
   return r == CUDA_SUCCESS;
 }
 
-// The pool as seen by the tensor-memory multi-query tile (head_dim 128): one
-// copy per (block, kv head) tile of block_size rows, landing as 8-row atoms of
+// The 16-bit pool as seen by the head_dim-128 tensor-core tiles: one copy per
+// (block, kv head) tile of block_size rows, landing as 8-row atoms of
 // 2 KB, each holding its rows' columns 0..63 (1 KB, 128-byte swizzled) then
 // columns 64..127. Dimensions, innermost first: 64 columns, 8 rows of an atom
 // (row stride), the two column halves (128 bytes apart), the atoms (8 rows
@@ -552,8 +552,11 @@ pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, co
   if (pl.mma) {
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
     const pkv_dtype_t cache_dtype = fp8 ? PKV_FP8_E4M3 : dtype;
-    if (!make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
-        !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
+    const bool one_copy = !fp8 && head_dim == 128 && tile_one_copy();
+    if (one_copy ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
+                       !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
+                 : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
+                       !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
   }
 
@@ -909,7 +912,7 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   memset(&kmap, 0, sizeof kmap);
   memset(&vmap, 0, sizeof vmap);
   const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-  const bool tc_map = tile == PKV_MQ_TILE_TENSOR && head_dim == 128;
+  const bool tc_map = head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy());
   if (tc_map ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
                    !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
              : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||

@@ -22,12 +22,44 @@
 
 namespace pkv {
 
-// Byte offset of 16-byte piece `piece` (of D/8) of token row `t` inside a tile
-// stored as D/64 swizzled boxes of BS rows x 128 bytes.
-template <int BS>
+#ifndef PKV_TILE_ONE_COPY
+#define PKV_TILE_ONE_COPY 1  // head_dim 128: one 4-D copy per (block, kv head) tile (build-time knob)
+#endif
+
+// Byte offset of 16-byte piece `piece` (of D/8) of token row `t` inside a
+// 16-bit (block, kv head) tile of NBOX = D/64 column halves in 128-byte
+// swizzled rows. With one copy per tile the tile is a run of 8-row atoms of
+// NBOX x 1024 bytes (each atom: its rows' columns 0..63, then 64..127, the
+// layout a 4-D tensor map of the pool delivers); otherwise NBOX boxes of BS
+// rows x 128 bytes, one per column half. For NBOX = 1 the two coincide.
+template <int BS, int NBOX = 2>
 __device__ __forceinline__ int swz_offset(int t, int piece) {
   const int box = piece >> 3, chunk = piece & 7;
+  if (PKV_TILE_ONE_COPY)
+    return (t >> 3) * (NBOX * 1024) + box * 1024 + (t & 7) * 128 + ((chunk ^ (t & 7)) << 4);
   return box * (BS * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
+}
+
+// Tiled 4D tensor copy global -> shared through a tensor map (x innermost).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One (block, kv head) tile of a 16-bit pool into `dst` in the swz_offset
+// layout; y is the tile's first row in the pool.
+template <int D, int BS>
+__device__ __forceinline__ void copy_tile16(unsigned char* dst, const CUtensorMap* map, int y, uint64_t* bar) {
+  if constexpr (D == 128 && PKV_TILE_ONE_COPY) {
+    tma_load_4d(dst, map, 0, 0, 0, y / 8, bar);
+  } else {
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_2d(dst + b * (BS * 128), map, 64 * b, y, bar);
+  }
 }
 
 template <typename T_, int D_, int BS_>
@@ -93,7 +125,7 @@ struct MmaTile {
       const int nz = (BS - nvalid) * (D / 8);
       for (int idx = lane; idx < nz; idx += 32) {
         const int t = nvalid + idx / (D / 8), piece = idx % (D / 8);
-        *reinterpret_cast<uint4*>(Vs + swz_offset<BS>(t, piece)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(Vs + swz_offset<BS, NBOX>(t, piece)) = make_uint4(0u, 0u, 0u, 0u);
       }
       __syncwarp();
     }
@@ -109,7 +141,7 @@ struct MmaTile {
 #pragma unroll
           for (int kk = 0; kk < KT; ++kk) {
             uint32_t a[4];
-            ldmatrix_x4(a, Ks + swz_offset<BS>(t, kk * 2 + (mi >> 1)));
+            ldmatrix_x4(a, Ks + swz_offset<BS, NBOX>(t, kk * 2 + (mi >> 1)));
             if (kk & 1) {
               Mma<T>::run(sacc2, a, qb[kk][0], qb[kk][1]);
             } else {
@@ -172,7 +204,7 @@ struct MmaTile {
 #pragma unroll
           for (int mt = 0; mt < KT; ++mt) {
             uint32_t a[4];
-            ldmatrix_x4_trans(a, Vs + swz_offset<BS>(t, mt * 2 + (mi & 1)));
+            ldmatrix_x4_trans(a, Vs + swz_offset<BS, NBOX>(t, mt * 2 + (mi & 1)));
             Mma<T>::run(acc[mt], a, b0, b1);
           }
         }
@@ -199,11 +231,8 @@ struct MmaTile {
   // Issue the tensor-map copies of one (block, kv head) tile pair into a stage.
   static __device__ __forceinline__ void issue_tiles(unsigned char* st, const CUtensorMap* kmap,
                                                      const CUtensorMap* vmap, int y, uint64_t* bar) {
-#pragma unroll
-    for (int b = 0; b < NBOX; ++b) {
-      tma_load_2d(st + b * BOXB, kmap, 64 * b, y, bar);
-      tma_load_2d(st + TILE + b * BOXB, vmap, 64 * b, y, bar);
-    }
+    copy_tile16<D, BS>(st, kmap, y, bar);
+    copy_tile16<D, BS>(st + TILE, vmap, y, bar);
   }
 };
 

@@ -19,4 +19,6 @@ cudaError_t decode_mma_f16(const DecodeParams& p, const CUtensorMap& kmap, const
   return cudaErrorInvalidValue;
 }
 
+bool tile_one_copy() { return PKV_TILE_ONE_COPY != 0; }
+
 }  // namespace pkv

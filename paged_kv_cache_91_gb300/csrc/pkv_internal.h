@@ -35,6 +35,10 @@ cudaError_t decode_mma_bf16(const DecodeParams& p, const CUtensorMap& kmap, cons
 // Multi-query attention (several causal query tokens per sequence; pkv_decode_mq.cuh).
 struct MqParams;
 // wide: the 64-row tile (query rows in the MMA's M dimension) instead of the 8-column one.
+// Whether the 16-bit tensor-core tiles take a head_dim-128 tile in one copy
+// (the pool's tensor map is then make_pool_map_tc's).
+bool tile_one_copy();
+
 cudaError_t decode_mq_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                           cudaStream_t stream);

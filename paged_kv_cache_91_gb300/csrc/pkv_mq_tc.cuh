@@ -254,7 +254,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
         const int y = (phys * p.num_kv_heads + kvh) * BS;
         unsigned char* dst = (which ? v_slot(j) : k_slot(j)) + lane * (BS / 8) * Sh::ATOM;
         if constexpr (DH == 2)
-          tc::tma_load_4d(dst, which ? &vmap : &kmap, 0, 0, 0, y / 8, bar);  // the block's BS rows, both halves
+          tma_load_4d(dst, which ? &vmap : &kmap, 0, 0, 0, y / 8, bar);  // the block's BS rows, both halves
         else
           tma_load_2d(dst, which ? &vmap : &kmap, 0, y, bar);
       }

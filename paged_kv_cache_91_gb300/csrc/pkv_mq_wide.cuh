@@ -133,12 +133,9 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
       unsigned char* st = smem + (i % ST) * Sh::STAGE;
       if (phys >= 0) {
         mbar_arrive_expect_tx(bar, Sh::STAGE);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b) {
-          const int y = (phys * p.num_kv_heads + kvh) * BS;
-          tma_load_2d(st + b * (BS * 128), &kmap, 64 * b, y, bar);
-          tma_load_2d(st + Sh::TILE + b * (BS * 128), &vmap, 64 * b, y, bar);
-        }
+        const int y = (phys * p.num_kv_heads + kvh) * BS;
+        copy_tile16<D, BS>(st, &kmap, y, bar);
+        copy_tile16<D, BS>(st + Sh::TILE, &vmap, y, bar);
       } else {
         mbar_arrive(bar);  // complete the phase without data; the block is skipped
       }
@@ -205,7 +202,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
               uint32_t b[4];
-              ldmatrix_x4(b, Ks + swz_offset<BS>(t, 2 * kk + (mi & 1)));
+              ldmatrix_x4(b, Ks + swz_offset<BS, D / 64>(t, 2 * kk + (mi & 1)));
               if (kk & 1) {
                 Mma<T>::run(s2, qa[kk], b[0], b[1]);
                 Mma<T>::run(s3, qa[kk], b[2], b[3]);
@@ -281,7 +278,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
 #pragma unroll
             for (int j = 0; j < KT; ++j) {
               uint32_t v[4];
-              ldmatrix_x4_trans(v, Vs + swz_offset<BS>(t, 2 * j + (mi >> 1)));
+              ldmatrix_x4_trans(v, Vs + swz_offset<BS, D / 64>(t, 2 * j + (mi >> 1)));
               Mma<T>::run(acc[2 * j], pa, v[0] & vm01, v[1] & vm89);
               Mma<T>::run(acc[2 * j + 1], pa, v[2] & vm01, v[3] & vm89);
             }
