@@ -403,9 +403,9 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
       if (m_ref != -INFINITY) {
 #pragma unroll
         for (int u = 0; u < NT / 2; ++u) {
-          const float a = fast_exp2(x[2 * u] - m_ref), b = fast_exp2(x[2 * u + 1] - m_ref);
-          ls[u & 3] += a + b;
-          pw[u] = Elem<T>::pack2(a, b);
+          pw[u] = Elem<T>::pack2(fast_exp2(x[2 * u] - m_ref), fast_exp2(x[2 * u + 1] - m_ref));
+          const float2 r = Elem<T>::to_float2(pw[u]);  // l sums the weights PV multiplies
+          ls[u & 3] += r.x + r.y;
         }
       } else {
 #pragma unroll
