@@ -69,6 +69,9 @@ def parse_args():
                          "(paged_attention_multi_query; speculative verification / chunked prefill)")
     ap.add_argument("--mq-tile", choices=["auto", "columns", "rows", "tensor"], default="auto",
                     help="multi-query tile (default: the library's choice by rows per kv head)")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="workload 4 through paged_attention_decode_shared_prefix: the 1024-token prefix is "
+                         "attended once for the whole batch, then each tail, then a merge")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
@@ -128,6 +131,21 @@ def default_partition(fp8: bool, mq: bool = False, block_size: int = 16) -> int:
     if mq:
         return min(2048, 128 * block_size)
     return 1024 if fp8 else 512
+
+
+SHARED_PREFIX_TOKENS = 1024  # workload 4's common prefix
+
+
+def shared_prefix_call_bytes(batch, prefix_tokens: int, ws_bytes: int):
+    """Bytes the shared-prefix call must move: the prefix's K/V once, every tail's K/V, q and out, the
+    tables, and the two stages' partials (written, then read by the merge)."""
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    S, H, D, B, e = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size, batch.elem_bytes
+    kv = W.unique_kv_bytes(batch)
+    tail_blocks = int(((batch.context_lens - prefix_tokens + B - 1) // B).sum())
+    tables = (prefix_tokens // B + tail_blocks) * 4 + S * 4
+    return kv + 2 * S * H * D * e + tables + 2 * ws_bytes
 
 
 def step_bytes(batch, partition_size: int, cache_bytes: int = 2):
@@ -454,7 +472,21 @@ def run_ours(args, dist):
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
     fp8 = args.kv_dtype == "fp8_e4m3"
-    if mq:
+    shared = args.shared_prefix
+    if shared:
+        if mq or fp8 or args.config != 4:
+            raise SystemExit("--shared-prefix runs workload 4 (16-bit cache, one query token per sequence)")
+        # the call's own inputs: the common prefix's blocks, then each sequence's tail table and length
+        pb, tails, tail_lens = W.split_shared_prefix(batch, SHARED_PREFIX_TOKENS)
+        prefix_dev = torch.from_numpy(pb).to(dev)
+        t["block_tables"] = torch.from_numpy(tails).to(dev)
+        t["context_lens"] = torch.from_numpy(tail_lens).to(dev)
+        max_tail = int(tail_lens.max())
+    if shared:
+        ws_bytes = binding.paged_attention_shared_prefix_workspace_size(
+            batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+            SHARED_PREFIX_TOKENS, max_tail)
+    elif mq:
         ws_bytes = binding.paged_attention_multi_query_workspace_size(
             int(batch.query_start_loc[-1]), batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
             mcl, P)
@@ -468,6 +500,9 @@ def run_ours(args, dist):
     launches_per_step = 2 + (1 if nparts > 1 else 0)
     cache_bytes = 1 if fp8 else 2
     kv_bytes, call_bytes = step_bytes(batch, P, cache_bytes)
+    if shared:
+        launches_per_step = 4  # write, prefix, tails, merge
+        call_bytes = shared_prefix_call_bytes(batch, SHARED_PREFIX_TOKENS, ws_bytes)
     if fp8:
         # the FP8 pool: every slot of the 16-bit pool quantized by the library's own write (setup, untimed)
         NB, Hkv, B, D = t["key_cache"].shape
@@ -488,7 +523,11 @@ def run_ours(args, dist):
             binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
 
     def decode(q, bt, cl, o, qsl=None):
-        if mq:
+        if shared:  # bt, cl: the tail tables and lengths
+            binding.paged_attention_decode_shared_prefix(o, q, t["key_cache"], t["value_cache"], prefix_dev,
+                                                         SHARED_PREFIX_TOKENS, bt, cl, batch.scale,
+                                                         max_tail_len=max_tail, workspace=ws, stream=stream)
+        elif mq:
             binding.paged_attention_multi_query(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
                                                 max_query_len=max_query_len, max_context_len=mcl, partition_size=P,
                                                 workspace=ws, stream=stream)
@@ -587,7 +626,7 @@ def run_ours(args, dist):
         kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
     else:
         kind = "mma" if 2 <= G <= 8 else "simt"
-    traffic = ncu_traffic(workload, kind)
+    traffic = None if shared else ncu_traffic(workload, kind)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -617,7 +656,9 @@ def run_ours(args, dist):
             "tokens_per_s": round(n_query_rows * dist.world * K / (total_ms / 1e3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
                             "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
-            "roofline": {"bound": "hbm", "kernel": ("paged_attention_multi_query" if mq else
+            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_shared_prefix (prefix, tail and merge "
+                         "kernels; bytes: the prefix once, the tails, q, out, partials)" if shared else
+                         ("paged_attention_multi_query" if mq else
                                                     "paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
                          + (" (multi-query kernel" if mq else " (decode kernel")
                          + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
@@ -635,6 +676,9 @@ def run_ours(args, dist):
         }
         if mq:
             line["multi_query"] = mq_summary(batch, args.mq_tile, dec_avg_ms)
+        if shared:
+            line["config"]["call"] = (f"paged_attention_decode_shared_prefix: the {SHARED_PREFIX_TOKENS}-token "
+                                      "prefix attended once for the whole batch, then each tail, then a merge")
         print(json.dumps(line), flush=True)
 
 

@@ -357,6 +357,56 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
                                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * paged_attention_decode_shared_prefix -- the decode step of a batch whose
+ * sequences all begin with the same prefix blocks (one prompt with several
+ * continuations, as in parallel sampling or beam search). Copy-on-write keeps
+ * those full blocks shared in the pool ("'안녕하세요 반갑습니다'로 배우는 vLLM
+ * — KV Cache와 PagedAttention 완전 해부", §9단계; "Sparse Computation and
+ * Memory Management for Efficient LLM Inference", Copy-on-Write). The result
+ * is exactly paged_attention_decode's with block table prefix_blocks ++
+ * block_tables[s] and context length prefix_len + tail_lens[s], but the
+ * prefix's K/V tiles are read and multiplied once for all sequences. All
+ * num_seqs * num_heads query rows of the batch attend the prefix as one
+ * multi-query problem on the tensor-memory tile (the 8-column tile below 64
+ * rows per kv head). Each sequence's tail is one decode token over its own
+ * blocks. The two parts' (m, l, o) partials are merged by the log-sum-exp
+ * rule of the split-K reduce.
+ *
+ *   out, query         [num_seqs][num_heads][head_dim], dtype
+ *   key_cache, value_cache   the pool, [num_blocks][num_kv_heads][block_size][head_dim]
+ *   prefix_blocks      [prefix_len / block_size] int32 physical ids of the shared
+ *                      prefix, in logical order; prefix_len must be a whole
+ *                      number of blocks (0: no prefix; then every sequence is
+ *                      its tail)
+ *   block_tables       [num_seqs][max_blocks_per_seq] int32: sequence s's blocks
+ *                      after the prefix (its logical blocks prefix_len / block_size ...)
+ *   tail_lens          [num_seqs] int32 tokens after the prefix (0 allowed); values
+ *                      outside [0, max_tail_len] are clamped and set PKV_DEVERR_CONTEXT
+ *   max_tail_len       host bound on tail_lens, <= max_blocks_per_seq * block_size
+ *   workspace          >= paged_attention_shared_prefix_workspace_size(...) bytes,
+ *                      16-byte aligned (always needed: both parts leave partials)
+ *
+ * 16-bit caches only (PKV_F16, PKV_BF16); head_dim 64 or 128; block_size 8, 16
+ * or 32. Errors as in paged_attention_decode: bad block ids are skipped with
+ * PKV_DEVERR_BLOCK_ID. Asynchronous on `stream`; three kernels (prefix, tails,
+ * merge).
+ */
+size_t paged_attention_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                                    int32_t num_kv_heads, int32_t head_dim,
+                                                    int32_t block_size, int32_t prefix_len,
+                                                    int32_t max_tail_len);
+
+pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, const void* key_cache,
+                                                  const void* value_cache, const int32_t* prefix_blocks,
+                                                  int32_t prefix_len, const int32_t* block_tables,
+                                                  int32_t max_blocks_per_seq, const int32_t* tail_lens,
+                                                  int32_t num_seqs, int32_t max_tail_len, float scale,
+                                                  int32_t block_size, int32_t num_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t num_blocks, pkv_dtype_t dtype, void* workspace,
+                                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * FP8 KV cache. The pages pass kv_cache_dtype, k_scale and v_scale to the cache
  * write ("[vLLM] PagedAttention: OS 페이징 기법으로 KV 캐시를 관리하는 방법",
  * section "PagedAttention 커널", write_to_paged_cache) without fixing the format.

@@ -67,6 +67,11 @@ def load():
     lib.paged_attention_multi_query_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.pkv_set_multi_query_tile.restype = i32
     lib.pkv_set_multi_query_tile.argtypes = [i32]
+    lib.paged_attention_shared_prefix_workspace_size.restype = sz
+    lib.paged_attention_shared_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_decode_shared_prefix.restype = i32
+    lib.paged_attention_decode_shared_prefix.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, i32, i32,
+                                                         i32, i32, i32, P, sz, P]
     lib.paged_attention_multi_query.restype = i32
     lib.paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32, i32,
                                                 i32, i32, i32, i32, P, sz, P]
@@ -332,6 +337,48 @@ def paged_attention_multi_query(out: torch.Tensor, query: torch.Tensor, key_cach
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
         _ptr(context_lens), _ptr(query_start_loc), S, T, int(max_query_len), int(max_context_len), float(scale),
         B, H, Hkv, D, NB, dt, int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
+    return out
+
+
+def paged_attention_shared_prefix_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                                 block_size: int, prefix_len: int, max_tail_len: int) -> int:
+    return int(load().paged_attention_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                                   block_size, prefix_len, max_tail_len))
+
+
+def paged_attention_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                         value_cache: torch.Tensor, prefix_blocks: torch.Tensor, prefix_len: int,
+                                         block_tables: torch.Tensor, tail_lens: torch.Tensor, scale: float,
+                                         max_tail_len: Optional[int] = None,
+                                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode for sequences that share their first prefix_len tokens (prefix_blocks [prefix_len / B] int32);
+    block_tables [S][max] and tail_lens [S] describe each sequence's tokens after the prefix. Same result as
+    paged_attention_decode over prefix_blocks ++ block_tables[s], with the prefix read once."""
+    lib = load()
+    dt = _cuda16("query", query)
+    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
+        if _cuda16(n, t) != dt:
+            raise PagedKVError(-1, f"{n} dtype differs from query")
+    for n, t in (("prefix_blocks", prefix_blocks), ("block_tables", block_tables), ("tail_lens", tail_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    NB, Hkv, B, D = key_cache.shape
+    S, H, D2 = query.shape
+    if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise PagedKVError(-1, "shape mismatch between query, out and caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or tail_lens.shape != (S,):
+        raise PagedKVError(-1, "block_tables must be [S][max_blocks] and tail_lens [S]")
+    maxb = block_tables.shape[1]
+    if max_tail_len is None:
+        max_tail_len = maxb * B
+    need = paged_attention_shared_prefix_workspace_size(S, H, Hkv, D, B, int(prefix_len), int(max_tail_len))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(lib, lib.paged_attention_decode_shared_prefix(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(prefix_blocks), int(prefix_len),
+        _ptr(block_tables), maxb, _ptr(tail_lens), S, int(max_tail_len), float(scale), B, H, Hkv, D, NB, dt,
+        _ptr(workspace), wbytes, _stream(query, stream)))
     return out
 
 

@@ -286,6 +286,73 @@ __global__ void __launch_bounds__(32 * kReduceRows)
   }
 }
 
+// Shared-prefix decode: the output row (s, h) merges the prefix stage's np1
+// partials (every sequence attends the same prefix) with its own tail's
+// partials, ceil(tail_len / P2) of them, by the same log-sum-exp rule as the
+// split-K reduce: out = sum_p l_p 2^(m_p - M) o_p / sum_p l_p 2^(m_p - M),
+// M = max_p m_p (each o_p already divided by its l_p). One warp per row, lane
+// l holds dims l * D / 32 ...
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceRows)
+    pkv_merge_prefix_kernel(T* __restrict__ out, const float* __restrict__ o1, const float* __restrict__ m1,
+                            const float* __restrict__ l1, int np1, const float* __restrict__ o2,
+                            const float* __restrict__ m2, const float* __restrict__ l2, int np2, int p2,
+                            const int32_t* __restrict__ tail_lens, int tail_limit, int num_seqs, int num_heads) {
+  pdl_begin();
+  constexpr int DPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;
+  if (row >= (size_t)num_seqs * num_heads) return;
+  const int s = (int)(row / num_heads);
+  int t = tail_lens[s];
+  t = t < 0 ? 0 : (t > tail_limit ? tail_limit : t);  // as the tail stage clamped it
+  const int n2 = (t + p2 - 1) / p2;
+  const int n = np1 + n2;
+  auto at = [&](int q) { return q < np1 ? row * np1 + q : row * np2 + (q - np1); };
+  // one round of loads for the first 32 partials: lane q holds partial q's m and l
+  float mq = -INFINITY, lq = 0.f;
+  if (lane < n) {
+    mq = lane < np1 ? m1[at(lane)] : m2[at(lane)];
+    lq = lane < np1 ? l1[at(lane)] : l2[at(lane)];
+  }
+  float M = mq;
+  for (int q = 32 + lane; q < n; q += 32) M = fmaxf(M, q < np1 ? m1[at(q)] : m2[at(q)]);
+  M = warp_max(M);
+  float acc[DPL], W = 0.f;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  for (int q0 = 0; q0 < n; q0 += 32) {
+    float w = 0.f;
+    if (q0 == 0) {
+      w = mq == -INFINITY ? 0.f : lq * fast_exp2(mq - M);
+    } else if (q0 + lane < n) {
+      const int q = q0 + lane;
+      const float m = q < np1 ? m1[at(q)] : m2[at(q)];
+      w = m == -INFINITY ? 0.f : (q < np1 ? l1[at(q)] : l2[at(q)]) * fast_exp2(m - M);
+    }
+    W += warp_sum(w);
+    const int cnt = n - q0 < 32 ? n - q0 : 32;
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {  // independent loads of the partial outputs
+      const int q = q0 + k;
+      const float wk = __shfl_sync(kFull, w, k);
+      const float* o = (q < np1 ? o1 : o2) + at(q) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, o[e], acc[e]);
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  T* dst = out + row * D + lane * DPL;
+  if constexpr (DPL == 4) {
+    uint2 v;
+    v.x = Elem<T>::pack2(acc[0] * inv, acc[1] * inv);
+    v.y = Elem<T>::pack2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = Elem<T>::pack2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
 // mq.query_start_loc == nullptr: decode rows (num_seqs * num_heads).
 template <typename T>
 cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cudaStream_t stream,
@@ -619,6 +686,40 @@ pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, co
   return PKV_OK;
 }
 
+// How a shared-prefix decode splits its work (paged_attention_decode_shared_prefix).
+struct PrefixPlan {
+  bool tensor;   // prefix stage on the tensor-memory tile (else the 8-column tile)
+  int rt1;       // prefix row tiles per kv head (rows = num_seqs * group)
+  int pp, np1;   // prefix partition size (tokens, whole 64-token tiles) and count
+  int p2, np2;   // tail partition size and the most partitions a tail can have
+  int rt2;       // tail row tiles per kv head (group rows)
+};
+
+PrefixPlan prefix_plan(int num_seqs, int group, int num_kv_heads, int block_size, int prefix_len,
+                       int max_tail_len) {
+  PrefixPlan pl{};
+  const long long rows = (long long)num_seqs * group;
+  pl.tensor = rows >= PKV_MQ_WIDE_MIN_ROWS;
+  const int rpt = pl.tensor ? 128 : 8;
+  pl.rt1 = (int)((rows + rpt - 1) / rpt);
+  // about 256 prefix CTAs, so that the whole GPU shares the prefix's tiles
+  const long long per = (long long)num_kv_heads * (pl.rt1 > 0 ? pl.rt1 : 1);
+  long long want = (256 + per - 1) / per;
+  const int tiles = (prefix_len + 63) / 64;
+  if (want > tiles) want = tiles;
+  if (want < 1) want = 1;
+  int pp = (int)(((prefix_len + want - 1) / want + 63) / 64 * 64);
+  const int cap = kMaxPartitionBlocks * block_size;
+  if (pp > cap) pp = cap;
+  if (pp < 64) pp = 64;
+  pl.pp = pp;
+  pl.np1 = prefix_len > 0 ? (prefix_len + pp - 1) / pp : 0;
+  pl.p2 = mq_default_partition(block_size);
+  pl.np2 = max_partitions_for(max_tail_len, pl.p2);
+  pl.rt2 = (group + 7) / 8;
+  return pl;
+}
+
 }  // namespace
 
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
@@ -926,6 +1027,174 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
                          : launch_reduce<__nv_bfloat16>(p, num_seqs, head_dim, stream, mq);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
   }
+  return PKV_OK;
+}
+
+size_t paged_attention_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                                    int32_t head_dim, int32_t block_size, int32_t prefix_len,
+                                                    int32_t max_tail_len) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
+      block_size <= 0 || prefix_len < 0 || max_tail_len < 0)
+    return 0;
+  const PrefixPlan pl = prefix_plan(num_seqs, num_heads / num_kv_heads, num_kv_heads, block_size, prefix_len,
+                                    max_tail_len);
+  return (size_t)num_seqs * num_heads * (pl.np1 + pl.np2) * (head_dim + 2) * sizeof(float);
+}
+
+pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, const void* key_cache,
+                                                  const void* value_cache, const int32_t* prefix_blocks,
+                                                  int32_t prefix_len, const int32_t* block_tables,
+                                                  int32_t max_blocks_per_seq, const int32_t* tail_lens,
+                                                  int32_t num_seqs, int32_t max_tail_len, float scale,
+                                                  int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_msg[0] = '\0';
+  if (num_seqs < 0 || prefix_len < 0 || max_tail_len < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs, prefix_len and max_tail_len must be >= 0");
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
+                num_kv_heads);
+  if (num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
+  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (prefix_len % block_size)
+    return fail(PKV_ERR_INVALID_ARG, "prefix_len %d must be a whole number of blocks of %d", prefix_len, block_size);
+  if (max_tail_len > 0 && (max_blocks_per_seq <= 0 || (long long)max_tail_len > (long long)max_blocks_per_seq * block_size))
+    return fail(PKV_ERR_INVALID_ARG, "max_tail_len %d exceeds max_blocks_per_seq * block_size", max_tail_len);
+  const int G = num_heads / num_kv_heads;
+  const PrefixPlan pl = prefix_plan(num_seqs, G, num_kv_heads, block_size, prefix_len, max_tail_len);
+  if (num_seqs > 65535 || (long long)num_kv_heads * pl.rt1 > 65535 || (long long)num_kv_heads * pl.rt2 > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and the kv heads' row tiles must be <= 65535");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
+  if ((long long)num_seqs * num_heads >= (1LL << 31)) return fail(PKV_ERR_UNSUPPORTED, "num_seqs * num_heads >= 2^31");
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !query || !key_cache || !value_cache || !tail_lens || (prefix_len > 0 && !prefix_blocks) ||
+      (max_tail_len > 0 && !block_tables))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
+  const size_t need = paged_attention_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                                   block_size, prefix_len, max_tail_len);
+  if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", need);
+  if (workspace_bytes < need) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned* err = error_word(dev);
+  if (!err) return fail(PKV_ERR_CUDA, "device error word unavailable on device %d", dev);
+
+  const size_t rows = (size_t)num_seqs * num_heads;
+  float* ws = static_cast<float*>(workspace);
+  float *o1 = ws, *m1 = o1 + rows * pl.np1 * head_dim, *l1 = m1 + rows * pl.np1;
+  float *o2 = l1 + rows * pl.np1, *m2 = o2 + rows * pl.np2 * head_dim, *l2 = m2 + rows * pl.np2;
+
+  DecodeParams base{};
+  base.out = out;
+  base.query = query;
+  base.key_cache = static_cast<const unsigned char*>(key_cache);
+  base.value_cache = static_cast<const unsigned char*>(value_cache);
+  base.err = err;
+  base.scale_log2 = scale * 1.4426950408889634f;
+  base.v_scale = 1.f;
+  base.num_heads = num_heads;
+  base.num_kv_heads = num_kv_heads;
+  base.group = G;
+  base.num_blocks = num_blocks;
+
+  const long long pool_rows = (long long)num_blocks * num_kv_heads * block_size;
+  auto maps = [&](int tile, CUtensorMap* km, CUtensorMap* vm) {
+    memset(km, 0, sizeof *km);
+    memset(vm, 0, sizeof *vm);
+    if (head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy()))
+      return make_pool_map_tc(km, key_cache, pool_rows, block_size, dtype) &&
+             make_pool_map_tc(vm, value_cache, pool_rows, block_size, dtype);
+    return make_pool_map(km, key_cache, pool_rows, head_dim, block_size, dtype) &&
+           make_pool_map(vm, value_cache, pool_rows, head_dim, block_size, dtype);
+  };
+  auto run = [&](const DecodeParams& p, const MqParams& mq, const CUtensorMap& km, const CUtensorMap& vm, int seqs,
+                 int tile) {
+    return dtype == PKV_F16 ? decode_mq_f16(p, mq, km, vm, head_dim, block_size, seqs, tile, stream)
+                            : decode_mq_bf16(p, mq, km, vm, head_dim, block_size, seqs, tile, stream);
+  };
+  CUtensorMap kmap, vmap;
+  // 1. the prefix, once: all num_seqs * group rows of a kv head as the query rows of one context
+  if (pl.np1 > 0) {
+    const int tile = pl.tensor ? PKV_MQ_TILE_TENSOR : PKV_MQ_TILE_COLUMNS;
+    if (!maps(tile, &kmap, &vmap)) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+    DecodeParams p = base;
+    p.block_tables = prefix_blocks;
+    p.max_blocks_per_seq = prefix_len / block_size;
+    p.partition_size = pl.pp;
+    p.max_partitions = pl.np1;
+    p.ctx_limit = prefix_len;
+    p.part_o = o1;
+    p.part_m = m1;
+    p.part_l = l1;
+    MqParams mq{};
+    mq.mode = MQ_ONE_SEQ;
+    mq.num_query_tokens = num_seqs;
+    mq.max_query_len = num_seqs;
+    mq.row_tiles = pl.rt1;
+    mq.ctx_const = prefix_len;
+    mq.causal = 0;
+    mq.partials = 1;
+    e = run(p, mq, kmap, vmap, 1, tile);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel launch");
+  }
+  // 2. each sequence's tail: one query token per sequence over its own blocks
+  if (max_tail_len > 0) {
+    if (!maps(PKV_MQ_TILE_COLUMNS, &kmap, &vmap))
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+    DecodeParams p = base;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = tail_lens;
+    p.partition_size = pl.p2;
+    p.max_partitions = pl.np2;
+    p.ctx_limit = max_tail_len;
+    p.part_o = o2;
+    p.part_m = m2;
+    p.part_l = l2;
+    MqParams mq{};
+    mq.mode = MQ_ONE_PER_SEQ;
+    mq.num_query_tokens = num_seqs;
+    mq.max_query_len = 1;
+    mq.row_tiles = pl.rt2;
+    mq.partials = 1;
+    e = run(p, mq, kmap, vmap, num_seqs, PKV_MQ_TILE_COLUMNS);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix tail kernel launch");
+  }
+  // 3. merge
+  const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
+  const dim3 blk(32 * kReduceRows);
+  if (dtype == PKV_F16)
+    e = head_dim == 128
+            ? launch_kernel(pkv_merge_prefix_kernel<__half, 128>, dim3(grid), blk, 0, stream, static_cast<__half*>(out),
+                            (const float*)o1, (const float*)m1, (const float*)l1, pl.np1, (const float*)o2,
+                            (const float*)m2, (const float*)l2, pl.np2, pl.p2, tail_lens, max_tail_len, num_seqs,
+                            num_heads)
+            : launch_kernel(pkv_merge_prefix_kernel<__half, 64>, dim3(grid), blk, 0, stream, static_cast<__half*>(out),
+                            (const float*)o1, (const float*)m1, (const float*)l1, pl.np1, (const float*)o2,
+                            (const float*)m2, (const float*)l2, pl.np2, pl.p2, tail_lens, max_tail_len, num_seqs,
+                            num_heads);
+  else
+    e = head_dim == 128
+            ? launch_kernel(pkv_merge_prefix_kernel<__nv_bfloat16, 128>, dim3(grid), blk, 0, stream,
+                            static_cast<__nv_bfloat16*>(out), (const float*)o1, (const float*)m1, (const float*)l1,
+                            pl.np1, (const float*)o2, (const float*)m2, (const float*)l2, pl.np2, pl.p2, tail_lens,
+                            max_tail_len, num_seqs, num_heads)
+            : launch_kernel(pkv_merge_prefix_kernel<__nv_bfloat16, 64>, dim3(grid), blk, 0, stream,
+                            static_cast<__nv_bfloat16*>(out), (const float*)o1, (const float*)m1, (const float*)l1,
+                            pl.np1, (const float*)o2, (const float*)m2, (const float*)l2, pl.np2, pl.p2, tail_lens,
+                            max_tail_len, num_seqs, num_heads);
+  if (e != cudaSuccess) return cuda_fail(e, "shared-prefix merge launch");
   return PKV_OK;
 }
 

@@ -25,22 +25,50 @@
 
 namespace pkv {
 
-// Extra parameters of a multi-query launch.
+// Extra parameters of a multi-query launch. The defaults give the call's own
+// meaning: query_start_loc packs each sequence's query tokens, which are its
+// last q_len positions and attend causally.
 struct MqParams {
-  const int32_t* query_start_loc;  // [num_seqs + 1]
-  int num_query_tokens;            // host bound on query_start_loc entries
-  int max_query_len;               // host bound on every q_len
-  int row_tiles;                   // ceil(max_query_len * G / 8)
+  const int32_t* query_start_loc = nullptr;  // [num_seqs + 1] (mode MQ_PACKED)
+  int num_query_tokens = 0;                  // host bound on query_start_loc entries
+  int max_query_len = 0;                     // host bound on every q_len
+  int row_tiles = 1;                         // ceil(max_query_len * G / rows per CTA)
+  int mode = 0;        // MQ_PACKED, MQ_ONE_PER_SEQ (query token s of sequence s) or MQ_ONE_SEQ
+                       // (sequence 0 holds all num_query_tokens tokens)
+  int ctx_const = -1;  // >= 0: every sequence's context length (context_lens is not read)
+  int causal = 1;      // 0: every query row sees the whole context
+  int partials = 0;    // 1: write (m, l, o) partials even for a single-partition context
 };
+constexpr int MQ_PACKED = 0, MQ_ONE_PER_SEQ = 1, MQ_ONE_SEQ = 2;
 
-// q_len of sequence s, or -1 (and PKV_DEVERR_QUERY) if query_start_loc is
-// inconsistent with the bounds or the (clamped) context.
+// Context length of sequence s, clamped like clamp_context.
+__device__ __forceinline__ int mq_context(const DecodeParams& p, const MqParams& mq, int s, bool report) {
+  if (mq.ctx_const >= 0) return mq.ctx_const < p.ctx_limit ? mq.ctx_const : p.ctx_limit;
+  return clamp_context(p, s, report);
+}
+
+// q_len of sequence s and its first query row q0, or -1 (and PKV_DEVERR_QUERY)
+// if query_start_loc is inconsistent with the bounds or the (clamped) context.
+// One query token per sequence over an empty context gives 0 (no rows).
 __device__ __forceinline__ int mq_query_len(const MqParams& mq, int s, int ctx, int& q0) {
+  if (mq.mode == MQ_ONE_PER_SEQ) {
+    q0 = s;
+    return ctx > 0 ? 1 : 0;
+  }
+  if (mq.mode == MQ_ONE_SEQ) {
+    q0 = 0;
+    return s == 0 ? mq.num_query_tokens : 0;
+  }
   q0 = mq.query_start_loc[s];
   const int q1 = mq.query_start_loc[s + 1];
   const int n = q1 - q0;
-  if (q0 < 0 || n < 0 || q1 > mq.num_query_tokens || n > mq.max_query_len || n > ctx) return -1;
+  if (q0 < 0 || n < 0 || q1 > mq.num_query_tokens || n > mq.max_query_len || (mq.causal && n > ctx)) return -1;
   return n;
+}
+
+// Positions [0, limit) that query row r (token r / G of the sequence's q_len) sees.
+__device__ __forceinline__ int mq_limit(const MqParams& mq, int ctx, int q_len, int r, int G) {
+  return mq.causal ? ctx - q_len + r / G + 1 : ctx;
 }
 
 template <typename Tile, int NW, int SPW>
@@ -61,7 +89,7 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const bool reporter = part == 0 && blockIdx.y == 0 && threadIdx.x == 0;
-  const int ctx = clamp_context(p, s, reporter);
+  const int ctx = mq_context(p, mq, s, reporter);
   int q0 = 0;
   const int q_len = mq_query_len(mq, s, ctx, q0);
   if (q_len < 0) {
@@ -76,9 +104,9 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
   const int tok0 = part * P;
   if (tok0 >= ctx) return;
   // the tile's last row sees the most tokens; nothing past its limit is read
-  const int lim_max = ctx - q_len + (row0 + ncol - 1) / G + 1;
+  const int lim_max = mq_limit(mq, ctx, q_len, row0 + ncol - 1, G);
   const int tok1 = min(min(tok0 + P, ctx), lim_max);
-  const bool direct = ctx <= P;
+  const bool direct = !mq.partials && ctx <= P;
   const int blk0 = tok0 / BS;
   const int nblk = tok1 > tok0 ? (tok1 - tok0 + BS - 1) / BS : 0;
   const int nmine = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
@@ -133,8 +161,8 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
     if (n < ncol) qrow = reinterpret_cast<const T*>(p.query) + ((size_t)(q0 + r / G) * p.num_heads + kvh * G + r % G) * D;
   }
   const int j0 = (lane & 3) * 2;
-  const int lim0 = j0 < ncol ? ctx - q_len + (row0 + j0) / G + 1 : 0;
-  const int lim1 = j0 + 1 < ncol ? ctx - q_len + (row0 + j0 + 1) / G + 1 : 0;
+  const int lim0 = j0 < ncol ? mq_limit(mq, ctx, q_len, row0 + j0, G) : 0;
+  const int lim1 = j0 + 1 < ncol ? mq_limit(mq, ctx, q_len, row0 + j0 + 1, G) : 0;
   typename Tile::QB qb;
   Tile::load_qb_row(qb, qrow, lane);
   const float sl2 = p.scale_log2;

@@ -135,7 +135,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
     if (threadIdx.x == 0) atomicOr(p.err, PKV_DEVERR_LAYOUT);
     return;
   }
-  const int ctx = clamp_context(p, s, reporter);
+  const int ctx = mq_context(p, mq, s, reporter);
   int q0 = 0;
   const int q_len = mq_query_len(mq, s, ctx, q0);
   if (q_len < 0) {
@@ -148,9 +148,9 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
   const int P = p.partition_size;
   const int tok0 = part * P;
   if (tok0 >= ctx) return;
-  const int lim_cta = ctx - q_len + (min(row0 + Sh::ROWS, R) - 1) / G + 1;  // the CTA's last row's limit
+  const int lim_cta = mq_limit(mq, ctx, q_len, min(row0 + Sh::ROWS, R) - 1, G);  // the CTA's last row's limit
   const int tok1 = min(min(tok0 + P, ctx), lim_cta);
-  const bool direct = ctx <= P;
+  const bool direct = !mq.partials && ctx <= P;
   const int ntile = tok1 > tok0 ? (tok1 - tok0 + NT - 1) / NT : 0;
   const int blk0 = tok0 / BS;
 
@@ -338,7 +338,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
       fence_proxy_async_smem();  // generic stores, read by the S MMAs
       mbar_arrive(q_full);
     }
-    const int lim = active ? ctx - q_len + r / G + 1 : 0;  // this row sees positions < lim
+    const int lim = active ? mq_limit(mq, ctx, q_len, r, G) : 0;  // this row sees positions < lim
     const int vis = min(lim, tok1);
     const float sl2 = p.scale_log2;
     const uint32_t all = (1u << NBT) - 1u;

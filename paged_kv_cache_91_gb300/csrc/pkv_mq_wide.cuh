@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
   const int g = lane >> 2, qd = lane & 3;
   const int G = p.group;
   const bool reporter = part == 0 && blockIdx.y == 0 && threadIdx.x == 0;
-  const int ctx = clamp_context(p, s, reporter);
+  const int ctx = mq_context(p, mq, s, reporter);
   int q0 = 0;
   const int q_len = mq_query_len(mq, s, ctx, q0);
   if (q_len < 0) {
@@ -74,9 +74,9 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
   const int P = p.partition_size;
   const int tok0 = part * P;
   if (tok0 >= ctx) return;
-  const int lim_cta = ctx - q_len + (min(row0 + Sh::ROWS, R) - 1) / G + 1;  // the CTA's last row's limit
+  const int lim_cta = mq_limit(mq, ctx, q_len, min(row0 + Sh::ROWS, R) - 1, G);  // the CTA's last row's limit
   const int tok1 = min(min(tok0 + P, ctx), lim_cta);
-  const bool direct = ctx <= P;
+  const bool direct = !mq.partials && ctx <= P;
   const int blk0 = tok0 / BS;
   const int nblk = tok1 > tok0 ? (tok1 - tok0 + BS - 1) / BS : 0;
 
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(NW * 32, PKV_MQ_WIDE_MIN_CTAS)
   const int wrow0 = row0 + 16 * warp;
   const bool wactive = wrow0 < R;
   const int rA = wrow0 + g, rB = wrow0 + g + 8;
-  const int limA = rA < R ? ctx - q_len + rA / G + 1 : 0;
-  const int limB = rB < R ? ctx - q_len + rB / G + 1 : 0;
-  const int lim_w = wactive ? ctx - q_len + (min(wrow0 + 16, R) - 1) / G + 1 : 0;
+  const int limA = rA < R ? mq_limit(mq, ctx, q_len, rA, G) : 0;
+  const int limB = rB < R ? mq_limit(mq, ctx, q_len, rB, G) : 0;
+  const int lim_w = wactive ? mq_limit(mq, ctx, q_len, min(wrow0 + 16, R) - 1, G) : 0;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);

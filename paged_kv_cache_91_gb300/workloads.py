@@ -158,6 +158,25 @@ def _fill_pool(seed: int, stream: int, shape, dtype: str, outlier_frac: float,
     return out
 
 
+def split_shared_prefix(batch: "DecodeBatch", prefix_tokens: int):
+    """The arguments of the shared-prefix decode for a batch built with
+    ``shared_prefix_tokens=prefix_tokens``: (prefix_blocks [prefix_tokens / B]
+    int32, tail_tables [S][max tail blocks] int32, tail_lens [S] int32). Sequence
+    s's full table is prefix_blocks followed by tail_tables[s]."""
+    B = batch.block_size
+    if prefix_tokens % B or (batch.context_lens < prefix_tokens).any():
+        raise ValueError("prefix must be block aligned and within every context")
+    n = prefix_tokens // B
+    if n and (batch.block_tables[:, :n] != batch.block_tables[0, :n]).any():
+        raise ValueError("the sequences do not share their first blocks")
+    prefix = np.ascontiguousarray(batch.block_tables[0, :n], dtype=np.int32)
+    tails = np.ascontiguousarray(batch.block_tables[:, n:], dtype=np.int32)
+    if tails.shape[1] == 0:
+        tails = np.full((batch.num_seqs, 1), -1, dtype=np.int32)
+    tail_lens = (batch.context_lens - prefix_tokens).astype(np.int32)
+    return prefix, tails, tail_lens
+
+
 def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
                 head_dim: int, block_size: int, dtype: str, num_blocks: int | None = None,
                 pool_factor: float = 1.0, shared_prefix_tokens: int = 0,
@@ -195,8 +214,8 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
     if shared_prefix_tokens % B:
         raise ValueError("shared prefix must be block aligned")
     prefix_blocks = shared_prefix_tokens // B
-    if shared_prefix_tokens and (ctx <= shared_prefix_tokens).any():
-        raise ValueError("each sequence needs a private tail after the shared prefix")
+    if shared_prefix_tokens and (ctx < shared_prefix_tokens).any():
+        raise ValueError("every sequence must hold the whole shared prefix")
     nblk = (ctx + B - 1) // B
     private = nblk - prefix_blocks if prefix_blocks else nblk
     needed = int(prefix_blocks + private.sum())

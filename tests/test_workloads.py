@@ -121,6 +121,24 @@ def test_shared_prefix_tables():
     assert W.unique_kv_bytes(b) < W.algorithmic_kv_bytes(b)
 
 
+def test_split_shared_prefix():
+    """The prefix / tail split concatenates back to every sequence's table; a context equal to the
+    prefix has an empty tail."""
+    b = W.build_batch(seed=6, context_lens=[64 + 20, 64, 64 + 33], num_heads=4, num_kv_heads=2, head_dim=64,
+                      block_size=16, dtype=F16, shared_prefix_tokens=64, pool_factor=1.2)
+    prefix, tails, lens = W.split_shared_prefix(b, 64)
+    assert prefix.dtype == tails.dtype == lens.dtype == np.int32
+    assert list(lens) == [20, 0, 33]
+    for s in range(3):
+        nb = (b.context_lens[s] + 15) // 16
+        full = np.concatenate([prefix, tails[s]])[:nb]
+        assert (full == b.block_tables[s, :nb]).all()
+    with pytest.raises(ValueError):
+        W.split_shared_prefix(b, 80)  # not block aligned
+    with pytest.raises(ValueError):
+        W.split_shared_prefix(b, 128)  # longer than a context
+
+
 def test_key_outliers():
     b = W.build_batch(seed=5, context_lens=[4096] * 4, num_heads=4, num_kv_heads=4, head_dim=64,
                       block_size=16, dtype=F16, key_outlier_frac=0.01, key_outlier_scale=8.0)
