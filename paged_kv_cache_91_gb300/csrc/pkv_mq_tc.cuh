@@ -15,10 +15,12 @@
 //                                                      16-bit, over S_j's columns
 //   O  += P_j . V_j      M 128, N = head_dim, K 64    A from tensor memory
 //
-// Roles (6 warps): warp 0 copies K tiles into a three-slot ring and V tiles
-// into a two-slot ring; one thread of warp 1 issues every MMA; warps 2..5 each
-// own 32 rows (their tensor-memory lane quarter) for the softmax, write P_j
-// back into tensor memory where S_j was, and finally normalise and store O. A
+// Roles (7 warps): warp 0 copies K tiles into a three-slot ring and warp 2 V
+// tiles into a two-slot ring, one copy per pool block (a copy takes about 100
+// cycles to issue, so one warp for both fell behind); one thread of warp 1
+// issues every MMA; warps 3..6 each own 32 rows (their tensor-memory lane
+// quarter) for the softmax, write P_j back into tensor memory where S_j was,
+// and finally normalise and store O. A
 // K slot is refilled as soon as its S MMA has completed, a V slot (and the S/P
 // buffer) once its PV has. S/P is double-buffered in tensor memory, so S_{j+1}
 // is usually ready when the softmax of tile j ends, and the softmax never
@@ -37,6 +39,10 @@
 #include "pkv_tcgen05.cuh"
 
 namespace pkv {
+
+#ifndef PKV_MQ_TC_COPY_WARPS
+#define PKV_MQ_TC_COPY_WARPS 2  // 1: one warp copies K and V; 2: one warp each (build-time knob)
+#endif
 
 template <typename T, int D, int BS>
 struct MqTcShape {
@@ -68,7 +74,9 @@ struct MqTcShape {
   static constexpr int TMEM_COLS = 256;           // O at columns [0, D), S/P buffers at 128 and 192
   static constexpr int S_COL = 128;
   static constexpr int IDS = (kMaxPartitionBlocks + 31) / 32;
-  static constexpr int THREADS = 192;
+  static constexpr int CW = PKV_MQ_TC_COPY_WARPS;  // copy warps: warp 0 (and warp 2 for V)
+  static constexpr int SW = CW + 1;                // first of the four row warps
+  static constexpr int THREADS = (SW + 4) * 32;
   static_assert(BS * 128 % 1024 == 0, "a block's rows must fill whole 1024-byte swizzle atoms");
   static_assert(NT % BS == 0 && NBT <= 32, "tile of whole blocks");
   static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -103,7 +111,8 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
 }
 
 template <typename T, int D, int BS>
-__global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3 warps per SM quarter)
+// Two CTAs per SM: 6 warps x 168 registers (3 warps per SM quarter), or 7 x 128 (4 per quarter).
+__global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     pkv_mq_tc_kernel(const DecodeParams p, const MqParams mq, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
@@ -155,7 +164,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
   const int blk0 = tok0 / BS;
 
   // softmax rows: warps 2..5, thread row = 32 (warp % 4) + lane (its tensor-memory lane)
-  const bool srole = warp >= 2;
+  const bool srole = warp >= Sh::SW;
   const int row = 32 * (warp & 3) + lane;
   const int r = row0 + row;
   const bool active = srole && r < R;
@@ -188,8 +197,10 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ---- producer: K tile j and V tile j into slot j % 2 of their rings
+  if (warp == 0 || (Sh::CW == 2 && warp == 2)) {
+    // ---- copies: K tile j into slot j % 3 of the K ring, V tile j into slot j % 2 of the V ring
+    // (one warp for both, or warp 0 for K and warp 2 for V)
+    const bool do_k = Sh::CW == 1 || warp == 0, do_v = Sh::CW == 1 || warp == 2;
     int ids[Sh::IDS];  // lane l: block ids l, l + 32, ... of the partition; -1 for a bad id
     const int nblk = (tok1 - tok0 + BS - 1) / BS;
 #pragma unroll
@@ -200,7 +211,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
         const int v = p.block_tables[(size_t)s * p.max_blocks_per_seq + blk0 + b];
         if ((unsigned)v < (unsigned)p.num_blocks) {
           ids[u] = v;
-        } else {
+        } else if (do_k) {
           atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
         }
       }
@@ -210,12 +221,13 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
     int nk = 0, nv = 0;
     unsigned zeroed = 0;  // V slots whose tail rows the rows zeroed (generic stores)
     long long t_last = clock64();
-    while (nv < ntile) {
+    while (do_v ? nv < ntile : nk < ntile) {
       int which = -1;  // 0: K tile nk, 1: V tile nv
       if (lane == 0) {
-        if (nk < ntile && (nk < KST || mbar_test_wait(k_empty + nk % KST, ((nk / KST) - 1) & 1)))
+        if (do_k && nk < ntile && (nk < KST || mbar_test_wait(k_empty + nk % KST, ((nk / KST) - 1) & 1)))
           which = 0;
-        else if (nv < nk && (nv < 2 || mbar_test_wait(pv_done + (nv & 1), ((nv >> 1) - 1) & 1)))
+        else if (do_v && nv < (do_k ? nk : ntile) &&
+                 (nv < 2 || mbar_test_wait(pv_done + (nv & 1), ((nv >> 1) - 1) & 1)))
           which = 1;
         else if (*abort || clock64() - t_last > kWaitLimitCycles)
           which = 2;
@@ -441,7 +453,7 @@ __global__ void __maxnreg__(168)  // 6 warps x 168 registers: two CTAs per SM (3
           break;
         }
         unsigned char* vs = v_slot(j);
-        for (int i = threadIdx.x - 64; i < NT * 8 * DH; i += 128) {
+        for (int i = threadIdx.x - 32 * Sh::SW; i < NT * 8 * DH; i += 128) {
           const int t = i / (8 * DH), c = i % (8 * DH);
           if (!((mask >> (t / BS)) & 1u) || tb + t >= ctx)
             *reinterpret_cast<uint4*>(vs + (t / 8) * Sh::ATOM + (c / 8) * 1024 + tc::sw128(t % 8, c % 8)) =
