@@ -389,7 +389,11 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
  * 16-bit caches only (PKV_F16, PKV_BF16); head_dim 64 or 128; block_size 8, 16
  * or 32. Errors as in paged_attention_decode: bad block ids are skipped with
  * PKV_DEVERR_BLOCK_ID. Asynchronous on `stream`; three kernels (prefix, tails,
- * merge).
+ * merge). The prefix kernel runs on a second stream beside the tails: event
+ * waits order it after the work already queued on `stream` and the merge after
+ * it, so the call is ordered on `stream` as a whole and can be captured into a
+ * CUDA graph. That stream and its two events are created on first use, one
+ * set per host thread and device, and kept until the process exits.
  */
 size_t paged_attention_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads,
                                                     int32_t num_kv_heads, int32_t head_dim,

@@ -520,6 +520,30 @@ Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int 
   return pl;
 }
 
+// A second stream (and its fork / join events) on which the shared-prefix call
+// runs its prefix stage beside the tail stage. One per host thread and device,
+// created on first use and kept until the process exits. null if creation failed
+// (the call then runs its stages in order on the caller's stream).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+
+SideStream* side_stream(int dev) {
+  thread_local SideStream side[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& x = side[dev];
+  if (!x.tried) {
+    x.tried = true;
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
+      x.s = nullptr;
+  }
+  return x.s ? &x : nullptr;
+}
+
 int sm_count(int dev) {
   static int counts[kMaxDevices] = {};
   if (!counts[dev]) {
@@ -1119,11 +1143,22 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
            make_pool_map(vm, value_cache, pool_rows, head_dim, block_size, dtype);
   };
   auto run = [&](const DecodeParams& p, const MqParams& mq, const CUtensorMap& km, const CUtensorMap& vm, int seqs,
-                 int tile) {
-    return dtype == PKV_F16 ? decode_mq_f16(p, mq, km, vm, head_dim, block_size, seqs, tile, stream)
-                            : decode_mq_bf16(p, mq, km, vm, head_dim, block_size, seqs, tile, stream);
+                 int tile, cudaStream_t st) {
+    return dtype == PKV_F16 ? decode_mq_f16(p, mq, km, vm, head_dim, block_size, seqs, tile, st)
+                            : decode_mq_bf16(p, mq, km, vm, head_dim, block_size, seqs, tile, st);
   };
   CUtensorMap kmap, vmap;
+  // The prefix stage runs on a side stream beside the tail stage when both exist:
+  // the fork event orders it after everything queued on `stream`, the join event
+  // orders the merge after it.
+  SideStream* side = pl.np1 > 0 && max_tail_len > 0 ? side_stream(dev) : nullptr;
+  cudaStream_t prefix_stream = stream;
+  if (side) {
+    e = cudaEventRecord(side->fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream fork");
+    prefix_stream = side->s;
+  }
   // 1. the prefix, once: all num_seqs * group rows of a kv head as the query rows of one context
   if (pl.np1 > 0) {
     const int tile = pl.tensor ? PKV_MQ_TILE_TENSOR : PKV_MQ_TILE_COLUMNS;
@@ -1145,7 +1180,7 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
     mq.ctx_const = prefix_len;
     mq.causal = 0;
     mq.partials = 1;
-    e = run(p, mq, kmap, vmap, 1, tile);
+    e = run(p, mq, kmap, vmap, 1, tile, prefix_stream);
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel launch");
   }
   // 2. each sequence's tail: one query token per sequence over its own blocks
@@ -1168,8 +1203,13 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
     mq.max_query_len = 1;
     mq.row_tiles = pl.rt2;
     mq.partials = 1;
-    e = run(p, mq, kmap, vmap, num_seqs, PKV_MQ_TILE_COLUMNS);
+    e = run(p, mq, kmap, vmap, num_seqs, PKV_MQ_TILE_COLUMNS, stream);
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix tail kernel launch");
+  }
+  if (side) {
+    e = cudaEventRecord(side->join, side->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream join");
   }
   // 3. merge
   const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
