@@ -123,3 +123,50 @@ def test_rejections(cuda_lib):
         binding.paged_attention_decode_shared_prefix(*args, 64, torch.from_numpy(tails).to(DEV),
                                                      torch.from_numpy(lens).to(DEV), batch.scale,
                                                      workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+def test_graph_capture_and_replay(cuda_lib):
+    """The calls are stream-ordered (the shared-prefix call forks to a side stream and joins back), so a
+    CUDA graph captured around a write + shared-prefix decode + plain decode replays them correctly."""
+    batch = W.build_batch(seed=513, context_lens=256 + np.arange(40, 40 + 12 * 23, 23), num_heads=16,
+                          num_kv_heads=4, head_dim=128, block_size=16, dtype=BF16, pool_factor=1.3,
+                          shared_prefix_tokens=256)
+    t = W.as_torch(batch, DEV)
+    pb, tails, lens = W.split_shared_prefix(batch, 256)
+    max_tail = int(lens.max())  # host values only inside the capture: no device-to-host read there
+    pb, tails, lens = (torch.from_numpy(x).to(DEV) for x in (pb, tails, lens))
+    H, Hkv, D, B = batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
+    ws_sp = torch.empty(binding.paged_attention_shared_prefix_workspace_size(batch.num_seqs, H, Hkv, D, B, 256,
+                                                                             max_tail),
+                        dtype=torch.uint8, device=DEV)
+    ws_dec = torch.empty(max(16, binding.paged_attention_workspace_size(batch.num_seqs, H, Hkv, D, B,
+                                                                        batch.max_context_len)),
+                         dtype=torch.uint8, device=DEV)
+    out_sp = torch.zeros_like(t["query"])
+    out_dec = torch.zeros_like(t["query"])
+
+    def step():
+        binding.paged_kv_write(t["new_key"], t["new_value"], t["key_cache"], t["value_cache"], t["slot_mapping"])
+        binding.paged_attention_decode_shared_prefix(out_sp, t["query"], t["key_cache"], t["value_cache"], pb, 256,
+                                                     tails, lens, batch.scale, max_tail_len=max_tail, workspace=ws_sp)
+        binding.paged_attention_decode(out_dec, t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
+                                       t["context_lens"], batch.scale, max_context_len=batch.max_context_len,
+                                       workspace=ws_dec)
+
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(side):
+        step()  # warm up (library first-use setup) outside the capture
+    torch.cuda.current_stream(DEV).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    out_sp.zero_()
+    out_dec.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = reference(batch)
+    check_close(as_bits(out_sp), ref, BF16, "shared prefix, graph replay")
+    check_close(as_bits(out_dec), ref, BF16, "decode, graph replay")
+    assert binding.device_errors() == 0
