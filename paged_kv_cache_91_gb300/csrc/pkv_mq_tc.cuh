@@ -110,6 +110,36 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   }
 }
 
+// 16 bytes from global to shared memory without a register round trip;
+// `bytes` = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Thread `row` of the rows' warps brings its query row (rows r = rt * ROWS + row, query token
+// r / G, head kvh * G + r % G; zeros past q_len * G) into Q's A-operand layout: 128-byte swizzled
+// rows, columns 64.. in the next ROWS x 128 bytes. Out of line, which keeps the softmax loop's
+// registers free.
+template <typename T, int D, int ROWS>
+__device__ __noinline__ void mq_tc_fetch_q(unsigned char* Qs, int row, const T* query, int q0, int kvh, int rt,
+                                           int q_len, int G, int num_heads) {
+  const int r = rt * ROWS + row;
+  const bool act = r < q_len * G;
+  const T* src = query;
+  if (act) src += ((size_t)(q0 + r / G) * num_heads + kvh * G + r % G) * D;
+  const uint32_t dst = smem_u32(Qs) + row * 128, rx = row & 7;
+  if (act) {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) cp_async16(dst + (c / 8) * (ROWS * 128) + (((c % 8) ^ rx) << 4), src + c * 8, 16u);
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      *reinterpret_cast<uint4*>(Qs + row * 128 + (c / 8) * (ROWS * 128) + (((c % 8) ^ rx) << 4)) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <typename T, int D, int BS>
 // Two CTAs per SM: 6 warps x 168 registers (3 warps per SM quarter), or 7 x 128 (4 per quarter).
 __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
@@ -144,6 +174,26 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     if (threadIdx.x == 0) atomicOr(p.err, PKV_DEVERR_LAYOUT);
     return;
   }
+  // The first copies need the partition's block ids. In the first partition, which has tokens
+  // whenever the context does, the copy warps load them together with the context length (as far
+  // as the table row goes; masked below), so that the first copy waits for one memory round trip
+  // rather than two. Later partitions are often past the context and load them once it is known.
+  // (Requesting the query rows early as well measured slower.)
+  const bool srole = warp >= Sh::SW;
+  const int row = 32 * (warp & 3) + lane;
+  const bool early = part == 0;
+  int raw[Sh::IDS];
+  auto load_raw = [&] {
+    const int bb = part * p.partition_size / BS;
+#pragma unroll
+    for (int u = 0; u < Sh::IDS; ++u) {
+      const int b = lane + 32 * u;
+      raw[u] = b < p.partition_size / BS && bb + b < p.max_blocks_per_seq
+                   ? p.block_tables[(size_t)s * p.max_blocks_per_seq + bb + b]
+                   : -1;
+    }
+  };
+  if (early && (warp == 0 || (Sh::CW == 2 && warp == 2))) load_raw();
   const int ctx = mq_context(p, mq, s, reporter);
   int q0 = 0;
   const int q_len = mq_query_len(mq, s, ctx, q0);
@@ -153,19 +203,16 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   }
   const int R = q_len * G;
   const int row0 = rt * Sh::ROWS;
-  if (row0 >= R) return;
   const int P = p.partition_size;
   const int tok0 = part * P;
-  if (tok0 >= ctx) return;
+  if (row0 >= R || tok0 >= ctx) return;
   const int lim_cta = mq_limit(mq, ctx, q_len, min(row0 + Sh::ROWS, R) - 1, G);  // the CTA's last row's limit
   const int tok1 = min(min(tok0 + P, ctx), lim_cta);
   const bool direct = !mq.partials && ctx <= P;
   const int ntile = tok1 > tok0 ? (tok1 - tok0 + NT - 1) / NT : 0;
   const int blk0 = tok0 / BS;
 
-  // softmax rows: warps 2..5, thread row = 32 (warp % 4) + lane (its tensor-memory lane)
-  const bool srole = warp >= Sh::SW;
-  const int row = 32 * (warp & 3) + lane;
+  // softmax rows: warps SW.., thread row = 32 (warp % 4) + lane (its tensor-memory lane)
   const int r = row0 + row;
   const bool active = srole && r < R;
   const size_t orow = active ? (size_t)(q0 + r / G) * p.num_heads + kvh * G + r % G : 0;  // output row
@@ -201,6 +248,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     // ---- copies: K tile j into slot j % 3 of the K ring, V tile j into slot j % 2 of the V ring
     // (one warp for both, or warp 0 for K and warp 2 for V)
     const bool do_k = Sh::CW == 1 || warp == 0, do_v = Sh::CW == 1 || warp == 2;
+    if (!early) load_raw();
     int ids[Sh::IDS];  // lane l: block ids l, l + 32, ... of the partition; -1 for a bad id
     const int nblk = (tok1 - tok0 + BS - 1) / BS;
 #pragma unroll
@@ -208,9 +256,8 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
       const int b = lane + 32 * u;
       ids[u] = -1;
       if (b < nblk) {
-        const int v = p.block_tables[(size_t)s * p.max_blocks_per_seq + blk0 + b];
-        if ((unsigned)v < (unsigned)p.num_blocks) {
-          ids[u] = v;
+        if ((unsigned)raw[u] < (unsigned)p.num_blocks) {
+          ids[u] = raw[u];
         } else if (do_k) {
           atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
         }
@@ -339,17 +386,11 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     __syncwarp();
   } else if (srole) {
     // ---- softmax rows
-    {  // Q rows into the A operand layout (zeros past R), while the producer starts the copies
-      const uint4* src = active ? reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.query) + orow * D)
-                                : nullptr;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = active ? src[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Qs + (c / 8) * (Sh::ROWS * 128) + tc::sw128(row, c % 8)) = v;
-      }
-      fence_proxy_async_smem();  // generic stores, read by the S MMAs
-      mbar_arrive(q_full);
-    }
+    // the query rows (zeros past R), copied while the copy warps start: tell the MMA thread once landed
+    mq_tc_fetch_q<T, D, Sh::ROWS>(Qs, row, reinterpret_cast<const T*>(p.query), q0, kvh, rt, q_len, G, p.num_heads);
+    cp_async_wait_all();
+    fence_proxy_async_smem();  // generic-proxy writes, read by the S MMAs
+    mbar_arrive(q_full);
     const int lim = active ? mq_limit(mq, ctx, q_len, r, G) : 0;  // this row sees positions < lim
     const int vis = min(lim, tok1);
     const float sl2 = p.scale_log2;
