@@ -307,7 +307,16 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *   partition_size    0 = 2048 tokens, capped at 128 blocks (every query row
  *                     writes a partial per partition, so long partitions are
  *                     fastest here); else as in paged_attention_decode
- *   workspace         paged_attention_multi_query_workspace_size(...) bytes
+ *   workspace         paged_attention_multi_query_workspace_size(...) bytes: the
+ *                     split-K partials (required when a context spans several
+ *                     partitions), then room for one int32 per sequence that
+ *                     the 128-row tile fills with the sequences ordered by
+ *                     context length, longest first, and dispatches its grid
+ *                     in that order (its long items start first, which
+ *                     shortens the grid's end). A workspace of only the
+ *                     partials' size, or none when there are no partials, is
+ *                     accepted: the sequences then run in index order. The
+ *                     order changes no result.
  * Everything else is as in paged_attention_decode (the decode-path choice does
  * not apply: this call always runs partitioned, on the tensor cores, for every
  * group size). A sequence whose query_start_loc entries are out of order, give

@@ -373,6 +373,54 @@ cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cud
 // copy-on-write block copy: every 16-byte piece of physical block src (all kv
 // heads, K and V) goes to block dst. Grid: (pieces, pairs).
 
+constexpr int kOrderBuckets = 1024;
+// The sequences by context length, longest first: a counting sort into 1024 length classes of
+// ceil(ctx_limit / 1024) tokens (the order within a class is arbitrary and does not change any result).
+// One CTA. The 128-row multi-query tile dispatches its grid in this order.
+__global__ void __launch_bounds__(1024)
+    pkv_mq_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs, int ctx_limit, int32_t* __restrict__ order) {
+  pdl_begin();
+  __shared__ int cnt[kOrderBuckets];
+  __shared__ int wsum[32];
+  const int t = threadIdx.x;
+  cnt[t] = 0;
+  __syncthreads();
+  const int gran = max(1, (ctx_limit + kOrderBuckets - 1) / kOrderBuckets);
+  auto key = [&](int s) {
+    int c = context_lens[s];
+    c = c < 0 ? 0 : (c > ctx_limit ? ctx_limit : c);
+    return min(kOrderBuckets - 1, c / gran);
+  };
+  for (int s = t; s < num_seqs; s += kOrderBuckets) atomicAdd(&cnt[key(s)], 1);
+  __syncthreads();
+  // thread t takes class b = 1023 - t: its first position is the count of all longer classes
+  const int b = kOrderBuckets - 1 - t;
+  const int v = cnt[b];
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if ((t & 31) >= o) x += y;
+  }
+  if ((t & 31) == 31) wsum[t >> 5] = x;
+  __syncthreads();
+  if (t < 32) {
+    int w = wsum[t];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, w, o);
+      if (t >= o) w += y;
+    }
+    wsum[t] = w;
+  }
+  __syncthreads();
+  const int first = x - v + ((t >> 5) ? wsum[(t >> 5) - 1] : 0);
+  cnt[b] = first;
+  __syncthreads();
+  for (int s = t; s < num_seqs; s += kOrderBuckets) order[atomicAdd(&cnt[key(s)], 1)] = s;
+}
+
+
 __global__ void pkv_copy_blocks_kernel(uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
                                        const int64_t* __restrict__ block_mapping, long long pieces_per_block,
                                        long long num_blocks, unsigned* err) {
@@ -922,15 +970,27 @@ pkv_status_t paged_attention_decode_fp8(void* out, const void* query, const void
                      partition_size, workspace, workspace_bytes, stream, true, k_scale, v_scale);
 }
 
+namespace {
+// Split-K partials of a multi-query call, at the start of its workspace.
+size_t mq_partials_bytes(int num_query_tokens, int num_heads, int head_dim, int block_size, int max_context_len,
+                         int partition_size) {
+  const int P = partition_size ? partition_size : mq_default_partition(block_size);
+  const int np = max_partitions_for(max_context_len, P);
+  return np > 1 ? (size_t)num_query_tokens * num_heads * np * (head_dim + 2) * sizeof(float) : 0;
+}
+// The sequence order of the 128-row tile, after the partials: one int32 per sequence, and a sequence
+// with query tokens has at least one, so num_query_tokens entries bound it.
+size_t mq_order_bytes(int n) { return ((size_t)n * sizeof(int32_t) + 255) / 256 * 256; }
+}  // namespace
+
 size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int32_t num_heads, int32_t num_kv_heads,
                                                   int32_t head_dim, int32_t block_size, int32_t max_context_len,
                                                   int32_t partition_size) {
   if (num_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_dim <= 0 ||
       block_size <= 0 || max_context_len < 0 || partition_size < 0)
     return 0;
-  const int P = partition_size ? partition_size : mq_default_partition(block_size);
-  const int np = max_partitions_for(max_context_len, P);
-  return np > 1 ? (size_t)num_query_tokens * num_heads * np * (head_dim + 2) * sizeof(float) : 0;
+  return mq_partials_bytes(num_query_tokens, num_heads, head_dim, block_size, max_context_len, partition_size) +
+         mq_order_bytes(num_query_tokens);
 }
 
 pkv_status_t paged_attention_multi_query(void* out, const void* query, const void* key_cache,
@@ -987,8 +1047,10 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
     return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
   const int np = max_partitions_for(max_context_len, P);
-  const size_t need = paged_attention_multi_query_workspace_size(num_query_tokens, num_heads, num_kv_heads, head_dim,
-                                                                 block_size, max_context_len, partition_size);
+  // the partials are required; room for the sequence order after them is optional (without it the
+  // 128-row tile runs the sequences in index order)
+  const size_t need = mq_partials_bytes(num_query_tokens, num_heads, head_dim, block_size, max_context_len,
+                                        partition_size);
   if (need) {
     if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", need);
     if (workspace_bytes < need)
@@ -1032,6 +1094,15 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   mq.num_query_tokens = num_query_tokens;
   mq.max_query_len = max_query_len;
   mq.row_tiles = (int)row_tiles;
+  const size_t order_at = (need + 255) / 256 * 256;
+  if (tile == PKV_MQ_TILE_TENSOR && num_seqs > 1 && workspace && aligned16(workspace) &&
+      workspace_bytes >= order_at + (size_t)num_seqs * sizeof(int32_t)) {
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + order_at);
+    e = launch_kernel(pkv_mq_order_kernel, dim3(1), dim3(kOrderBuckets), 0, stream, context_lens, num_seqs,
+                      max_context_len, order);
+    if (e != cudaSuccess) return cuda_fail(e, "sequence order kernel launch");
+    mq.order = order;
+  }
 
   CUtensorMap kmap, vmap;
   memset(&kmap, 0, sizeof kmap);

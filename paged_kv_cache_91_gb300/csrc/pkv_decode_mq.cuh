@@ -38,6 +38,7 @@ struct MqParams {
   int ctx_const = -1;  // >= 0: every sequence's context length (context_lens is not read)
   int causal = 1;      // 0: every query row sees the whole context
   int partials = 0;    // 1: write (m, l, o) partials even for a single-partition context
+  const int32_t* order = nullptr;  // 128-row tile: sequence of grid index z (longest context first)
 };
 constexpr int MQ_PACKED = 0, MQ_ONE_PER_SEQ = 1, MQ_ONE_SEQ = 2;
 

@@ -166,7 +166,9 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
 
   const int part = blockIdx.x;
   const int kvh = blockIdx.y / mq.row_tiles, rt = blockIdx.y % mq.row_tiles;
-  const int s = blockIdx.z;
+  // with an order, grid index z runs over the sequences longest context first, so that the long
+  // items start early and the grid's end is made of short ones
+  const int s = mq.order ? mq.order[blockIdx.z] : (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const bool reporter = part == 0 && blockIdx.y == 0 && threadIdx.x == 0;

@@ -232,11 +232,13 @@ def test_fp8_zero_work_is_a_noop(lib):
 
 def test_multi_query_workspace_size(lib):
     ws = lib.paged_attention_multi_query_workspace_size
-    assert ws(100, 32, 8, 128, 16, 512, 512) == 0  # one partition
-    assert ws(100, 32, 8, 128, 16, 513, 512) == 100 * 32 * 2 * 130 * 4
-    assert ws(100, 32, 8, 128, 16, 2048, 0) == 0  # 0 selects 2048 tokens
-    assert ws(100, 32, 8, 128, 8, 2048, 0) == 100 * 32 * 2 * 130 * 4  # capped at 128 blocks of 8
-    assert ws(7, 4, 4, 64, 16, 2048, 256) == 7 * 4 * 8 * 66 * 4
+    order = 512  # room for the sequence order: 100 int32, rounded up to 256 bytes
+    assert ws(100, 32, 8, 128, 16, 512, 512) == order  # one partition: no partials
+    assert ws(100, 32, 8, 128, 16, 513, 512) == 100 * 32 * 2 * 130 * 4 + order
+    assert ws(100, 32, 8, 128, 16, 2048, 0) == order  # 0 selects 2048 tokens
+    assert ws(100, 32, 8, 128, 8, 2048, 0) == 100 * 32 * 2 * 130 * 4 + order  # capped at 128 blocks of 8
+    assert ws(7, 4, 4, 64, 16, 2048, 256) == 7 * 4 * 8 * 66 * 4 + 256
+    assert ws(0, 4, 4, 64, 16, 2048, 256) == 0
     assert ws(-1, 4, 4, 64, 16, 2048, 256) == 0
 
 

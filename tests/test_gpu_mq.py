@@ -166,3 +166,34 @@ def test_query_count_above_context_is_reported():
     run_mq(batch, t, max_query_len=2)
     torch.cuda.synchronize()
     assert binding.device_errors() & 16
+
+
+def test_sequence_order_changes_nothing(mq_tile):
+    """With room for it in the workspace, the 128-row tile runs the sequences longest context first; with a
+    workspace of only the partials' size it runs them in index order. The outputs are bit-identical (the
+    order moves whole items between CTAs, never the arithmetic of one) and match the oracle."""
+    rng = np.random.default_rng(95)
+    S = 24
+    ctx = rng.integers(64, 3000, size=S)  # some past 2048 tokens: split into two partitions
+    ql = np.minimum(rng.integers(20, 65, size=S), ctx)
+    batch = W.build_batch(seed=96, context_lens=ctx, num_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                          dtype=F16, pool_factor=1.2, query_lens=ql)
+    t = W.as_torch(batch, DEV)
+    T, H, Hkv, D, B = int(batch.query_start_loc[-1]), batch.num_heads, batch.num_kv_heads, batch.head_dim, 16
+    full = binding.paged_attention_multi_query_workspace_size(T, H, Hkv, D, B, batch.max_context_len)
+    order_room = (T * 4 + 255) // 256 * 256
+    partials = full - order_room
+    assert partials > 0
+    outs = []
+    for nbytes in (full, partials):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        out = torch.empty_like(t["query"])
+        binding.paged_attention_multi_query(out, t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
+                                            t["context_lens"], t["query_start_loc"], batch.scale,
+                                            max_query_len=int(ql.max()), max_context_len=batch.max_context_len,
+                                            workspace=ws)
+        outs.append(as_bits(out))
+    torch.cuda.synchronize()
+    assert np.array_equal(outs[0], outs[1])
+    check_close(outs[0], reference(batch), F16, f"{mq_tile}, sequence order")
+    assert binding.device_errors() == 0
