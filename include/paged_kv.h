@@ -310,9 +310,9 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *   workspace         paged_attention_multi_query_workspace_size(...) bytes: the
  *                     split-K partials (required when a context spans several
  *                     partitions), then room for one int32 per sequence that
- *                     the 128-row tile fills with the sequences ordered by
- *                     context length, longest first, and dispatches its grid
- *                     in that order (its long items start first, which
+ *                     the 8-column and 128-row tiles fill with the sequences
+ *                     ordered by context length, longest first, and dispatch
+ *                     their grids in that order (its long items start first, which
  *                     shortens the grid's end). A workspace of only the
  *                     partials' size, or none when there are no partials, is
  *                     accepted: the sequences then run in index order. The

@@ -376,7 +376,7 @@ cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cud
 constexpr int kOrderBuckets = 1024;
 // The sequences by context length, longest first: a counting sort into 1024 length classes of
 // ceil(ctx_limit / 1024) tokens (the order within a class is arbitrary and does not change any result).
-// One CTA. The 128-row multi-query tile dispatches its grid in this order.
+// One CTA. The 8-column and 128-row multi-query tiles dispatch their grids in this order.
 __global__ void __launch_bounds__(1024)
     pkv_mq_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs, int ctx_limit, int32_t* __restrict__ order) {
   pdl_begin();
@@ -1048,7 +1048,7 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
     return fail(PKV_ERR_INVALID_ARG, "out, query and caches must be 16-byte aligned");
   const int np = max_partitions_for(max_context_len, P);
   // the partials are required; room for the sequence order after them is optional (without it the
-  // 128-row tile runs the sequences in index order)
+  // tiles run the sequences in index order)
   const size_t need = mq_partials_bytes(num_query_tokens, num_heads, head_dim, block_size, max_context_len,
                                         partition_size);
   if (need) {
@@ -1095,7 +1095,7 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   mq.max_query_len = max_query_len;
   mq.row_tiles = (int)row_tiles;
   const size_t order_at = (need + 255) / 256 * 256;
-  if (tile == PKV_MQ_TILE_TENSOR && num_seqs > 1 && workspace && aligned16(workspace) &&
+  if (tile != PKV_MQ_TILE_ROWS && num_seqs > 1 && workspace && aligned16(workspace) &&
       workspace_bytes >= order_at + (size_t)num_seqs * sizeof(int32_t)) {
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + order_at);
     e = launch_kernel(pkv_mq_order_kernel, dim3(1), dim3(kOrderBuckets), 0, stream, context_lens, num_seqs,

@@ -38,7 +38,7 @@ struct MqParams {
   int ctx_const = -1;  // >= 0: every sequence's context length (context_lens is not read)
   int causal = 1;      // 0: every query row sees the whole context
   int partials = 0;    // 1: write (m, l, o) partials even for a single-partition context
-  const int32_t* order = nullptr;  // 128-row tile: sequence of grid index z (longest context first)
+  const int32_t* order = nullptr;  // if set, the sequence of grid index z (longest context first)
 };
 constexpr int MQ_PACKED = 0, MQ_ONE_PER_SEQ = 1, MQ_ONE_SEQ = 2;
 
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
 
   const int part = blockIdx.x;
   const int kvh = blockIdx.y / mq.row_tiles, rt = blockIdx.y % mq.row_tiles;
-  const int s = blockIdx.z;
+  const int s = mq.order ? mq.order[blockIdx.z] : (int)blockIdx.z;  // long contexts first
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const bool reporter = part == 0 && blockIdx.y == 0 && threadIdx.x == 0;
