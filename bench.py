@@ -367,7 +367,7 @@ def mq_summary(batch, tile_arg, call_ms):
     vis = (ql * (ctx - ql) + ql * (ql + 1) // 2).sum()  # positions seen, summed over query tokens
     flops = 4.0 * batch.head_dim * batch.num_heads * float(vis)
     rows_per_kv_head = int(ql.max()) * (batch.num_heads // batch.num_kv_heads)
-    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head >= 64 else "columns")
+    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head > 16 else "columns")
     return {"tile": tile, "rows_per_kv_head": rows_per_kv_head, "attention_gflop_per_call": round(flops / 1e9, 2),
             "attention_tflops": round(flops / (call_ms * 1e-3) / 1e12, 1)}
 

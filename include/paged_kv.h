@@ -338,7 +338,8 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *                        (tcgen05): scores and outputs accumulate in tensor
  *                        memory, one thread per row runs the softmax.
  *   PKV_MQ_TILE_AUTO     TENSOR when max_query_len * (num_heads / num_kv_heads)
- *                        >= 64, else COLUMNS (default).
+ *                        > 16 (more than two 8-column CTAs per kv head), else
+ *                        COLUMNS (default).
  */
 #define PKV_MQ_TILE_AUTO 0
 #define PKV_MQ_TILE_COLUMNS 1
