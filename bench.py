@@ -63,7 +63,8 @@ def parse_args():
                     help="decode path (default: the library's automatic choice)")
     ap.add_argument("--kv-dtype", choices=["auto", "fp8_e4m3"], default="auto",
                     help="auto: the cache holds the workload's fp16/bf16 values; fp8_e4m3: E4M3 codes "
-                         "(paged_kv_write_fp8 / paged_attention_decode_fp8, k_scale = v_scale = FP8_SCALE)")
+                         "(paged_kv_write_fp8 / paged_attention_decode_fp8, or paged_attention_multi_query_fp8 "
+                         "with --query-len; k_scale = v_scale = FP8_SCALE)")
     ap.add_argument("--query-len", type=int, default=None,
                     help="multi-query step: each sequence's last N context tokens are written and attend causally "
                          "(paged_attention_multi_query; speculative verification / chunked prefill)")
@@ -176,6 +177,8 @@ KERNEL_SOURCES = {
     "mma_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mma_fp8.cu"),
     "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_mq_wide.cuh", "pkv_mq_tc.cuh",
            "pkv_tcgen05.cuh", "pkv_decode_mq.cu"),
+    "mq_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mq.cuh",
+               "pkv_decode_mq_fp8.cu"),
 }
 
 
@@ -334,15 +337,18 @@ def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1, fp8_pools=None)
             return el, reps
 
 
-def time_oracle_mq(batch, budget_s: float):
-    """Run the multi-query oracle over the whole batch until budget_s; returns (seconds, reps)."""
+def time_oracle_mq(batch, budget_s: float, fp8_pools=None):
+    """Run the multi-query oracle over the whole batch until budget_s; returns (seconds, reps).
+    fp8_pools: (key codes, value codes) of an FP8 cache with k_scale = v_scale = FP8_SCALE."""
     import oracle
 
+    kc, vc = fp8_pools if fp8_pools is not None else (batch.key_cache, batch.value_cache)
+    sc = FP8_SCALE if fp8_pools is not None else 1.0
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.multi_query_c(batch.query, batch.key_cache, batch.value_cache, batch.block_tables,
-                             batch.context_lens, batch.query_start_loc, batch.scale, batch.dtype)
+        oracle.multi_query_c(batch.query, kc, vc, batch.block_tables, batch.context_lens, batch.query_start_loc,
+                             batch.scale, batch.dtype, k_scale=sc, v_scale=sc)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -357,7 +363,7 @@ def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
 # ----------------------------------------------------------------------------
 
 
-def mq_summary(batch, tile_arg, call_ms):
+def mq_summary(batch, tile_arg, call_ms, fp8=False):
     """The multi-query tile that ran and the rate of its attention arithmetic (causal QK and PV, 4 flops per
     (row, visible position, dim))."""
     import numpy as np
@@ -368,6 +374,8 @@ def mq_summary(batch, tile_arg, call_ms):
     flops = 4.0 * batch.head_dim * batch.num_heads * float(vis)
     rows_per_kv_head = int(ql.max()) * (batch.num_heads // batch.num_kv_heads)
     tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head > 16 else "columns")
+    if fp8:
+        tile = "columns"  # the one tile with an E4M3 contraction
     return {"tile": tile, "rows_per_kv_head": rows_per_kv_head, "attention_gflop_per_call": round(flops / 1e9, 2),
             "attention_tflops": round(flops / (call_ms * 1e-3) / 1e12, 1)}
 
@@ -460,8 +468,6 @@ def run_ours(args, dist):
     P = args.partition_size
     t = W.as_torch(batch, dev)
     mq = args.query_len is not None
-    if mq and args.kv_dtype != "auto":
-        raise SystemExit("--query-len runs on 16-bit caches only")
     max_query_len = int(np.diff(batch.query_start_loc).max()) if mq else 1
     n_query_rows = int(batch.query_start_loc[-1]) if mq else batch.num_seqs  # query tokens per step
     out = torch.empty_like(t["query"])
@@ -527,6 +533,11 @@ def run_ours(args, dist):
             binding.paged_attention_decode_shared_prefix(o, q, t["key_cache"], t["value_cache"], prefix_dev,
                                                          SHARED_PREFIX_TOKENS, bt, cl, batch.scale,
                                                          max_tail_len=max_tail, workspace=ws, stream=stream)
+        elif mq and fp8:
+            binding.paged_attention_multi_query_fp8(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
+                                                    FP8_SCALE, FP8_SCALE, max_query_len=max_query_len,
+                                                    max_context_len=mcl, partition_size=P, workspace=ws,
+                                                    stream=stream)
         elif mq:
             binding.paged_attention_multi_query(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
                                                 max_query_len=max_query_len, max_context_len=mcl, partition_size=P,
@@ -621,7 +632,7 @@ def run_ours(args, dist):
     workload = f"cfg{args.config}" + ("-fp8" if fp8 else "") + (f"-q{args.query_len}" if mq else "")
     G = batch.num_heads // batch.num_kv_heads
     if mq:
-        kind = "mq"
+        kind = "mq_fp8" if fp8 else "mq"
     elif fp8:
         kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
     else:
@@ -633,11 +644,11 @@ def run_ours(args, dist):
         import oracle
 
         seqs = list(range(batch.num_seqs))
+        pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
         if mq:
-            el, reps = time_oracle_mq(batch, args.cpu_seconds)
+            el, reps = time_oracle_mq(batch, args.cpu_seconds, fp8_pools=pools)
             what = "multi-query"
         else:
-            pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
             el, reps = time_oracle(batch, seqs, args.cpu_seconds, fp8_pools=pools)
             what = "decode"
         cpu = {"value": round(kv_bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
@@ -658,7 +669,7 @@ def run_ours(args, dist):
                             "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
             "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_shared_prefix (prefix, tail and merge "
                          "kernels; bytes: the prefix once, the tails, q, out, partials)" if shared else
-                         ("paged_attention_multi_query" if mq else
+                         ("paged_attention_multi_query" + ("_fp8" if fp8 else "") if mq else
                                                     "paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
                          + (" (multi-query kernel" if mq else " (decode kernel")
                          + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
@@ -675,7 +686,7 @@ def run_ours(args, dist):
             "cpu_baseline": cpu,
         }
         if mq:
-            line["multi_query"] = mq_summary(batch, args.mq_tile, dec_avg_ms)
+            line["multi_query"] = mq_summary(batch, args.mq_tile, dec_avg_ms, fp8)
         if shared:
             line["config"]["call"] = (f"paged_attention_decode_shared_prefix: the {SHARED_PREFIX_TOKENS}-token "
                                       "prefix attended once for the whole batch, then each tail, then a merge")

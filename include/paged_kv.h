@@ -367,6 +367,34 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
                                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * paged_attention_multi_query_fp8 -- paged_attention_multi_query over an FP8
+ * (E4M3) pool ("vLLM PagedAttention Kernel", the kv_cache_dtype, k_scale and
+ * v_scale of reshape_and_cache; the scales as in paged_attention_decode_fp8:
+ * a cached code c stands for c * k_scale in K and c * v_scale in V).
+ *
+ *   key_cache,        [num_blocks][num_kv_heads][block_size][head_dim] uint8
+ *   value_cache       E4M3 codes, as written by paged_kv_write_fp8
+ *   dtype             of query and out (PKV_F16 or PKV_BF16)
+ *   k_scale, v_scale  finite and > 0
+ * head_dim must be 128 (PKV_ERR_UNSUPPORTED otherwise). Every other argument,
+ * the workspace (paged_attention_multi_query_workspace_size) and the results'
+ * meaning are those of paged_attention_multi_query. Every row count runs on
+ * the 8-column tile (pkv_set_multi_query_tile does not apply): the tensor
+ * tiles multiply 16-bit operands only, so rows past 8 per kv head cost one
+ * more pass over the context per 8 rows.
+ */
+pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const void* key_cache,
+                                             const void* value_cache, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                             const int32_t* query_start_loc, int32_t num_seqs,
+                                             int32_t num_query_tokens, int32_t max_query_len,
+                                             int32_t max_context_len, float scale, int32_t block_size,
+                                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                             int32_t num_blocks, pkv_dtype_t dtype, float k_scale,
+                                             float v_scale, int32_t partition_size, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * paged_attention_decode_shared_prefix -- the decode step of a batch whose
  * sequences all begin with the same prefix blocks (one prompt with several
  * continuations, as in parallel sampling or beam search). Copy-on-write keeps

@@ -75,6 +75,9 @@ def load():
     lib.paged_attention_multi_query.restype = i32
     lib.paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32, i32,
                                                 i32, i32, i32, i32, P, sz, P]
+    lib.paged_attention_multi_query_fp8.restype = i32
+    lib.paged_attention_multi_query_fp8.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32,
+                                                    i32, i32, i32, i32, f32, f32, i32, P, sz, P]
     lib.paged_attention_decode_fp8.restype = i32
     lib.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
                                                f32, f32, i32, P, sz, P]
@@ -297,21 +300,16 @@ def paged_attention_multi_query_workspace_size(num_query_tokens: int, num_heads:
                                                                  partition_size))
 
 
-def paged_attention_multi_query(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
-                                value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
-                                query_start_loc: torch.Tensor, scale: float, max_query_len: Optional[int] = None,
-                                max_context_len: Optional[int] = None, partition_size: int = 0,
-                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Causal attention of several query tokens per sequence (query/out [T][H][D], packed by
-    query_start_loc [S+1] int32): sequence s's q_len tokens are its last q_len context positions.
-
-    ``max_query_len`` bounds every q_len on the host; when omitted it is read from
-    query_start_loc, which synchronises the stream.
-    """
+def _multi_query(out, query, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale,
+                 max_query_len, max_context_len, partition_size, workspace, stream, fp8, k_scale, v_scale):
     lib = load()
     dt = _cuda16("query", query)
-    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
-        if _cuda16(n, t) != dt:
+    if _cuda16("out", out) != dt:
+        raise PagedKVError(-1, "out dtype differs from query")
+    for n, t in (("key_cache", key_cache), ("value_cache", value_cache)):
+        if fp8:
+            _cuda_fp8(n, t)
+        elif _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
     for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
                  ("query_start_loc", query_start_loc)):
@@ -333,11 +331,42 @@ def paged_attention_multi_query(out: torch.Tensor, query: torch.Tensor, key_cach
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib, lib.paged_attention_multi_query(
-        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
-        _ptr(context_lens), _ptr(query_start_loc), S, T, int(max_query_len), int(max_context_len), float(scale),
-        B, H, Hkv, D, NB, dt, int(partition_size), _ptr(workspace), wbytes, _stream(query, stream)))
+    head = (_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
+            _ptr(context_lens), _ptr(query_start_loc), S, T, int(max_query_len), int(max_context_len), float(scale),
+            B, H, Hkv, D, NB, dt)
+    tail = (int(partition_size), _ptr(workspace), wbytes, _stream(query, stream))
+    if fp8:
+        _check(lib, lib.paged_attention_multi_query_fp8(*head, float(k_scale), float(v_scale), *tail))
+    else:
+        _check(lib, lib.paged_attention_multi_query(*head, *tail))
     return out
+
+
+def paged_attention_multi_query(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                query_start_loc: torch.Tensor, scale: float, max_query_len: Optional[int] = None,
+                                max_context_len: Optional[int] = None, partition_size: int = 0,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of several query tokens per sequence (query/out [T][H][D], packed by
+    query_start_loc [S+1] int32): sequence s's q_len tokens are its last q_len context positions.
+
+    ``max_query_len`` bounds every q_len on the host; when omitted it is read from
+    query_start_loc, which synchronises the stream.
+    """
+    return _multi_query(out, query, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale,
+                        max_query_len, max_context_len, partition_size, workspace, stream, False, 1.0, 1.0)
+
+
+def paged_attention_multi_query_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                    value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                    context_lens: torch.Tensor, query_start_loc: torch.Tensor, scale: float,
+                                    k_scale: float, v_scale: float, max_query_len: Optional[int] = None,
+                                    max_context_len: Optional[int] = None, partition_size: int = 0,
+                                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_attention_multi_query over an E4M3 pool whose elements are code * k_scale (K) and
+    code * v_scale (V); head_dim 128."""
+    return _multi_query(out, query, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale,
+                        max_query_len, max_context_len, partition_size, workspace, stream, True, k_scale, v_scale)
 
 
 def paged_attention_shared_prefix_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

@@ -996,15 +996,16 @@ size_t paged_attention_multi_query_workspace_size(int32_t num_query_tokens, int3
          mq_order_bytes(num_query_tokens);
 }
 
-pkv_status_t paged_attention_multi_query(void* out, const void* query, const void* key_cache,
-                                         const void* value_cache, const int32_t* block_tables,
-                                         int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                         const int32_t* query_start_loc, int32_t num_seqs, int32_t num_query_tokens,
-                                         int32_t max_query_len, int32_t max_context_len, float scale,
-                                         int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
-                                         int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
-                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
-                                         cudaStream_t stream) {
+namespace {
+// Both multi-query entry points. fp8: the caches hold E4M3 codes of value / k_scale and
+// value / v_scale; only the 8-column tile (head_dim 128) reads them.
+pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const void* value_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_query_tokens,
+                     int32_t max_query_len, int32_t max_context_len, float scale, int32_t block_size,
+                     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                     pkv_dtype_t dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream, bool fp8, float k_scale, float v_scale) {
   g_msg[0] = '\0';
   if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0)
     return fail(PKV_ERR_INVALID_ARG, "num_seqs, num_query_tokens and max_query_len must be >= 0");
@@ -1018,6 +1019,10 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   if (!supported_block_size(block_size))
     return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
   if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (fp8 && !(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+  if (fp8 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "multi-query over an FP8 pool needs head_dim 128 (got %d)", head_dim);
   if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len < 0");
   if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
     return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
@@ -1035,6 +1040,7 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   int tile = g_mq_tile.load(std::memory_order_relaxed);
   if (tile == PKV_MQ_TILE_AUTO)
     tile = (long long)max_query_len * G >= PKV_MQ_WIDE_MIN_ROWS ? PKV_MQ_TILE_TENSOR : PKV_MQ_TILE_COLUMNS;
+  if (fp8) tile = PKV_MQ_TILE_COLUMNS;  // the one tile with an E4M3 contraction
   const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128 : tile == PKV_MQ_TILE_ROWS ? 64 : 8;
   const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
   if (num_seqs > 65535 || (long long)num_kv_heads * row_tiles > 65535)
@@ -1075,8 +1081,8 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.err = err;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.v_scale = 1.f;
+  p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);  // scores in the base-2 domain
+  p.v_scale = fp8 ? v_scale : 1.f;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_heads = num_heads;
   p.num_kv_heads = num_kv_heads;
@@ -1111,14 +1117,19 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
   memset(&kmap, 0, sizeof kmap);
   memset(&vmap, 0, sizeof vmap);
   const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-  const bool tc_map = head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy());
+  const bool tc_map = !fp8 && head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy());
+  const pkv_dtype_t cache_dtype = fp8 ? PKV_FP8_E4M3 : dtype;
   if (tc_map ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
                    !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
-             : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, dtype) ||
-                   !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, dtype))
+             : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
+                   !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
-                       : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);
+  if (fp8)
+    e = dtype == PKV_F16 ? decode_mq_fp8_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                         : decode_mq_fp8_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  else
+    e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
+                         : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);
   if (e != cudaSuccess) return cuda_fail(e, "multi-query kernel launch");
   if (np > 1) {
     e = dtype == PKV_F16 ? launch_reduce<__half>(p, num_seqs, head_dim, stream, mq)
@@ -1126,6 +1137,38 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
   }
   return PKV_OK;
+}
+}  // namespace
+
+pkv_status_t paged_attention_multi_query(void* out, const void* query, const void* key_cache,
+                                         const void* value_cache, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                         const int32_t* query_start_loc, int32_t num_seqs, int32_t num_query_tokens,
+                                         int32_t max_query_len, int32_t max_context_len, float scale,
+                                         int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+  return mq_impl(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                 query_start_loc, num_seqs, num_query_tokens, max_query_len, max_context_len, scale, block_size,
+                 num_heads, num_kv_heads, head_dim, num_blocks, dtype, partition_size, workspace, workspace_bytes,
+                 stream, false, 1.f, 1.f);
+}
+
+pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const void* key_cache,
+                                             const void* value_cache, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                             const int32_t* query_start_loc, int32_t num_seqs,
+                                             int32_t num_query_tokens, int32_t max_query_len,
+                                             int32_t max_context_len, float scale, int32_t block_size,
+                                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                             int32_t num_blocks, pkv_dtype_t dtype, float k_scale, float v_scale,
+                                             int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                             cudaStream_t stream) {
+  return mq_impl(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                 query_start_loc, num_seqs, num_query_tokens, max_query_len, max_context_len, scale, block_size,
+                 num_heads, num_kv_heads, head_dim, num_blocks, dtype, partition_size, workspace, workspace_bytes,
+                 stream, true, k_scale, v_scale);
 }
 
 size_t paged_attention_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,

@@ -2,10 +2,6 @@
 #include "pkv_decode_mma_fp8.cuh"
 #include "pkv_internal.h"
 
-#ifndef PKV_MMA_FP8_RING_BYTES
-#define PKV_MMA_FP8_RING_BYTES (48 * 1024)  // ring bytes per CTA (build-time tuning knob)
-#endif
-
 namespace pkv {
 
 namespace {

@@ -43,6 +43,9 @@
 #ifndef PKV_MMA_FP8_MIN_CTAS
 #define PKV_MMA_FP8_MIN_CTAS 4  // __launch_bounds__ minimum CTAs per SM (build-time tuning knob)
 #endif
+#ifndef PKV_MMA_FP8_RING_BYTES
+#define PKV_MMA_FP8_RING_BYTES (48 * 1024)  // ring bytes per CTA (build-time tuning knob)
+#endif
 
 namespace pkv {
 
@@ -80,10 +83,17 @@ struct MmaTileE4M3 {
   // >= G are zero.
   static __device__ __forceinline__ void load_qb(QB& qb, const T* q, int G, int lane, float sl2, float& sa,
                                                  float& sb) {
-    const int g = lane >> 2, qd = lane & 3;
-    uint32_t w[16];  // q[g][32qd .. 32qd + 31] as 16-bit pairs
-    if (g < G) {
-      const uint4* src = reinterpret_cast<const uint4*>(q + g * D + 32 * qd);
+    load_qb_row(qb, (lane >> 2) < G ? q + (lane >> 2) * D : nullptr, lane, sl2, sa, sb);
+  }
+
+  // The same operand with column n = lane / 4 taken from the query row `qr`
+  // (nullptr: a zero column), each column with its own 2^-k.
+  static __device__ __forceinline__ void load_qb_row(QB& qb, const T* qr, int lane, float sl2, float& sa,
+                                                     float& sb) {
+    const int qd = lane & 3;
+    uint32_t w[16];  // qr[32qd .. 32qd + 31] as 16-bit pairs
+    if (qr) {
+      const uint4* src = reinterpret_cast<const uint4*>(qr + 32 * qd);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint4 v = src[u];
@@ -96,7 +106,7 @@ struct MmaTileE4M3 {
 #pragma unroll
       for (int e = 0; e < 16; ++e) w[e] = 0u;
     }
-    float inv = 1.f;  // 2^-k of head g
+    float inv = 1.f;  // 2^-k of column lane / 4
     if constexpr (!std::is_same<T, __half>::value) {
       float amax = 0.f;
 #pragma unroll
@@ -130,11 +140,16 @@ struct MmaTileE4M3 {
 
   // Fold one (block, kv head) tile into the lane's running state for its two
   // heads (columns 2 (lane % 4) and + 1): tokens 0 .. nvalid-1 take part. acc is
-  // in V's code units. Zeroes the value rows past nvalid in shared memory (the
-  // stage then needs a proxy fence before the copy engine refills it).
+  // in V's code units. CAUSAL: besides, the first column sees only tokens whose
+  // position tok_base + t is below lim0 (the second: lim1), so a column may see
+  // no token of a tile, or of all tiles so far (its m then stays -inf). Zeroes
+  // the value rows past nvalid in shared memory (the stage then needs a proxy
+  // fence before the copy engine refills it).
+  template <bool CAUSAL = false>
   static __device__ __forceinline__ void run(unsigned char* Ks, unsigned char* Vs, int nvalid, const QB& qb,
                                              int lane, float sla, float slb, float& m0, float& m1, float& l0,
-                                             float& l1, float (&acc)[KT][4]) {
+                                             float& l1, float (&acc)[KT][4], int tok_base = 0, int lim0 = 0,
+                                             int lim1 = 0) {
     const int g = lane >> 2, qd = lane & 3;
     if (nvalid < BS) {
       // value rows past the context may hold anything (NaN codes too): zero them
@@ -171,10 +186,17 @@ struct MmaTileE4M3 {
         for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
         const bool va = ta < nvalid;
         const bool vb = BS >= 16 && ta + 8 < nvalid;
-        const float x00 = va ? sacc[0] * sla : -INFINITY;
-        const float x01 = va ? sacc[1] * slb : -INFINITY;
-        const float x10 = vb ? sacc[2] * sla : -INFINITY;
-        const float x11 = vb ? sacc[3] * slb : -INFINITY;
+        bool va0 = va, va1 = va, vb0 = vb, vb1 = vb;
+        if constexpr (CAUSAL) {
+          va0 = va && tok_base + ta < lim0;
+          va1 = va && tok_base + ta < lim1;
+          vb0 = vb && tok_base + ta + 8 < lim0;
+          vb1 = vb && tok_base + ta + 8 < lim1;
+        }
+        const float x00 = va0 ? sacc[0] * sla : -INFINITY;
+        const float x01 = va1 ? sacc[1] * slb : -INFINITY;
+        const float x10 = vb0 ? sacc[2] * sla : -INFINITY;
+        const float x11 = vb1 ? sacc[3] * slb : -INFINITY;
         float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -186,7 +208,11 @@ struct MmaTileE4M3 {
         const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
         if (__any_sync(kFull, up0 || up1)) {
           const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
-          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+          float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+          if constexpr (CAUSAL) {  // a column that keeps its m may still hold -inf there
+            if (!up0) al0 = 1.f;
+            if (!up1) al1 = 1.f;
+          }
           l0 *= al0;
           l1 *= al1;
 #pragma unroll
@@ -199,8 +225,13 @@ struct MmaTileE4M3 {
           m0 = mn0;
           m1 = mn1;
         }
-        const uint32_t pa = Elem<__half>::pack2(fast_exp2(x00 - m0), fast_exp2(x01 - m1));
-        const uint32_t pb = Elem<__half>::pack2(fast_exp2(x10 - m0), fast_exp2(x11 - m1));
+        float r0 = m0, r1 = m1;  // exponentials against the reference
+        if constexpr (CAUSAL) {  // a column that has seen nothing yet: against 0 (its x are all -inf)
+          if (r0 == -INFINITY) r0 = 0.f;
+          if (r1 == -INFINITY) r1 = 0.f;
+        }
+        const uint32_t pa = Elem<__half>::pack2(fast_exp2(x00 - r0), fast_exp2(x01 - r1));
+        const uint32_t pb = Elem<__half>::pack2(fast_exp2(x10 - r0), fast_exp2(x11 - r1));
         const float2 fa = Elem<__half>::to_float2(pa), fb = Elem<__half>::to_float2(pb);
         // l: this lane's rows only; finish() adds the lanes of a column
         l0 += fa.x + fb.x;

@@ -165,8 +165,11 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
   const int lim0 = j0 < ncol ? mq_limit(mq, ctx, q_len, row0 + j0, G) : 0;
   const int lim1 = j0 + 1 < ncol ? mq_limit(mq, ctx, q_len, row0 + j0 + 1, G) : 0;
   typename Tile::QB qb;
-  Tile::load_qb_row(qb, qrow, lane);
-  const float sl2 = p.scale_log2;
+  float sla = p.scale_log2, slb = p.scale_log2;  // score multipliers of this lane's two columns
+  if constexpr (Tile::FP8)
+    Tile::load_qb_row(qb, qrow, lane, p.scale_log2, sla, slb);  // per-column f16 scaling of a bf16 query
+  else
+    Tile::load_qb_row(qb, qrow, lane);
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float acc[Tile::KT][4];
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
       const int lb = warp + NW * i;
       const int base = (blk0 + lb) * BS;
       const int nvalid = min(BS, tok1 - base);
-      Tile::template run<true>(Ks, Ks + Sh::TILE, nvalid, qb, lane, sl2, sl2, m0, m1, l0, l1, acc, base, lim0,
+      Tile::template run<true>(Ks, Ks + Sh::TILE, nvalid, qb, lane, sla, slb, m0, m1, l0, l1, acc, base, lim0,
                                lim1);
       if (nvalid < BS) zeroed |= 1u << k;
     }
@@ -236,6 +239,7 @@ __global__ void __launch_bounds__(NW * 32, Tile::MIN_CTAS)
       o += rw[n * D + d] * f;
     }
     o = L > 0.f ? o / L : 0.f;
+    if constexpr (Tile::FP8) o *= p.v_scale * Tile::UNIT;  // V codes -> values
     const int r = row0 + n;
     const size_t row = (size_t)(q0 + r / G) * p.num_heads + kvh * G + r % G;  // output row (query token, head)
     if (direct) {

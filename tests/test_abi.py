@@ -36,6 +36,7 @@ def test_header_declares_the_boundary():
               "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
               "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
               "paged_attention_multi_query", "paged_attention_multi_query_workspace_size",
+              "paged_attention_multi_query_fp8",
               "pkv_set_multi_query_tile"):
         assert n in names
 
@@ -274,6 +275,36 @@ def test_multi_query_nothing_to_do_is_a_noop(lib):
     assert multi_query(lib, num_seqs=0, out=None) == OK
     assert multi_query(lib, num_query_tokens=0, out=None) == OK
     assert multi_query(lib, max_query_len=0, out=None) == OK
+
+
+def multi_query_fp8(lib, **kw):
+    a = dict(out=fake(1), query=fake(2), key_cache=fake(3), value_cache=fake(4), block_tables=fake(5),
+             max_blocks_per_seq=8, context_lens=fake(6), query_start_loc=fake(7), num_seqs=2, num_query_tokens=5,
+             max_query_len=4, max_context_len=128, scale=0.125, block_size=16, num_heads=8, num_kv_heads=2,
+             head_dim=128, num_blocks=16, dtype=0, k_scale=0.5, v_scale=0.25, partition_size=0, workspace=None,
+             workspace_bytes=0, stream=None)
+    a.update(kw)
+    return lib.paged_attention_multi_query_fp8(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), UNSUPPORTED),                  # the E4M3 tile is head_dim 128
+    (dict(k_scale=0.0), INVALID),
+    (dict(v_scale=-1.0), INVALID),
+    (dict(k_scale=float("inf")), INVALID),
+    (dict(dtype=2), INVALID),                          # the query dtype: f16 or bf16
+    (dict(query_start_loc=None), INVALID),
+    (dict(max_query_len=129), INVALID),
+    (dict(max_blocks_per_seq=200, max_context_len=3000), WORKSPACE),
+])
+def test_multi_query_fp8_rejects_on_host(lib, kw, status):
+    assert multi_query_fp8(lib, **kw) == status
+    assert lib.pkv_last_error_message() != b""
+
+
+def test_multi_query_fp8_nothing_to_do_is_a_noop(lib):
+    assert multi_query_fp8(lib, num_seqs=0, out=None) == OK
+    assert multi_query_fp8(lib, num_query_tokens=0, out=None) == OK
 
 
 def test_multi_query_tile_switch(lib):
