@@ -197,3 +197,55 @@ def test_sequence_order_changes_nothing(mq_tile):
     assert np.array_equal(outs[0], outs[1])
     check_close(outs[0], reference(batch), F16, f"{mq_tile}, sequence order")
     assert binding.device_errors() == 0
+
+
+def test_many_short_sequences(mq_tile):
+    """2500 sequences (the length sort loops over more sequences than it has threads), contexts of 1 to 40
+    tokens, up to 4 query tokens each, GQA 8: up to 32 rows per kv head."""
+    rng = np.random.default_rng(97)
+    S = 2500
+    ctx = rng.integers(1, 41, size=S)
+    ql = np.minimum(rng.integers(1, 5, size=S), ctx)
+    batch = W.build_batch(seed=98, context_lens=ctx, num_heads=16, num_kv_heads=2, head_dim=64, block_size=16,
+                          dtype=BF16, pool_factor=1.1, query_lens=ql)
+    t = W.as_torch(batch, DEV)
+    out = run_mq(batch, t)
+    torch.cuda.synchronize()
+    check_close(as_bits(out), reference(batch), BF16, f"{mq_tile}, {S} sequences")
+    assert binding.device_errors() == 0
+
+
+def test_graph_capture_and_replay(mq_tile):
+    """The call is stream-ordered (length sort, tile, reduce): a CUDA graph captured around it replays
+    correctly, contexts long enough to be split into partitions."""
+    rng = np.random.default_rng(99)
+    ctx = rng.integers(100, 2600, size=12)
+    ql = np.minimum(rng.integers(1, 24, size=12), ctx)
+    batch = W.build_batch(seed=100, context_lens=ctx, num_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
+                          dtype=F16, pool_factor=1.2, query_lens=ql)
+    t = W.as_torch(batch, DEV)
+    T, H, Hkv, D = int(batch.query_start_loc[-1]), batch.num_heads, batch.num_kv_heads, batch.head_dim
+    ws = torch.empty(binding.paged_attention_multi_query_workspace_size(T, H, Hkv, D, 16, batch.max_context_len),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.zeros_like(t["query"])
+    mql = int(ql.max())
+
+    def call():
+        binding.paged_attention_multi_query(out, t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
+                                            t["context_lens"], t["query_start_loc"], batch.scale, max_query_len=mql,
+                                            max_context_len=batch.max_context_len, workspace=ws)
+
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(side):
+        call()  # warm up outside the capture
+    torch.cuda.current_stream(DEV).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    check_close(as_bits(out), reference(batch), F16, f"{mq_tile}, graph replay")
+    assert binding.device_errors() == 0
