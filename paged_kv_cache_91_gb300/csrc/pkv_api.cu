@@ -163,53 +163,26 @@ __global__ void pkv_write_fp8_kernel(const uint4* __restrict__ key, const uint4*
 // ---------------------------------------------------------------------------
 // split-K reduce: merge the partitions' (m_p, l_p, o_p) of one (seq, head) by
 // log-sum-exp: out = sum_p w_p o_p / sum_p w_p with w_p = l_p 2^(m_p - max m).
-// One warp per output row, kReduceRows rows per CTA; lane p holds the weight
-// of partition p (p < 32 per round) and each lane merges D/32 dims. An output
-// row is (seq, head) in decode, and (query token, head) in the multi-query
-// case (qsl != nullptr), whose query token's sequence is found by binary
-// search in query_start_loc.
+// One warp per output row; lane p holds the weight of partition p (p < 32 per
+// round) and each lane merges D/32 dims.
 
 constexpr int kReduceRows = 4;
 constexpr int kReduceEarly = 4;  // partitions whose partial outputs are fetched with the first loads
 
-template <typename T, int D>
-__global__ void __launch_bounds__(32 * kReduceRows)
-    pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o, const float* __restrict__ part_m,
-                      const float* __restrict__ part_l, const int32_t* __restrict__ context_lens, int num_seqs,
-                      int num_heads, int partition_size, int max_partitions, int ctx_limit, const MqParams mq) {
-  pdl_begin();
-  constexpr int DPL = D / 32;  // dims per lane: 4 (float4) or 2 (float2)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;  // (seq or query token) * num_heads + h
-  const size_t nrows = (size_t)(mq.query_start_loc ? mq.num_query_tokens : num_seqs) * num_heads;
-  if (row >= nrows) return;
-  int s = (int)(row / num_heads);
-  if (mq.query_start_loc) {
-    // the sequence whose query rows contain this one (the last s with query_start_loc[s] <= qrow)
-    const int qrow = s;
-    int lo = 0, hi = num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (mq.query_start_loc[mid] <= qrow) lo = mid; else hi = mid - 1;
-    }
-    s = lo;
-    const int c = context_lens[s];
-    int q0 = 0;
-    const int n = mq_query_len(mq, s, c < 0 ? 0 : (c > ctx_limit ? ctx_limit : c), q0);
-    if (n < 0 || qrow < q0 || qrow >= q0 + n) return;  // reported by the attention kernel; row not written
-  }
-  const size_t base = row * max_partitions;
-  // One round of loads: the context length, this lane's partition (m, l), and the
-  // partial outputs of the first partitions. All are in bounds whatever the
-  // context length turns out to be; entries past the sequence's partitions are
-  // masked below.
-  const int ctx_raw = context_lens[s];
-  float mp = -INFINITY, lp = 0.f;
+// The first round of loads for output row `row` (partials at base = row * max_partitions):
+// this lane's partition (m, l) and the partial outputs of the first kReduceEarly partitions.
+// All are in bounds whatever the row's partition count; entries past it are masked later.
+template <int D>
+__device__ __forceinline__ void reduce_load_row(const float* __restrict__ part_o, const float* __restrict__ part_m,
+                                                const float* __restrict__ part_l, size_t base, int max_partitions,
+                                                int lane, float& mp, float& lp, float (&o_early)[kReduceEarly][D / 32]) {
+  constexpr int DPL = D / 32;
+  mp = -INFINITY;
+  lp = 0.f;
   if (lane < max_partitions) {
     mp = part_m[base + lane];
     lp = part_l[base + lane];
   }
-  float o_early[kReduceEarly][DPL];
 #pragma unroll
   for (int k = 0; k < kReduceEarly; ++k) {
     if (k < max_partitions) {
@@ -226,9 +199,16 @@ __global__ void __launch_bounds__(32 * kReduceRows)
       for (int e = 0; e < DPL; ++e) o_early[k][e] = 0.f;
     }
   }
-  const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > ctx_limit ? ctx_limit : ctx_raw);
-  const int np = (ctx + partition_size - 1) / partition_size;
-  if (np <= 1) return;  // the decode kernel wrote this row directly
+}
+
+// Merge the np (> 1) partials of output row `row` into out[row][:], given the first round of loads.
+template <typename T, int D>
+__device__ __forceinline__ void reduce_combine_row(T* __restrict__ out, const float* __restrict__ part_o,
+                                                   const float* __restrict__ part_m,
+                                                   const float* __restrict__ part_l, size_t base, size_t row,
+                                                   int np, float mp, float lp,
+                                                   const float (&o_early)[kReduceEarly][D / 32], int lane) {
+  constexpr int DPL = D / 32;
   if (lane >= np) mp = -INFINITY;
   // global max over all partitions (np may exceed 32)
   float M = mp;
@@ -286,6 +266,59 @@ __global__ void __launch_bounds__(32 * kReduceRows)
     *reinterpret_cast<uint2*>(dst) = v;
   } else {
     *reinterpret_cast<uint32_t*>(dst) = Elem<T>::pack2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// Decode: output row (seq, head), kReduceRows rows per CTA. One round of loads
+// (the context length, and the row's first partials) precedes the partition
+// count, which hides one memory round trip.
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceRows)
+    pkv_reduce_kernel(T* __restrict__ out, const float* __restrict__ part_o, const float* __restrict__ part_m,
+                      const float* __restrict__ part_l, const int32_t* __restrict__ context_lens, int num_seqs,
+                      int num_heads, int partition_size, int max_partitions, int ctx_limit) {
+  pdl_begin();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * kReduceRows + warp;  // seq * num_heads + h
+  if (row >= (size_t)num_seqs * num_heads) return;
+  const int s = (int)(row / num_heads);
+  const size_t base = row * max_partitions;
+  const int ctx_raw = context_lens[s];
+  float mp, lp;
+  float o_early[kReduceEarly][D / 32];
+  reduce_load_row<D>(part_o, part_m, part_l, base, max_partitions, lane, mp, lp, o_early);
+  const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > ctx_limit ? ctx_limit : ctx_raw);
+  const int np = (ctx + partition_size - 1) / partition_size;
+  if (np <= 1) return;  // the decode kernel wrote this row directly
+  reduce_combine_row<T, D>(out, part_o, part_m, part_l, base, row, np, mp, lp, o_early, lane);
+}
+
+// Multi-query: one CTA per (sequence, head). It reads the context length first and leaves at once
+// when the context fits one partition (the attention kernel then wrote the rows directly); else
+// its warps take the sequence's query rows (query token q0 + i, this head) in turn. No row has to
+// search query_start_loc for its sequence.
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceRows)
+    pkv_reduce_mq_kernel(T* __restrict__ out, const float* __restrict__ part_o, const float* __restrict__ part_m,
+                         const float* __restrict__ part_l, const int32_t* __restrict__ context_lens, int num_heads,
+                         int partition_size, int max_partitions, int ctx_limit, const MqParams mq) {
+  pdl_begin();
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = context_lens[s];
+  const int ctx = c < 0 ? 0 : (c > ctx_limit ? ctx_limit : c);
+  const int np = (ctx + partition_size - 1) / partition_size;
+  if (np <= 1) return;
+  int q0 = 0;
+  const int n = mq_query_len(mq, s, ctx, q0);
+  if (n <= 0) return;  // n < 0: reported by the attention kernel, the rows are not written
+  for (int i = warp; i < n; i += kReduceRows) {
+    const size_t row = (size_t)(q0 + i) * num_heads + h;
+    const size_t base = row * max_partitions;
+    float mp, lp;
+    float o_early[kReduceEarly][D / 32];
+    reduce_load_row<D>(part_o, part_m, part_l, base, max_partitions, lane, mp, lp, o_early);
+    reduce_combine_row<T, D>(out, part_o, part_m, part_l, base, row, np, mp, lp, o_early, lane);
   }
 }
 
@@ -360,16 +393,23 @@ __global__ void __launch_bounds__(32 * kReduceRows)
 template <typename T>
 cudaError_t launch_reduce(const DecodeParams& p, int num_seqs, int head_dim, cudaStream_t stream,
                           const MqParams& mq = MqParams{}) {
-  const size_t rows = (size_t)(mq.query_start_loc ? mq.num_query_tokens : num_seqs) * p.num_heads;
-  const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
   T* out = static_cast<T*>(p.out);
   const float *po = p.part_o, *pm = p.part_m, *pl = p.part_l;
+  if (mq.query_start_loc) {  // multi-query: a CTA per (sequence, head)
+    const dim3 grid((unsigned)num_seqs, (unsigned)p.num_heads);
+    if (head_dim == 128)
+      return launch_kernel(pkv_reduce_mq_kernel<T, 128>, grid, dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
+                           p.context_lens, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit, mq);
+    return launch_kernel(pkv_reduce_mq_kernel<T, 64>, grid, dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
+                         p.context_lens, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit, mq);
+  }
+  const size_t rows = (size_t)num_seqs * p.num_heads;
+  const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
   if (head_dim == 128)
     return launch_kernel(pkv_reduce_kernel<T, 128>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
-                         p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit,
-                         mq);
+                         p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
   return launch_kernel(pkv_reduce_kernel<T, 64>, dim3(grid), dim3(32 * kReduceRows), 0, stream, out, po, pm, pl,
-                       p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit, mq);
+                       p.context_lens, num_seqs, p.num_heads, p.partition_size, p.max_partitions, p.ctx_limit);
 }
 
 // ---------------------------------------------------------------------------
@@ -1043,8 +1083,9 @@ pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const 
   if (fp8) tile = PKV_MQ_TILE_COLUMNS;  // the one tile with an E4M3 contraction
   const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128 : tile == PKV_MQ_TILE_ROWS ? 64 : 8;
   const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
-  if (num_seqs > 65535 || (long long)num_kv_heads * row_tiles > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_kv_heads * ceil(max_query_len * group / %d) must be <= 65535",
+  if (num_seqs > 65535 || num_heads > 65535 || (long long)num_kv_heads * row_tiles > 65535)
+    return fail(PKV_ERR_UNSUPPORTED,
+                "num_seqs, num_heads and num_kv_heads * ceil(max_query_len * group / %d) must be <= 65535",
                 rows_per_tile);
   if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
     return fail(PKV_ERR_UNSUPPORTED, "pool rows num_blocks * num_kv_heads * block_size must be < 2^31");
