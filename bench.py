@@ -178,7 +178,7 @@ KERNEL_SOURCES = {
     "mq": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mq.cuh", "pkv_mq_wide.cuh", "pkv_mq_tc.cuh",
            "pkv_tcgen05.cuh", "pkv_decode_mq.cu"),
     "mq_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mq.cuh",
-               "pkv_decode_mq_fp8.cu"),
+               "pkv_mq_tc.cuh", "pkv_tcgen05.cuh", "pkv_decode_mq_fp8.cu"),
 }
 
 
@@ -373,9 +373,9 @@ def mq_summary(batch, tile_arg, call_ms, fp8=False):
     vis = (ql * (ctx - ql) + ql * (ql + 1) // 2).sum()  # positions seen, summed over query tokens
     flops = 4.0 * batch.head_dim * batch.num_heads * float(vis)
     rows_per_kv_head = int(ql.max()) * (batch.num_heads // batch.num_kv_heads)
-    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head > 16 else "columns")
-    if fp8:
-        tile = "columns"  # the one tile with an E4M3 contraction
+    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head > (32 if fp8 else 16) else "columns")
+    if fp8 and tile == "rows":
+        tile = "columns"  # no FP8 form of the 64-row tile
     return {"tile": tile, "rows_per_kv_head": rows_per_kv_head, "attention_gflop_per_call": round(flops / 1e9, 2),
             "attention_tflops": round(flops / (call_ms * 1e-3) / 1e12, 1)}
 

@@ -378,10 +378,13 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
  *   k_scale, v_scale  finite and > 0
  * head_dim must be 128 (PKV_ERR_UNSUPPORTED otherwise). Every other argument,
  * the workspace (paged_attention_multi_query_workspace_size) and the results'
- * meaning are those of paged_attention_multi_query. Every row count runs on
- * the 8-column tile (pkv_set_multi_query_tile does not apply): the tensor
- * tiles multiply 16-bit operands only, so rows past 8 per kv head cost one
- * more pass over the context per 8 rows.
+ * meaning are those of paged_attention_multi_query. Tiles: the 8-column tile
+ * multiplies the codes widened in registers (f16 MMAs); the tensor-memory tile
+ * widens each K/V tile's codes to f16 in shared memory, and a bf16 query is
+ * scaled per row by a power of two into f16, so that both MMAs multiply f16.
+ * PKV_MQ_TILE_AUTO takes the tensor-memory tile above 32 rows per kv head (the
+ * 8-column tile is relatively faster over an FP8 pool); PKV_MQ_TILE_ROWS runs
+ * the 8-column tile.
  */
 pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const void* key_cache,
                                              const void* value_cache, const int32_t* block_tables,

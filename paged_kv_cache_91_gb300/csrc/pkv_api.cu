@@ -26,6 +26,11 @@ constexpr int kDefaultPartition = 512;
 // wins, by 1.5x at 32 rows.
 #define PKV_MQ_WIDE_MIN_ROWS 17
 #endif
+#ifndef PKV_MQ_WIDE_MIN_ROWS_FP8
+// The same over an FP8 pool, where the 8-column tile is relatively faster: 24 rows 0.266 against
+// 0.362 ms, 32 rows even, 48 rows 0.509 against 0.371 ms (workload 3).
+#define PKV_MQ_WIDE_MIN_ROWS_FP8 33
+#endif
 // An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
 // weigh twice as much per byte: longer partitions measure faster.
 constexpr int kDefaultPartitionFp8 = 1024;
@@ -538,6 +543,21 @@ bool make_pool_map(CUtensorMap* map, const void* base, long long rows, int head_
   const CUresult r = enc(map, type,
                          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// An FP8 pool as the tensor-memory multi-query tile reads it: each (block, kv head) tile lands as
+// block_size rows of 128 codes, unswizzled (the tile widens them to f16 in shared memory).
+bool make_pool_map_fp8_rows(CUtensorMap* map, const void* base, long long rows, int block_size) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)block_size};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1079,8 +1099,10 @@ pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const 
   // to the 8-column tile, which reads no padding rows.
   int tile = g_mq_tile.load(std::memory_order_relaxed);
   if (tile == PKV_MQ_TILE_AUTO)
-    tile = (long long)max_query_len * G >= PKV_MQ_WIDE_MIN_ROWS ? PKV_MQ_TILE_TENSOR : PKV_MQ_TILE_COLUMNS;
-  if (fp8) tile = PKV_MQ_TILE_COLUMNS;  // the one tile with an E4M3 contraction
+    tile = (long long)max_query_len * G >= (fp8 ? PKV_MQ_WIDE_MIN_ROWS_FP8 : PKV_MQ_WIDE_MIN_ROWS)
+               ? PKV_MQ_TILE_TENSOR
+               : PKV_MQ_TILE_COLUMNS;
+  if (fp8 && tile != PKV_MQ_TILE_TENSOR) tile = PKV_MQ_TILE_COLUMNS;  // no FP8 form of the 64-row tile
   const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128 : tile == PKV_MQ_TILE_ROWS ? 64 : 8;
   const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
   if (num_seqs > 65535 || num_heads > 65535 || (long long)num_kv_heads * row_tiles > 65535)
@@ -1159,15 +1181,18 @@ pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const 
   memset(&vmap, 0, sizeof vmap);
   const long long rows = (long long)num_blocks * num_kv_heads * block_size;
   const bool tc_map = !fp8 && head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy());
+  const bool fp8_rows = fp8 && tile == PKV_MQ_TILE_TENSOR;
   const pkv_dtype_t cache_dtype = fp8 ? PKV_FP8_E4M3 : dtype;
-  if (tc_map ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
-                   !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
-             : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
-                   !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
+  if (fp8_rows ? !make_pool_map_fp8_rows(&kmap, key_cache, rows, block_size) ||
+                     !make_pool_map_fp8_rows(&vmap, value_cache, rows, block_size)
+      : tc_map ? !make_pool_map_tc(&kmap, key_cache, rows, block_size, dtype) ||
+                     !make_pool_map_tc(&vmap, value_cache, rows, block_size, dtype)
+               : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
+                     !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
   if (fp8)
-    e = dtype == PKV_F16 ? decode_mq_fp8_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream)
-                         : decode_mq_fp8_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+    e = dtype == PKV_F16 ? decode_mq_fp8_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
+                         : decode_mq_fp8_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);
   else
     e = dtype == PKV_F16 ? decode_mq_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
                          : decode_mq_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);

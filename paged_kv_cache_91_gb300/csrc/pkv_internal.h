@@ -45,12 +45,13 @@ cudaError_t decode_mq_f16(const DecodeParams& p, const MqParams& mq, const CUten
 cudaError_t decode_mq_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                            cudaStream_t stream);
-// Multi-query attention over an FP8 (E4M3) pool: the 8-column tile, head_dim 128.
+// Multi-query attention over an FP8 (E4M3) pool, head_dim 128: tile PKV_MQ_TILE_TENSOR (the pool
+// through make_pool_map_fp8_rows) or the 8-column tile (make_pool_map).
 cudaError_t decode_mq_fp8_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs,
+                              const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                               cudaStream_t stream);
 cudaError_t decode_mq_fp8_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
-                               const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs,
+                               const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                                cudaStream_t stream);
 
 // Persistent equal-work decode (pkv_decode_stream.cuh): CTAs per SM, launch, reduce.

@@ -35,6 +35,7 @@
 
 #include <type_traits>
 
+#include "pkv_decode_mma_fp8.cuh"
 #include "pkv_decode_mq.cuh"
 #include "pkv_tcgen05.cuh"
 
@@ -61,8 +62,10 @@ struct MqTcShape {
   static constexpr int OFF_V = OFF_K + KST * TILE;
   static constexpr int OFF_BARS = OFF_V + VST * TILE;
   // k_full[3], k_empty[3], v_full[2], pv_done[2] (PV_j done: V slot and S/P buffer j % 2 free),
-  // s_full[2], p_full[2] (per S/P buffer: no row can reach tile j + 2 before PV_j), fin, q_full
-  static constexpr int NBARS = 16;
+  // s_full[2], p_full[2] (per S/P buffer: no row can reach tile j + 2 before PV_j), fin, q_full,
+  // and for an FP8 pool k_raw[3], v_raw[2] (the codes have landed; k_full / v_full then mean widened)
+  static constexpr int NBARS = 21;
+  static constexpr int HALF = TILE / 2;           // FP8 pool: the codes of a tile land in its slot's upper half
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;  // tensor-memory base, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 8;
   // The operands need 1024-byte aligned atoms; the dynamic shared memory of a
@@ -140,13 +143,94 @@ __device__ __noinline__ void mq_tc_fetch_q(unsigned char* Qs, int row, const T* 
   }
 }
 
-template <typename T, int D, int BS>
+// FP8 pool: widen the E4M3 codes of one 64-token tile, landed as 64 rows of 128 codes at src (the
+// upper half of the slot), into the slot's f16 operand layout at dst (8-token atoms of two
+// 128-byte-swizzled 1 KB halves, columns 0..63 then 64..127), in place. Lane (t = lane / 4, quarter
+// q = lane % 4) takes codes 32q .. 32q + 31 of token 8a + t of every atom a. The whole tile is read
+// into registers before anything is written (the output overwrites the codes).
+__device__ __forceinline__ void mq_tc_widen_tile(unsigned char* dst, const unsigned char* src, int lane) {
+  const int t8 = lane >> 2, q = lane & 3;
+  uint4 c[8][2];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    const int t = 8 * a + t8;
+    c[a][0] = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q);
+    c[a][1] = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q + 16);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    const uint32_t w[8] = {c[a][0].x, c[a][0].y, c[a][0].z, c[a][0].w, c[a][1].x, c[a][1].y, c[a][1].z, c[a][1].w};
+    unsigned char* row = dst + a * 2048 + (q >> 1) * 1024 + t8 * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t h[4];
+      e4m3x4_to_f16x2(w[2 * k], h[0], h[1]);
+      e4m3x4_to_f16x2(w[2 * k + 1], h[2], h[3]);
+      const int cc = (q & 1) * 4 + k;
+      *reinterpret_cast<uint4*>(row + ((cc ^ t8) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  }
+}
+
+// FP8 pool with a bf16 query: thread `row` stores its query row (as in mq_tc_fetch_q) in f16,
+// multiplied by 2^k so that its largest magnitude lies in [2^14, 2^15) (every bf16 value keeps its
+// 8 significant bits unless it lies below 2^-14 of that range, where its contribution is far below
+// the fp32 accumulation error); returns 2^-k, which the row's score multiplier takes back. Zeros
+// and 1 past q_len * G.
+template <int D, int ROWS>
+__device__ __noinline__ float mq_tc_fetch_q_bf16_as_f16(unsigned char* Qs, int row, const __nv_bfloat16* query,
+                                                         int q0, int kvh, int rt, int q_len, int G, int num_heads) {
+  const int r = rt * ROWS + row;
+  const uint32_t rx = row & 7;
+  if (r >= q_len * G) {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      *reinterpret_cast<uint4*>(Qs + row * 128 + (c / 8) * (ROWS * 128) + (((c % 8) ^ rx) << 4)) = make_uint4(0, 0, 0, 0);
+    return 1.f;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(query + ((size_t)(q0 + r / G) * num_heads + kvh * G + r % G) * D);
+  // two passes over the row (the second reads it from cache): its largest magnitude, then the stores
+  float amax = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 v = src[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = Elem<__nv_bfloat16>::to_float2(w[e]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127;  // floor(log2(amax))
+  int k = amax > 0.f ? 14 - ex : 0;
+  k = k < -60 ? -60 : (k > 60 ? 60 : k);
+  const float pw = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 v = src[c];
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = Elem<__nv_bfloat16>::to_float2(w[e]);
+      w[e] = Elem<__half>::pack2(f.x * pw, f.y * pw);
+    }
+    *reinterpret_cast<uint4*>(Qs + row * 128 + (c / 8) * (ROWS * 128) + (((c % 8) ^ rx) << 4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+}
+
+template <typename T, int D, int BS, bool F8 = false>
 // Two CTAs per SM: 6 warps x 168 registers (3 warps per SM quarter), or 7 x 128 (4 per quarter).
 __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     pkv_mq_tc_kernel(const DecodeParams p, const MqParams mq, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
   using Sh = MqTcShape<T, D, BS>;
+  // FP8 pool: both MMAs multiply f16 (the codes widen exactly; a bf16 query is scaled into f16)
+  using TP = typename std::conditional<F8, __half, T>::type;  // the type of P (and, with F8, of Q, K and V)
+  static_assert(!F8 || (D == 128 && Sh::CW == 2), "an FP8 pool: head_dim 128, one copy warp each for K and V");
   constexpr int NT = Sh::NT, NBT = Sh::NBT, DH = Sh::DH;
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int KST = Sh::KST;
@@ -158,6 +242,8 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   uint64_t* p_full = k_full + 12;
   uint64_t* fin = k_full + 14;
   uint64_t* q_full = k_full + 15;
+  uint64_t* k_raw = k_full + 16;  // FP8 pool only
+  uint64_t* v_raw = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned char* Qs = smem;
@@ -233,6 +319,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     for (int k = 0; k < 12; ++k) mbar_init(k_full + k, 1);
+    for (int k = 16; k < 21; ++k) mbar_init(k_full + k, 1);
     mbar_init(p_full, 128);
     mbar_init(p_full + 1, 128);
     mbar_init(fin, 1);
@@ -265,6 +352,70 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
         }
       }
     }
+    if constexpr (F8) {
+      // FP8 pool: this warp's tiles (K: 3 slots, freed by S; V: 2 slots, freed by PV). Either widen
+      // the oldest tile whose codes have landed, or copy the next tile's codes into its slot's upper
+      // half once the slot is free, whichever is ready first.
+      const int NS = do_k ? KST : 2;
+      uint64_t* landed = do_k ? k_raw : v_raw;
+      uint64_t* widened = do_k ? k_full : v_full;
+      uint64_t* freed = do_k ? k_empty : pv_done;
+      auto slot = [&](int j) { return do_k ? k_slot(j) : v_slot(j); };
+      int ni = 0, nc = 0;  // tiles issued, tiles widened
+      long long t_last = clock64();
+      while (nc < ntile) {
+        int act = -1;  // 0: widen tile nc, 1: copy tile ni
+        if (lane == 0) {
+          if (nc < ni && mbar_test_wait(landed + nc % NS, (nc / NS) & 1))
+            act = 0;
+          else if (ni < ntile && (ni < NS || mbar_test_wait(freed + ni % NS, ((ni / NS) - 1) & 1)))
+            act = 1;
+          else if (*abort || clock64() - t_last > kWaitLimitCycles)
+            act = 2;
+        }
+        act = __shfl_sync(kFull, act, 0);
+        if (act == 2) {
+          if (lane == 0) *abort = 1;
+          break;
+        }
+        if (act < 0) {
+          __nanosleep(64);
+          continue;
+        }
+        if (act == 0) {
+          mq_tc_widen_tile(slot(nc), slot(nc) + Sh::HALF, lane);
+          fence_proxy_async_smem();  // generic stores, read by the MMAs
+          __syncwarp();
+          if (lane == 0) mbar_arrive(widened + nc % NS);
+          ++nc;
+        } else {
+          const int j = ni;
+          int phys = -1;  // lane i < NBT: block j * NBT + i of the partition
+#pragma unroll
+          for (int u = 0; u < Sh::IDS; ++u) {
+            const int b = j * NBT + (lane & (NBT - 1));
+            const int x = __shfl_sync(kFull, ids[u], b & 31);
+            if ((b >> 5) == u) phys = x;
+          }
+          if (lane >= NBT || j * NBT + lane >= nblk) phys = -1;
+          const unsigned mask = __ballot_sync(kFull, phys >= 0);
+          uint64_t* bar = landed + j % NS;
+          if (lane == 0) {
+            fence_proxy_async_smem();  // the widening (and the rows' zeros) wrote this slot: before the copies
+            mbar_arrive_expect_tx(bar, __popc(mask) * BS * 128);
+          }
+          __syncwarp();
+          if (phys >= 0)  // block i of the tile: BS rows of 128 codes at row i * BS of the upper half
+            tma_load_2d(slot(j) + Sh::HALF + lane * BS * 128, do_k ? &kmap : &vmap, 0,
+                        (phys * p.num_kv_heads + kvh) * BS, bar);
+          ++ni;
+        }
+        t_last = clock64();
+      }
+      // no copy may still be landing when the CTA leaves
+      if (lane == 0)
+        for (int j = nc; j < ni; ++j) mbar_wait(landed + j % NS, (j / NS) & 1);
+    } else {
     // Copy whichever slot frees first: K tile nk once S_{nk-3} is done, V tile
     // nv (never ahead of K) once PV_{nv-2} is done.
     int nk = 0, nv = 0;
@@ -326,10 +477,11 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
       for (int j = nk > KST ? nk - KST : 0; j < nk; ++j) mbar_wait(k_full + j % KST, (j / KST) & 1);
       for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) mbar_wait(v_full + (j & 1), (j >> 1) & 1);
     }
+    }
   } else if (warp == 1) {
     // ---- MMA issue (one thread)
     if (lane == 0) {
-      constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+      constexpr bool BF = std::is_same<TP, __nv_bfloat16>::value;
       constexpr uint32_t IDESC_S = tc::idesc_f16(BF, Sh::ROWS, NT, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_f16(BF, Sh::ROWS, D, false, true);
       const uint32_t q_addr = smem_u32(Qs);
@@ -389,13 +541,19 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   } else if (srole) {
     // ---- softmax rows
     // the query rows (zeros past R), copied while the copy warps start: tell the MMA thread once landed
-    mq_tc_fetch_q<T, D, Sh::ROWS>(Qs, row, reinterpret_cast<const T*>(p.query), q0, kvh, rt, q_len, G, p.num_heads);
-    cp_async_wait_all();
+    float qscale = 1.f;  // FP8 pool, bf16 query: the 2^-k the row was scaled by
+    if constexpr (F8 && std::is_same<T, __nv_bfloat16>::value) {
+      qscale = mq_tc_fetch_q_bf16_as_f16<D, Sh::ROWS>(Qs, row, reinterpret_cast<const __nv_bfloat16*>(p.query), q0,
+                                                      kvh, rt, q_len, G, p.num_heads);
+    } else {
+      mq_tc_fetch_q<T, D, Sh::ROWS>(Qs, row, reinterpret_cast<const T*>(p.query), q0, kvh, rt, q_len, G, p.num_heads);
+      cp_async_wait_all();
+    }
     fence_proxy_async_smem();  // generic-proxy writes, read by the S MMAs
     mbar_arrive(q_full);
     const int lim = active ? mq_limit(mq, ctx, q_len, r, G) : 0;  // this row sees positions < lim
     const int vis = min(lim, tok1);
-    const float sl2 = p.scale_log2;
+    const float sl2 = p.scale_log2 * qscale;
     const uint32_t all = (1u << NBT) - 1u;
     // which blocks of each tile were fetched: the same test as the producer's
     int ids[Sh::IDS];
@@ -458,8 +616,8 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
       if (m_ref != -INFINITY) {
 #pragma unroll
         for (int u = 0; u < NT / 2; ++u) {
-          pw[u] = Elem<T>::pack2(fast_exp2(x[2 * u] - m_ref), fast_exp2(x[2 * u + 1] - m_ref));
-          const float2 r = Elem<T>::to_float2(pw[u]);  // l sums the weights PV multiplies
+          pw[u] = Elem<TP>::pack2(fast_exp2(x[2 * u] - m_ref), fast_exp2(x[2 * u + 1] - m_ref));
+          const float2 r = Elem<TP>::to_float2(pw[u]);  // l sums the weights PV multiplies
           ls[u & 3] += r.x + r.y;
         }
       } else {
@@ -511,7 +669,8 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     if (ok) ok = tc_wait(pv_done + ((ntile - 1) & 1), ((ntile - 1) >> 1) & 1, abort);
     tc::fence_after_sync();
     ok = ok && !*abort;
-    const float inv = ok && l > 0.f ? 1.f / l : 0.f;
+    // 1 / l (FP8 pool: times the value of one V code)
+    const float inv = ok && l > 0.f ? (F8 ? p.v_scale : 1.f) / l : 0.f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -551,11 +710,11 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   }
 }
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool F8 = false>
 cudaError_t launch_mq_tc(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, int num_seqs, cudaStream_t stream) {
   using Sh = MqTcShape<T, D, BS>;
-  auto kern = pkv_mq_tc_kernel<T, D, BS>;
+  auto kern = pkv_mq_tc_kernel<T, D, BS, F8>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -92,3 +92,22 @@ def test_bad_block_id_is_reported(cuda_lib):
     out = run_mq_fp8(batch, t, to_dev_u8(kc8), to_dev_u8(vc8), ks, vs)
     assert binding.device_errors() & 1
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("tile", ["columns", "tensor"])
+@pytest.mark.parametrize("H,Hkv,dtype,B,ctx,ql,ks,vs,P", [CASES[0], CASES[2], CASES[3], CASES[4]])
+def test_both_tiles_match_oracle(cuda_lib, tile, H, Hkv, dtype, B, ctx, ql, ks, vs, P):
+    """The 8-column tile (E4M3 contraction) and the tensor-memory tile (codes widened to f16 in shared
+    memory; a bf16 query scaled per row into f16) on the same FP8 inputs, each against the oracle."""
+    batch = W.build_batch(seed=840 + H + B + len(ctx), context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
+                          head_dim=128, block_size=B, dtype=dtype, pool_factor=1.3, query_lens=ql)
+    kc8, vc8 = fp8_pools(batch, ks, vs)
+    t = W.as_torch(batch, DEV)
+    prev = binding.set_multi_query_tile(binding.MQ_TILE_TENSOR if tile == "tensor" else binding.MQ_TILE_COLUMNS)
+    try:
+        binding.device_errors(clear=True)
+        out = run_mq_fp8(batch, t, to_dev_u8(kc8), to_dev_u8(vc8), ks, vs, partition_size=P)
+    finally:
+        binding.set_multi_query_tile(prev)
+    check_close(as_bits(out), reference(batch, kc8, vc8, ks, vs), dtype, f"{tile}: H {H} Hkv {Hkv} P {P}")
+    assert binding.device_errors() == 0
