@@ -29,6 +29,13 @@
 // by more than 2^8, which keeps P within the 16-bit range. Two CTAs share an
 // SM, so one CTA's start and end overlap the other's streaming.
 //
+// FP8 (E4M3) pool (F8): each K/V tile's codes land, one copy per pool block,
+// in the upper half of the tile's f16 slot; the copy warp that issued them
+// widens them in place into the f16 operand layout (the codes convert to f16
+// exactly) and only then signals the MMA thread. A bf16 query is scaled per row
+// by a power of two into f16, so both MMAs multiply f16; the output takes
+// v_scale.
+//
 // Every wait is bounded: a copy or MMA that does not complete makes the CTA
 // stop, set PKV_DEVERR_TIMEOUT and write an empty result.
 #pragma once
