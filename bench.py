@@ -137,13 +137,14 @@ def default_partition(fp8: bool, mq: bool = False, block_size: int = 16) -> int:
 SHARED_PREFIX_TOKENS = 1024  # workload 4's common prefix
 
 
-def shared_prefix_call_bytes(batch, prefix_tokens: int, ws_bytes: int):
+def shared_prefix_call_bytes(batch, prefix_tokens: int, ws_bytes: int, cache_bytes: int = 2):
     """Bytes the shared-prefix call must move: the prefix's K/V once, every tail's K/V, q and out, the
-    tables, and the two stages' partials (written, then read by the merge)."""
+    tables, and the two stages' partials (written, then read by the merge). cache_bytes: per cached
+    K/V element (1 for an FP8 cache)."""
     from paged_kv_cache_91_gb300 import workloads as W
 
     S, H, D, B, e = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size, batch.elem_bytes
-    kv = W.unique_kv_bytes(batch)
+    kv = W.unique_kv_bytes(batch) * cache_bytes // e
     tail_blocks = int(((batch.context_lens - prefix_tokens + B - 1) // B).sum())
     tables = (prefix_tokens // B + tail_blocks) * 4 + S * 4
     return kv + 2 * S * H * D * e + tables + 2 * ws_bytes
@@ -480,8 +481,8 @@ def run_ours(args, dist):
     fp8 = args.kv_dtype == "fp8_e4m3"
     shared = args.shared_prefix
     if shared:
-        if mq or fp8 or args.config != 4:
-            raise SystemExit("--shared-prefix runs workload 4 (16-bit cache, one query token per sequence)")
+        if mq or args.config != 4:
+            raise SystemExit("--shared-prefix runs workload 4 (one query token per sequence)")
         # the call's own inputs: the common prefix's blocks, then each sequence's tail table and length
         pb, tails, tail_lens = W.split_shared_prefix(batch, SHARED_PREFIX_TOKENS)
         prefix_dev = torch.from_numpy(pb).to(dev)
@@ -508,7 +509,7 @@ def run_ours(args, dist):
     kv_bytes, call_bytes = step_bytes(batch, P, cache_bytes)
     if shared:
         launches_per_step = 4  # write, prefix, tails, merge
-        call_bytes = shared_prefix_call_bytes(batch, SHARED_PREFIX_TOKENS, ws_bytes)
+        call_bytes = shared_prefix_call_bytes(batch, SHARED_PREFIX_TOKENS, ws_bytes, cache_bytes)
     if fp8:
         # the FP8 pool: every slot of the 16-bit pool quantized by the library's own write (setup, untimed)
         NB, Hkv, B, D = t["key_cache"].shape
@@ -529,7 +530,12 @@ def run_ours(args, dist):
             binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
 
     def decode(q, bt, cl, o, qsl=None):
-        if shared:  # bt, cl: the tail tables and lengths
+        if shared and fp8:  # bt, cl: the tail tables and lengths
+            binding.paged_attention_decode_shared_prefix_fp8(o, q, t["key_cache"], t["value_cache"], prefix_dev,
+                                                             SHARED_PREFIX_TOKENS, bt, cl, batch.scale, FP8_SCALE,
+                                                             FP8_SCALE, max_tail_len=max_tail, workspace=ws,
+                                                             stream=stream)
+        elif shared:
             binding.paged_attention_decode_shared_prefix(o, q, t["key_cache"], t["value_cache"], prefix_dev,
                                                          SHARED_PREFIX_TOKENS, bt, cl, batch.scale,
                                                          max_tail_len=max_tail, workspace=ws, stream=stream)
@@ -667,7 +673,8 @@ def run_ours(args, dist):
             "tokens_per_s": round(n_query_rows * dist.world * K / (total_ms / 1e3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
                             "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
-            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_shared_prefix (prefix, tail and merge "
+            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_shared_prefix" + ("_fp8" if fp8 else "")
+                         + " (prefix, tail and merge "
                          "kernels; bytes: the prefix once, the tails, q, out, partials)" if shared else
                          ("paged_attention_multi_query" + ("_fp8" if fp8 else "") if mq else
                                                     "paged_attention_decode_fp8" if fp8 else "paged_attention_decode")

@@ -427,8 +427,8 @@ pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const
  *   workspace          >= paged_attention_shared_prefix_workspace_size(...) bytes,
  *                      16-byte aligned (always needed: both parts leave partials)
  *
- * 16-bit caches only (PKV_F16, PKV_BF16); head_dim 64 or 128; block_size 8, 16
- * or 32. Errors as in paged_attention_decode: bad block ids are skipped with
+ * 16-bit caches (PKV_F16, PKV_BF16; an FP8 pool: the _fp8 form below); head_dim
+ * 64 or 128; block_size 8, 16 or 32. Errors as in paged_attention_decode: bad block ids are skipped with
  * PKV_DEVERR_BLOCK_ID. Asynchronous on `stream`; three kernels (prefix, tails,
  * merge). The prefix kernel runs on a second stream beside the tails: event
  * waits order it after the work already queued on `stream` and the merge after
@@ -450,6 +450,24 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
                                                   int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t num_blocks, pkv_dtype_t dtype, void* workspace,
                                                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * paged_attention_decode_shared_prefix_fp8 -- paged_attention_decode_shared_prefix
+ * over an FP8 (E4M3) pool: key_cache and value_cache hold uint8 codes standing
+ * for code * k_scale and code * v_scale (as in paged_attention_decode_fp8; both
+ * scales finite and > 0), head_dim 128, dtype the query's and out's (PKV_F16 or
+ * PKV_BF16). The stages run the FP8 forms of the multi-query tiles; the
+ * workspace and every other argument are those of the 16-bit call.
+ */
+pkv_status_t paged_attention_decode_shared_prefix_fp8(void* out, const void* query, const void* key_cache,
+                                                      const void* value_cache, const int32_t* prefix_blocks,
+                                                      int32_t prefix_len, const int32_t* block_tables,
+                                                      int32_t max_blocks_per_seq, const int32_t* tail_lens,
+                                                      int32_t num_seqs, int32_t max_tail_len, float scale,
+                                                      int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                                      int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                                      float k_scale, float v_scale, void* workspace,
+                                                      size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * FP8 KV cache. The pages pass kv_cache_dtype, k_scale and v_scale to the cache

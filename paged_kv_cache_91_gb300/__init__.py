@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     paged_attention_decode,
     paged_attention_decode_fp8,
     paged_attention_decode_shared_prefix,
+    paged_attention_decode_shared_prefix_fp8,
     paged_attention_multi_query,
     paged_attention_multi_query_fp8,
     paged_attention_multi_query_workspace_size,

@@ -72,6 +72,9 @@ def load():
     lib.paged_attention_decode_shared_prefix.restype = i32
     lib.paged_attention_decode_shared_prefix.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, i32, i32,
                                                          i32, i32, i32, P, sz, P]
+    lib.paged_attention_decode_shared_prefix_fp8.restype = i32
+    lib.paged_attention_decode_shared_prefix_fp8.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, i32,
+                                                             i32, i32, i32, i32, f32, f32, P, sz, P]
     lib.paged_attention_multi_query.restype = i32
     lib.paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, f32, i32, i32, i32,
                                                 i32, i32, i32, i32, P, sz, P]
@@ -375,18 +378,16 @@ def paged_attention_shared_prefix_workspace_size(num_seqs: int, num_heads: int, 
                                                                    block_size, prefix_len, max_tail_len))
 
 
-def paged_attention_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
-                                         value_cache: torch.Tensor, prefix_blocks: torch.Tensor, prefix_len: int,
-                                         block_tables: torch.Tensor, tail_lens: torch.Tensor, scale: float,
-                                         max_tail_len: Optional[int] = None,
-                                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Decode for sequences that share their first prefix_len tokens (prefix_blocks [prefix_len / B] int32);
-    block_tables [S][max] and tail_lens [S] describe each sequence's tokens after the prefix. Same result as
-    paged_attention_decode over prefix_blocks ++ block_tables[s], with the prefix read once."""
+def _shared_prefix(out, query, key_cache, value_cache, prefix_blocks, prefix_len, block_tables, tail_lens, scale,
+                   max_tail_len, workspace, stream, fp8, k_scale, v_scale):
     lib = load()
     dt = _cuda16("query", query)
-    for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
-        if _cuda16(n, t) != dt:
+    if _cuda16("out", out) != dt:
+        raise PagedKVError(-1, "out dtype differs from query")
+    for n, t in (("key_cache", key_cache), ("value_cache", value_cache)):
+        if fp8:
+            _cuda_fp8(n, t)
+        elif _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
     for n, t in (("prefix_blocks", prefix_blocks), ("block_tables", block_tables), ("tail_lens", tail_lens)):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
@@ -404,11 +405,37 @@ def paged_attention_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor,
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size()
-    _check(lib, lib.paged_attention_decode_shared_prefix(
-        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(prefix_blocks), int(prefix_len),
-        _ptr(block_tables), maxb, _ptr(tail_lens), S, int(max_tail_len), float(scale), B, H, Hkv, D, NB, dt,
-        _ptr(workspace), wbytes, _stream(query, stream)))
+    head = (_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(prefix_blocks), int(prefix_len),
+            _ptr(block_tables), maxb, _ptr(tail_lens), S, int(max_tail_len), float(scale), B, H, Hkv, D, NB, dt)
+    tail = (_ptr(workspace), wbytes, _stream(query, stream))
+    if fp8:
+        _check(lib, lib.paged_attention_decode_shared_prefix_fp8(*head, float(k_scale), float(v_scale), *tail))
+    else:
+        _check(lib, lib.paged_attention_decode_shared_prefix(*head, *tail))
     return out
+
+
+def paged_attention_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                         value_cache: torch.Tensor, prefix_blocks: torch.Tensor, prefix_len: int,
+                                         block_tables: torch.Tensor, tail_lens: torch.Tensor, scale: float,
+                                         max_tail_len: Optional[int] = None,
+                                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode for sequences that share their first prefix_len tokens (prefix_blocks [prefix_len / B] int32);
+    block_tables [S][max] and tail_lens [S] describe each sequence's tokens after the prefix. Same result as
+    paged_attention_decode over prefix_blocks ++ block_tables[s], with the prefix read once."""
+    return _shared_prefix(out, query, key_cache, value_cache, prefix_blocks, prefix_len, block_tables, tail_lens,
+                          scale, max_tail_len, workspace, stream, False, 1.0, 1.0)
+
+
+def paged_attention_decode_shared_prefix_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                             value_cache: torch.Tensor, prefix_blocks: torch.Tensor,
+                                             prefix_len: int, block_tables: torch.Tensor, tail_lens: torch.Tensor,
+                                             scale: float, k_scale: float, v_scale: float,
+                                             max_tail_len: Optional[int] = None,
+                                             workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_attention_decode_shared_prefix over an E4M3 pool (elements code * k_scale, code * v_scale)."""
+    return _shared_prefix(out, query, key_cache, value_cache, prefix_blocks, prefix_len, block_tables, tail_lens,
+                          scale, max_tail_len, workspace, stream, True, k_scale, v_scale)
 
 
 def device_errors(clear: bool = True) -> int:

@@ -1248,14 +1248,16 @@ size_t paged_attention_shared_prefix_workspace_size(int32_t num_seqs, int32_t nu
   return (size_t)num_seqs * num_heads * (pl.np1 + pl.np2) * (head_dim + 2) * sizeof(float);
 }
 
-pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, const void* key_cache,
-                                                  const void* value_cache, const int32_t* prefix_blocks,
-                                                  int32_t prefix_len, const int32_t* block_tables,
-                                                  int32_t max_blocks_per_seq, const int32_t* tail_lens,
-                                                  int32_t num_seqs, int32_t max_tail_len, float scale,
-                                                  int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
-                                                  int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
-                                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+namespace {
+// Both shared-prefix entry points. fp8: the caches hold E4M3 codes of value / k_scale and
+// value / v_scale (head_dim 128); the stages run the multi-query kernels' FP8 forms.
+pkv_status_t shared_prefix_impl(void* out, const void* query, const void* key_cache, const void* value_cache,
+                                const int32_t* prefix_blocks, int32_t prefix_len, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* tail_lens, int32_t num_seqs,
+                                int32_t max_tail_len, float scale, int32_t block_size, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream, bool fp8,
+                                float k_scale, float v_scale) {
   g_msg[0] = '\0';
   if (num_seqs < 0 || prefix_len < 0 || max_tail_len < 0)
     return fail(PKV_ERR_INVALID_ARG, "num_seqs, prefix_len and max_tail_len must be >= 0");
@@ -1268,6 +1270,10 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
   if (!supported_block_size(block_size))
     return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", block_size);
   if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (fp8 && !(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+  if (fp8 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "the shared-prefix call over an FP8 pool needs head_dim 128 (got %d)", head_dim);
   if (prefix_len % block_size)
     return fail(PKV_ERR_INVALID_ARG, "prefix_len %d must be a whole number of blocks of %d", prefix_len, block_size);
   if (max_tail_len > 0 && (max_blocks_per_seq <= 0 || (long long)max_tail_len > (long long)max_blocks_per_seq * block_size))
@@ -1308,8 +1314,8 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
   base.key_cache = static_cast<const unsigned char*>(key_cache);
   base.value_cache = static_cast<const unsigned char*>(value_cache);
   base.err = err;
-  base.scale_log2 = scale * 1.4426950408889634f;
-  base.v_scale = 1.f;
+  base.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);  // scores in the base-2 domain
+  base.v_scale = fp8 ? v_scale : 1.f;
   base.num_heads = num_heads;
   base.num_kv_heads = num_kv_heads;
   base.group = G;
@@ -1319,6 +1325,12 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
   auto maps = [&](int tile, CUtensorMap* km, CUtensorMap* vm) {
     memset(km, 0, sizeof *km);
     memset(vm, 0, sizeof *vm);
+    if (fp8 && tile == PKV_MQ_TILE_TENSOR)
+      return make_pool_map_fp8_rows(km, key_cache, pool_rows, block_size) &&
+             make_pool_map_fp8_rows(vm, value_cache, pool_rows, block_size);
+    if (fp8)
+      return make_pool_map(km, key_cache, pool_rows, head_dim, block_size, PKV_FP8_E4M3) &&
+             make_pool_map(vm, value_cache, pool_rows, head_dim, block_size, PKV_FP8_E4M3);
     if (head_dim == 128 && (tile == PKV_MQ_TILE_TENSOR || tile_one_copy()))
       return make_pool_map_tc(km, key_cache, pool_rows, block_size, dtype) &&
              make_pool_map_tc(vm, value_cache, pool_rows, block_size, dtype);
@@ -1327,6 +1339,9 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
   };
   auto run = [&](const DecodeParams& p, const MqParams& mq, const CUtensorMap& km, const CUtensorMap& vm, int seqs,
                  int tile, cudaStream_t st) {
+    if (fp8)
+      return dtype == PKV_F16 ? decode_mq_fp8_f16(p, mq, km, vm, head_dim, block_size, seqs, tile, st)
+                              : decode_mq_fp8_bf16(p, mq, km, vm, head_dim, block_size, seqs, tile, st);
     return dtype == PKV_F16 ? decode_mq_f16(p, mq, km, vm, head_dim, block_size, seqs, tile, st)
                             : decode_mq_bf16(p, mq, km, vm, head_dim, block_size, seqs, tile, st);
   };
@@ -1419,6 +1434,36 @@ pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, 
                             max_tail_len, num_seqs, num_heads);
   if (e != cudaSuccess) return cuda_fail(e, "shared-prefix merge launch");
   return PKV_OK;
+}
+}  // namespace
+
+pkv_status_t paged_attention_decode_shared_prefix(void* out, const void* query, const void* key_cache,
+                                                  const void* value_cache, const int32_t* prefix_blocks,
+                                                  int32_t prefix_len, const int32_t* block_tables,
+                                                  int32_t max_blocks_per_seq, const int32_t* tail_lens,
+                                                  int32_t num_seqs, int32_t max_tail_len, float scale,
+                                                  int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return shared_prefix_impl(out, query, key_cache, value_cache, prefix_blocks, prefix_len, block_tables,
+                            max_blocks_per_seq, tail_lens, num_seqs, max_tail_len, scale, block_size, num_heads,
+                            num_kv_heads, head_dim, num_blocks, dtype, workspace, workspace_bytes, stream, false,
+                            1.f, 1.f);
+}
+
+pkv_status_t paged_attention_decode_shared_prefix_fp8(void* out, const void* query, const void* key_cache,
+                                                      const void* value_cache, const int32_t* prefix_blocks,
+                                                      int32_t prefix_len, const int32_t* block_tables,
+                                                      int32_t max_blocks_per_seq, const int32_t* tail_lens,
+                                                      int32_t num_seqs, int32_t max_tail_len, float scale,
+                                                      int32_t block_size, int32_t num_heads, int32_t num_kv_heads,
+                                                      int32_t head_dim, int32_t num_blocks, pkv_dtype_t dtype,
+                                                      float k_scale, float v_scale, void* workspace,
+                                                      size_t workspace_bytes, cudaStream_t stream) {
+  return shared_prefix_impl(out, query, key_cache, value_cache, prefix_blocks, prefix_len, block_tables,
+                            max_blocks_per_seq, tail_lens, num_seqs, max_tail_len, scale, block_size, num_heads,
+                            num_kv_heads, head_dim, num_blocks, dtype, workspace, workspace_bytes, stream, true,
+                            k_scale, v_scale);
 }
 
 pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream) {

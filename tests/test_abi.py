@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
               "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
               "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
               "paged_attention_multi_query", "paged_attention_multi_query_workspace_size",
-              "paged_attention_multi_query_fp8",
+              "paged_attention_multi_query_fp8", "paged_attention_decode_shared_prefix_fp8",
               "pkv_set_multi_query_tile"):
         assert n in names
 

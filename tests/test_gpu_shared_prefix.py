@@ -171,3 +171,50 @@ def test_graph_capture_and_replay(cuda_lib):
     check_close(as_bits(out_sp), ref, BF16, "shared prefix, graph replay")
     check_close(as_bits(out_dec), ref, BF16, "decode, graph replay")
     assert binding.device_errors() == 0
+
+
+FP8_CASES = [
+    # H, Hkv, dtype, B, num_seqs, prefix tokens, tail range, k_scale, v_scale
+    (32, 8, F16, 16, 16, 256, (1, 200), 2 ** -6, 2 ** -6),        # 64 rows: the prefix on the tensor tile
+    (8, 8, BF16, 16, 8, 512, (0, 300), 2 ** -5, 2 ** -7),         # MHA, 8 rows: prefix on the 8-column tile
+    (16, 4, BF16, 32, 12, 1024, (1, 700), 0.013, 0.021),          # bf16 query scaled per row, block 32
+    (64, 8, BF16, 16, 40, 2048, (1, 64), 2 ** -6, 2 ** -6),       # 320 rows, long prefix in partitions
+]
+
+
+@pytest.mark.parametrize("H,Hkv,dtype,B,S,prefix,tails,ks,vs", FP8_CASES)
+def test_shared_prefix_fp8_matches_decode_oracle(cuda_lib, H, Hkv, dtype, B, S, prefix, tails, ks, vs):
+    """paged_attention_decode_shared_prefix_fp8 against the oracle's decode of the full tables over the same
+    E4M3 codes (the pools are the 16-bit pools encoded by the oracle)."""
+    from test_gpu_fp8 import fp8_pools, to_dev_u8
+    rng = np.random.default_rng(900 + H + B + S)
+    ctx = prefix + rng.integers(tails[0], tails[1] + 1, size=S)
+    batch = W.build_batch(seed=901 + S, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=128,
+                          block_size=B, dtype=dtype, pool_factor=1.3, shared_prefix_tokens=prefix)
+    kc8, vc8 = fp8_pools(batch, ks, vs)
+    t = W.as_torch(batch, DEV)
+    pb, tails_t, lens = W.split_shared_prefix(batch, prefix)
+    out = torch.empty_like(t["query"])
+    binding.device_errors(clear=True)
+    binding.paged_attention_decode_shared_prefix_fp8(out, t["query"], to_dev_u8(kc8), to_dev_u8(vc8),
+                                                     torch.from_numpy(pb).to(DEV), prefix,
+                                                     torch.from_numpy(tails_t).to(DEV), torch.from_numpy(lens).to(DEV),
+                                                     batch.scale, ks, vs, max_tail_len=int(lens.max()))
+    torch.cuda.synchronize()
+    ref = oracle.decode_c(batch.query, kc8, vc8, batch.block_tables, batch.context_lens, batch.scale, dtype,
+                          k_scale=ks, v_scale=vs)
+    check_close(as_bits(out), ref, dtype, f"fp8, prefix {prefix}")
+    assert binding.device_errors() == 0
+
+
+def test_shared_prefix_fp8_rejects_head_dim_64(cuda_lib):
+    batch = W.build_batch(seed=910, context_lens=[64 + 5], num_heads=4, num_kv_heads=2, head_dim=64,
+                          block_size=16, dtype=F16, pool_factor=1.5, shared_prefix_tokens=64)
+    t = W.as_torch(batch, DEV)
+    pb, tails, lens = W.split_shared_prefix(batch, 64)
+    k8 = torch.zeros(t["key_cache"].shape, dtype=torch.uint8, device=DEV)
+    with pytest.raises(binding.PagedKVError):
+        binding.paged_attention_decode_shared_prefix_fp8(torch.empty_like(t["query"]), t["query"], k8, k8.clone(),
+                                                         torch.from_numpy(pb).to(DEV), 64,
+                                                         torch.from_numpy(tails).to(DEV),
+                                                         torch.from_numpy(lens).to(DEV), batch.scale, 1.0, 1.0)
