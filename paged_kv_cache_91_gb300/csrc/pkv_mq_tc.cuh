@@ -157,12 +157,17 @@ __device__ __noinline__ void mq_tc_fetch_q(unsigned char* Qs, int row, const T* 
 // into registers before anything is written (the output overwrites the codes).
 __device__ __forceinline__ void mq_tc_widen_tile(unsigned char* dst, const unsigned char* src, int lane) {
   const int t8 = lane >> 2, q = lane & 3;
+  // An 8-lane phase of a 16-byte load covers two token rows 128 bytes apart; odd rows fetch their
+  // second 16 bytes first, so that the two rows fall on different banks.
+  const int h0 = (t8 & 1) * 16, h1 = 16 - h0;
   uint4 c[8][2];
 #pragma unroll
   for (int a = 0; a < 8; ++a) {
     const int t = 8 * a + t8;
-    c[a][0] = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q);
-    c[a][1] = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q + 16);
+    const uint4 x = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q + h0);
+    const uint4 y = *reinterpret_cast<const uint4*>(src + t * 128 + 32 * q + h1);
+    c[a][0] = h0 ? y : x;
+    c[a][1] = h0 ? x : y;
   }
   __syncwarp();
 #pragma unroll
