@@ -404,14 +404,15 @@ pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const
  * those full blocks shared in the pool ("'안녕하세요 반갑습니다'로 배우는 vLLM
  * — KV Cache와 PagedAttention 완전 해부", §9단계; "Sparse Computation and
  * Memory Management for Efficient LLM Inference", Copy-on-Write). The result
- * is exactly paged_attention_decode's with block table prefix_blocks ++
- * block_tables[s] and context length prefix_len + tail_lens[s], but the
- * prefix's K/V tiles are read and multiplied once for all sequences. All
- * num_seqs * num_heads query rows of the batch attend the prefix as one
- * multi-query problem on the tensor-memory tile (the 8-column tile below 64
- * rows per kv head). Each sequence's tail is one decode token over its own
- * blocks. The two parts' (m, l, o) partials are merged by the log-sum-exp
- * rule of the split-K reduce.
+ * is paged_attention_decode's, up to rounding order, with block table
+ * prefix_blocks ++ block_tables[s] and context length prefix_len +
+ * tail_lens[s], but the prefix's K/V tiles are read and multiplied once for
+ * all sequences. All num_seqs * num_heads query rows of the batch attend the
+ * prefix as one multi-query problem on the tensor-memory tile (the 8-column
+ * tile at 16 or fewer rows per kv head, num_seqs * group; the FP8 form
+ * switches at the same 16 rows, so both forms share one workspace size). Each
+ * sequence's tail is one decode token over its own blocks. The two parts'
+ * (m, l, o) partials are merged by the log-sum-exp rule of the split-K reduce.
  *
  *   out, query         [num_seqs][num_heads][head_dim], dtype
  *   key_cache, value_cache   the pool, [num_blocks][num_kv_heads][block_size][head_dim]

@@ -834,6 +834,8 @@ PrefixPlan prefix_plan(int num_seqs, int group, int num_kv_heads, int block_size
                        int max_tail_len) {
   PrefixPlan pl{};
   const long long rows = (long long)num_seqs * group;
+  // One threshold for 16-bit and FP8 pools: the partition count depends on the tile, and the workspace
+  // size function does not know the pool's dtype.
   pl.tensor = rows >= PKV_MQ_WIDE_MIN_ROWS;
   const int rpt = pl.tensor ? 128 : 8;
   pl.rt1 = (int)((rows + rpt - 1) / rpt);
