@@ -319,13 +319,14 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *                     order changes no result.
  * Everything else is as in paged_attention_decode (the decode-path choice does
  * not apply: this call always runs partitioned, on the tensor cores, for every
- * group size). A sequence whose query_start_loc entries are out of order, give
- * it more than max_query_len or context_lens[s] tokens, or reach past
- * num_query_tokens is skipped (its rows are not written) and sets
+ * group size). A sequence whose query_start_loc entries are out of order,
+ * give it more than max_query_len or context_lens[s] tokens, or reach past
+ * num_query_tokens is skipped (its rows are not written), and the call sets
  * PKV_DEVERR_QUERY.
  */
 /*
- * Multi-query tiles (pkv_set_multi_query_tile). Both compute the same result.
+ * Multi-query tiles (pkv_set_multi_query_tile). All three compute the same
+ * result, up to rounding order.
  *   PKV_MQ_TILE_COLUMNS  8 (query token, head) rows of one kv head per CTA, in
  *                        the n = 8 dimension of the MMA, the CTA's warps
  *                        splitting the context's blocks. Reads no padding rows
@@ -339,7 +340,8 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *                        memory, one thread per row runs the softmax.
  *   PKV_MQ_TILE_AUTO     TENSOR when max_query_len * (num_heads / num_kv_heads)
  *                        > 16 (more than two 8-column CTAs per kv head), else
- *                        COLUMNS (default).
+ *                        COLUMNS (default). Over an FP8 pool the switch is at
+ *                        > 32 rows (paged_attention_multi_query_fp8).
  */
 #define PKV_MQ_TILE_AUTO 0
 #define PKV_MQ_TILE_COLUMNS 1
