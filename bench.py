@@ -68,7 +68,7 @@ def parse_args():
     ap.add_argument("--query-len", type=int, default=None,
                     help="multi-query step: each sequence's last N context tokens are written and attend causally "
                          "(paged_attention_multi_query; speculative verification / chunked prefill)")
-    ap.add_argument("--mq-tile", choices=["auto", "columns", "rows", "tensor"], default="auto",
+    ap.add_argument("--mq-tile", choices=["auto", "columns", "rows", "tensor", "pairs"], default="auto",
                     help="multi-query tile (default: the library's choice by rows per kv head)")
     ap.add_argument("--shared-prefix", action="store_true",
                     help="workload 4 through paged_attention_decode_shared_prefix: the 1024-token prefix is "
@@ -180,6 +180,8 @@ KERNEL_SOURCES = {
            "pkv_tcgen05.cuh", "pkv_decode_mq.cu"),
     "mq_fp8": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mq.cuh",
                "pkv_mq_tc.cuh", "pkv_tcgen05.cuh", "pkv_decode_mq_fp8.cu"),
+    "mq_fp8_pairs": ("pkv_common.cuh", "pkv_decode_mma.cuh", "pkv_decode_mma_fp8.cuh", "pkv_decode_mq.cuh",
+                     "pkv_mq_pairs.cuh", "pkv_decode_mq_pairs.cu"),
 }
 
 
@@ -374,9 +376,16 @@ def mq_summary(batch, tile_arg, call_ms, fp8=False):
     vis = (ql * (ctx - ql) + ql * (ql + 1) // 2).sum()  # positions seen, summed over query tokens
     flops = 4.0 * batch.head_dim * batch.num_heads * float(vis)
     rows_per_kv_head = int(ql.max()) * (batch.num_heads // batch.num_kv_heads)
-    tile = tile_arg if tile_arg != "auto" else ("tensor" if rows_per_kv_head > (32 if fp8 else 16) else "columns")
+    if tile_arg != "auto":
+        tile = tile_arg
+    elif rows_per_kv_head > (32 if fp8 else 16):
+        tile = "tensor"
+    else:
+        tile = "pairs" if fp8 and rows_per_kv_head > 8 else "columns"
     if fp8 and tile == "rows":
         tile = "columns"  # no FP8 form of the 64-row tile
+    if not fp8 and tile == "pairs":
+        tile = "columns"  # the 16-row pairs exist for FP8 pools only
     return {"tile": tile, "rows_per_kv_head": rows_per_kv_head, "attention_gflop_per_call": round(flops / 1e9, 2),
             "attention_tflops": round(flops / (call_ms * 1e-3) / 1e12, 1)}
 
@@ -474,7 +483,8 @@ def run_ours(args, dist):
     out = torch.empty_like(t["query"])
     mcl = batch.max_context_len
     binding.set_multi_query_tile({"auto": binding.MQ_TILE_AUTO, "columns": binding.MQ_TILE_COLUMNS,
-                                  "rows": binding.MQ_TILE_ROWS, "tensor": binding.MQ_TILE_TENSOR}[args.mq_tile])
+                                  "rows": binding.MQ_TILE_ROWS, "tensor": binding.MQ_TILE_TENSOR,
+                                  "pairs": binding.MQ_TILE_PAIRS}[args.mq_tile])
     if args.path:
         binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
                                  "persistent": binding.DECODE_PERSISTENT}[args.path])
@@ -639,6 +649,8 @@ def run_ours(args, dist):
     G = batch.num_heads // batch.num_kv_heads
     if mq:
         kind = "mq_fp8" if fp8 else "mq"
+        if mq_summary(batch, args.mq_tile, 1.0, fp8)["tile"] == "pairs":
+            kind = "mq_fp8_pairs"
     elif fp8:
         kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
     else:

@@ -325,8 +325,8 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  * PKV_DEVERR_QUERY.
  */
 /*
- * Multi-query tiles (pkv_set_multi_query_tile). All three compute the same
- * result, up to rounding order.
+ * Multi-query tiles (pkv_set_multi_query_tile). All compute the same result,
+ * up to rounding order.
  *   PKV_MQ_TILE_COLUMNS  8 (query token, head) rows of one kv head per CTA, in
  *                        the n = 8 dimension of the MMA, the CTA's warps
  *                        splitting the context's blocks. Reads no padding rows
@@ -338,15 +338,20 @@ pkv_status_t pkv_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream
  *   PKV_MQ_TILE_TENSOR   128 rows per CTA on the fifth-generation tensor cores
  *                        (tcgen05): scores and outputs accumulate in tensor
  *                        memory, one thread per row runs the softmax.
+ *   PKV_MQ_TILE_PAIRS    FP8 pools only (COLUMNS over a 16-bit pool): 16 rows
+ *                        per CTA as two 8-column groups over one K/V ring,
+ *                        each K/V code widened once for both groups.
  *   PKV_MQ_TILE_AUTO     TENSOR when max_query_len * (num_heads / num_kv_heads)
  *                        > 16 (more than two 8-column CTAs per kv head), else
- *                        COLUMNS (default). Over an FP8 pool the switch is at
- *                        > 32 rows (paged_attention_multi_query_fp8).
+ *                        COLUMNS (default). Over an FP8 pool: TENSOR above 32
+ *                        rows, PAIRS from 9 to 32, COLUMNS up to 8
+ *                        (paged_attention_multi_query_fp8).
  */
 #define PKV_MQ_TILE_AUTO 0
 #define PKV_MQ_TILE_COLUMNS 1
 #define PKV_MQ_TILE_ROWS 2
 #define PKV_MQ_TILE_TENSOR 3
+#define PKV_MQ_TILE_PAIRS 4
 
 /* Choose the multi-query tile for later calls in this process (PKV_MQ_TILE_*).
  * Returns the previous choice, or -1 for an unknown value (nothing changes). */
@@ -385,8 +390,9 @@ pkv_status_t paged_attention_multi_query(void* out, const void* query, const voi
  * widens each K/V tile's codes to f16 in shared memory, and a bf16 query is
  * scaled per row by a power of two into f16, so that both MMAs multiply f16.
  * PKV_MQ_TILE_AUTO takes the tensor-memory tile above 32 rows per kv head (the
- * 8-column tile is relatively faster over an FP8 pool); PKV_MQ_TILE_ROWS runs
- * the 8-column tile.
+ * 8-column forms are relatively faster over an FP8 pool), PKV_MQ_TILE_PAIRS
+ * from 9 to 32 rows and the 8-column tile up to 8; PKV_MQ_TILE_ROWS runs the
+ * 8-column tile.
  */
 pkv_status_t paged_attention_multi_query_fp8(void* out, const void* query, const void* key_cache,
                                              const void* value_cache, const int32_t* block_tables,

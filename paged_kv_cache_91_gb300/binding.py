@@ -284,7 +284,7 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
     return out
 
 
-MQ_TILE_AUTO, MQ_TILE_COLUMNS, MQ_TILE_ROWS, MQ_TILE_TENSOR = 0, 1, 2, 3
+MQ_TILE_AUTO, MQ_TILE_COLUMNS, MQ_TILE_ROWS, MQ_TILE_TENSOR, MQ_TILE_PAIRS = 0, 1, 2, 3, 4
 
 
 def set_multi_query_tile(tile: int) -> int:

@@ -954,7 +954,7 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
 
 int32_t pkv_set_multi_query_tile(int32_t tile) {
   if (tile != PKV_MQ_TILE_AUTO && tile != PKV_MQ_TILE_COLUMNS && tile != PKV_MQ_TILE_ROWS &&
-      tile != PKV_MQ_TILE_TENSOR)
+      tile != PKV_MQ_TILE_TENSOR && tile != PKV_MQ_TILE_PAIRS)
     return -1;
   return g_mq_tile.exchange(tile);
 }
@@ -1099,13 +1099,19 @@ pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const 
   const int G = num_heads / num_kv_heads;
   // Many rows per kv head go to a tile with query rows in the MMA's M, a few
   // to the 8-column tile, which reads no padding rows.
+  // Over an FP8 pool, 9 to 32 rows run as 16-row pairs of 8-column groups, which widen each code once.
+  const long long kv_rows = (long long)max_query_len * G;
   int tile = g_mq_tile.load(std::memory_order_relaxed);
   if (tile == PKV_MQ_TILE_AUTO)
-    tile = (long long)max_query_len * G >= (fp8 ? PKV_MQ_WIDE_MIN_ROWS_FP8 : PKV_MQ_WIDE_MIN_ROWS)
-               ? PKV_MQ_TILE_TENSOR
-               : PKV_MQ_TILE_COLUMNS;
-  if (fp8 && tile != PKV_MQ_TILE_TENSOR) tile = PKV_MQ_TILE_COLUMNS;  // no FP8 form of the 64-row tile
-  const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128 : tile == PKV_MQ_TILE_ROWS ? 64 : 8;
+    tile = kv_rows >= (fp8 ? PKV_MQ_WIDE_MIN_ROWS_FP8 : PKV_MQ_WIDE_MIN_ROWS) ? PKV_MQ_TILE_TENSOR
+           : fp8 && kv_rows > 8                                             ? PKV_MQ_TILE_PAIRS
+                                                                            : PKV_MQ_TILE_COLUMNS;
+  if (fp8 && tile == PKV_MQ_TILE_ROWS) tile = PKV_MQ_TILE_COLUMNS;  // no FP8 form of the 64-row tile
+  if (!fp8 && tile == PKV_MQ_TILE_PAIRS) tile = PKV_MQ_TILE_COLUMNS;  // the pairs exist for FP8 only
+  const int rows_per_tile = tile == PKV_MQ_TILE_TENSOR ? 128
+                            : tile == PKV_MQ_TILE_ROWS ? 64
+                            : tile == PKV_MQ_TILE_PAIRS ? 16
+                                                        : 8;
   const long long row_tiles = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
   if (num_seqs > 65535 || num_heads > 65535 || (long long)num_kv_heads * row_tiles > 65535)
     return fail(PKV_ERR_UNSUPPORTED,
@@ -1192,7 +1198,10 @@ pkv_status_t mq_impl(void* out, const void* query, const void* key_cache, const 
                : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
                      !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  if (fp8)
+  if (fp8 && tile == PKV_MQ_TILE_PAIRS)
+    e = dtype == PKV_F16 ? decode_mq_pairs_fp8_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream)
+                         : decode_mq_pairs_fp8_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, stream);
+  else if (fp8)
     e = dtype == PKV_F16 ? decode_mq_fp8_f16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream)
                          : decode_mq_fp8_bf16(p, mq, kmap, vmap, head_dim, block_size, num_seqs, tile, stream);
   else

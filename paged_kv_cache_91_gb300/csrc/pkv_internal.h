@@ -53,6 +53,13 @@ cudaError_t decode_mq_fp8_f16(const DecodeParams& p, const MqParams& mq, const C
 cudaError_t decode_mq_fp8_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs, int tile,
                                cudaStream_t stream);
+// The same over 16-row tiles of two 8-column groups (PKV_MQ_TILE_PAIRS; the pool through make_pool_map).
+cudaError_t decode_mq_pairs_fp8_f16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
+                                    const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs,
+                                    cudaStream_t stream);
+cudaError_t decode_mq_pairs_fp8_bf16(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
+                                     const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs,
+                                     cudaStream_t stream);
 
 // Persistent equal-work decode (pkv_decode_stream.cuh): CTAs per SM, launch, reduce.
 struct StreamParams;

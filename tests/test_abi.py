@@ -313,6 +313,7 @@ def test_multi_query_tile_switch(lib):
         assert lib.pkv_set_multi_query_tile(1) == 2
         assert lib.pkv_set_multi_query_tile(9) == -1
         assert lib.pkv_set_multi_query_tile(3) == 1  # the tensor-memory tile
-        assert lib.pkv_set_multi_query_tile(0) == 3
+        assert lib.pkv_set_multi_query_tile(4) == 3  # the FP8 16-row pairs
+        assert lib.pkv_set_multi_query_tile(0) == 4
     finally:
         lib.pkv_set_multi_query_tile(prev)

@@ -60,9 +60,12 @@ def test_multi_query_flops_and_tile_labels():
     visible = (3 * 7 + 3 * 4 // 2) + (5 * 35 + 5 * 6 // 2)  # per query token: its causal prefix
     assert m["attention_gflop_per_call"] == round(4.0 * 64 * 8 * visible / 1e9, 2)
     assert m["rows_per_kv_head"] == 20 and m["tile"] == "tensor"  # above 16 rows
-    assert bench.mq_summary(b, "auto", 1.0, fp8=True)["tile"] == "columns"  # FP8: above 32 rows only
+    assert bench.mq_summary(b, "auto", 1.0, fp8=True)["tile"] == "pairs"  # FP8: 16-row pairs from 9 to 32 rows
     assert bench.mq_summary(b, "rows", 1.0, fp8=True)["tile"] == "columns"
     assert bench.mq_summary(b, "tensor", 1.0, fp8=True)["tile"] == "tensor"
+    assert bench.mq_summary(b, "pairs", 1.0)["tile"] == "columns"  # no 16-bit form of the pairs
+    few = tiny([10, 40], H=8, Hkv=4, query_lens=[3, 4])  # G = 2: 8 rows per kv head
+    assert bench.mq_summary(few, "auto", 1.0, fp8=True)["tile"] == "columns"
 
 
 def test_kernel_hashes_cover_existing_sources():

@@ -43,6 +43,8 @@ CASES = [
     (32, 4, BF16, 32, [64, 333, 1024, 2050], [6, 2, 6, 1], 0.013, 0.021, 256),           # GQA 8: 48 rows, split
     (4, 4, F16, 16, [9, 33, 64], [9, 33, 64], 2 ** -6, 2 ** -6, 0),                      # the whole prompt, causal
     (16, 2, F16, 16, [2048, 4000], [16, 3], 2 ** -6, 2 ** -6, 1024),                     # 128 rows, long contexts
+    (12, 4, F16, 16, [50, 700, 2100], [3, 1, 3], 2 ** -6, 2 ** -6, 0),                    # GQA 3: 9 rows, pairs
+    (16, 4, BF16, 32, [300, 1000, 2500], [6, 5, 2], 0.013, 0.021, 0),                     # 24 rows: a ragged pair
 ]
 
 
@@ -94,16 +96,20 @@ def test_bad_block_id_is_reported(cuda_lib):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("tile", ["columns", "tensor"])
-@pytest.mark.parametrize("H,Hkv,dtype,B,ctx,ql,ks,vs,P", [CASES[0], CASES[2], CASES[3], CASES[4]])
+TILES = {"columns": binding.MQ_TILE_COLUMNS, "tensor": binding.MQ_TILE_TENSOR, "pairs": binding.MQ_TILE_PAIRS}
+
+
+@pytest.mark.parametrize("tile", ["columns", "tensor", "pairs"])
+@pytest.mark.parametrize("H,Hkv,dtype,B,ctx,ql,ks,vs,P", [CASES[0], CASES[2], CASES[3], CASES[4], CASES[6]])
 def test_both_tiles_match_oracle(cuda_lib, tile, H, Hkv, dtype, B, ctx, ql, ks, vs, P):
-    """The 8-column tile (E4M3 contraction) and the tensor-memory tile (codes widened to f16 in shared
-    memory; a bf16 query scaled per row into f16) on the same FP8 inputs, each against the oracle."""
+    """The 8-column tile (E4M3 contraction), the 16-row pairs of 8-column groups (each widened K/V fragment
+    shared by both groups) and the tensor-memory tile (codes widened to f16 in shared memory; a bf16 query
+    scaled per row into f16) on the same FP8 inputs, each against the oracle."""
     batch = W.build_batch(seed=840 + H + B + len(ctx), context_lens=ctx, num_heads=H, num_kv_heads=Hkv,
                           head_dim=128, block_size=B, dtype=dtype, pool_factor=1.3, query_lens=ql)
     kc8, vc8 = fp8_pools(batch, ks, vs)
     t = W.as_torch(batch, DEV)
-    prev = binding.set_multi_query_tile(binding.MQ_TILE_TENSOR if tile == "tensor" else binding.MQ_TILE_COLUMNS)
+    prev = binding.set_multi_query_tile(TILES[tile])
     try:
         binding.device_errors(clear=True)
         out = run_mq_fp8(batch, t, to_dev_u8(kc8), to_dev_u8(vc8), ks, vs, partition_size=P)
