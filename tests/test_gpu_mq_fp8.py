@@ -45,6 +45,7 @@ CASES = [
     (16, 2, F16, 16, [2048, 4000], [16, 3], 2 ** -6, 2 ** -6, 1024),                     # 128 rows, long contexts
     (12, 4, F16, 16, [50, 700, 2100], [3, 1, 3], 2 ** -6, 2 ** -6, 0),                    # GQA 3: 9 rows, pairs
     (16, 4, BF16, 32, [300, 1000, 2500], [6, 5, 2], 0.013, 0.021, 0),                     # 24 rows: a ragged pair
+    (16, 4, F16, 16, [0, 5, 90, 600], [0, 4, 0, 4], 2 ** -6, 2 ** -6, 0),                 # empty context, q_len 0
 ]
 
 
