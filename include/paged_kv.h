@@ -123,7 +123,8 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
                                   cudaStream_t stream);
 
 /*
- * Decode paths (pkv_set_decode_path). Both compute the same result.
+ * Decode paths (pkv_set_decode_path). Both compute the same result, up to
+ * rounding order.
  *   PKV_DECODE_PERSISTENT  one wave of CTAs. The (sequence, head group, block)
  *                          tiles of the whole batch are split into equal ranges,
  *                          one per warp. A sequence cut by a range boundary
