@@ -317,3 +317,20 @@ def test_multi_query_tile_switch(lib):
         assert lib.pkv_set_multi_query_tile(0) == 4
     finally:
         lib.pkv_set_multi_query_tile(prev)
+
+
+def test_binding_constants_match_the_header():
+    """The binding's dtype, decode-path, tile and device-error constants are the header's values."""
+    from paged_kv_cache_91_gb300 import binding
+
+    with open(HEADER) as f:
+        text = f.read()
+    defines = {m[0]: int(m[1]) for m in re.findall(r"^#define PKV_(\w+) (\d+)u?\b", text, flags=re.M)}
+    enum = {m[0]: int(m[1]) for m in re.findall(r"PKV_(F16|BF16|FP8_E4M3) = (\d+)", text)}
+    assert enum == {"F16": binding.PKV_F16, "BF16": binding.PKV_BF16, "FP8_E4M3": binding.PKV_FP8_E4M3}
+    for name in ("AUTO", "PARTITIONED", "PERSISTENT"):
+        assert defines[f"DECODE_{name}"] == getattr(binding, f"DECODE_{name}")
+    for name in ("AUTO", "COLUMNS", "ROWS", "TENSOR", "PAIRS"):
+        assert defines[f"MQ_TILE_{name}"] == getattr(binding, f"MQ_TILE_{name}")
+    header_bits = {v: k[len("DEVERR_"):] for k, v in defines.items() if k.startswith("DEVERR_")}
+    assert header_bits == binding.DEVERR_BITS
