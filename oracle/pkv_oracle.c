@@ -302,8 +302,11 @@ int oracle_decode(double* out, const uint16_t* query, const void* key_cache,
     long long n = pairs ? npairs : (long long)num_seqs * num_heads;
     int rc = 0;
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc)
+    /* a thread count for this loop only: omp_set_num_threads would outlive the call */
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc) num_threads(nt)
+#else
+    (void)num_threads;
 #endif
     for (long long i = 0; i < n; ++i) {
         int s = pairs ? pairs[2 * i] : (int)(i / num_heads);
@@ -393,8 +396,10 @@ int oracle_multi_query(double* out, const uint16_t* query, const void* key_cache
     long long n = (long long)num_seqs * num_heads;
     int rc1 = 0, rc2 = 0;
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc1, rc2)
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc1, rc2) num_threads(nt)
+#else
+    (void)num_threads;
 #endif
     for (long long i = 0; i < n; ++i) {
         int r = mq_pair(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
