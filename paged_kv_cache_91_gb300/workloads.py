@@ -177,6 +177,102 @@ def split_shared_prefix(batch: "DecodeBatch", prefix_tokens: int):
     return prefix, tails, tail_lens
 
 
+def _draw_queries(seed: int, ctx: np.ndarray, query_lens, H: int, D: int, dtype: str):
+    """The step's query rows: one per sequence with a context (decode), or q_s per sequence packed by
+    query_start_loc. Returns (q_len per sequence, query_start_loc or None, query bits)."""
+    S = int(ctx.shape[0])
+    qrng = np.random.default_rng([seed, _S_QUERY])
+    if query_lens is None:
+        qlen = (ctx > 0).astype(np.int64)
+        return qlen, None, round_f32_to(qrng.standard_normal((S, H, D), dtype=np.float32), dtype)
+    qlen = np.asarray(query_lens, dtype=np.int64)
+    if qlen.shape != ctx.shape or (qlen < 0).any() or (qlen > ctx).any():
+        raise ValueError("query_lens must give 0 <= q_s <= ctx_s per sequence")
+    qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    return qlen, qsl, round_f32_to(qrng.standard_normal((int(qsl[-1]), H, D), dtype=np.float32), dtype)
+
+
+def _new_tokens(ctx, qlen, qsl, tables, kc, vc, B: int):
+    """One row per new token: sequence s's last qlen[s] context positions (decode: row s, or slot -1 when
+    ctx = 0). Their K/V are copied from the pool. Returns (slot_mapping, new_key, new_value)."""
+    S = int(ctx.shape[0])
+    Hkv, D = kc.shape[1], kc.shape[3]
+    rows = S if qsl is None else int(qsl[-1])
+    slot_mapping = np.full(rows, -1, dtype=np.int64)
+    new_key = np.zeros((rows, Hkv, D), dtype=np.uint16)
+    new_value = np.zeros((rows, Hkv, D), dtype=np.uint16)
+    for s in range(S):
+        c, n = int(ctx[s]), int(qlen[s])
+        r0 = s if qsl is None else int(qsl[s])
+        for i in range(n):
+            p = c - n + i
+            phys = int(tables[s, p // B])
+            off = p % B
+            slot_mapping[r0 + i] = phys * B + off
+            new_key[r0 + i] = kc[phys, :, off, :]
+            new_value[r0 + i] = vc[phys, :, off, :]
+    live = slot_mapping[slot_mapping >= 0]
+    if len(np.unique(live)) != len(live):
+        raise ValueError("two sequences write the same slot")
+    return slot_mapping, new_key, new_value
+
+
+def with_query_lens(batch: "DecodeBatch", query_lens) -> "DecodeBatch":
+    """The same pool, tables and contexts with q_s query tokens per sequence (None: one decode token).
+    Equal to building the batch again with ``query_lens``: the queries come from the same seeded stream."""
+    ctx = batch.context_lens.astype(np.int64)
+    seed = batch.meta["seed"]
+    qlen, qsl, query = _draw_queries(seed, ctx, query_lens, batch.num_heads, batch.head_dim, batch.dtype)
+    sm, nk, nv = _new_tokens(ctx, qlen, qsl, batch.block_tables, batch.key_cache, batch.value_cache,
+                             batch.block_size)
+    return DecodeBatch(
+        name=batch.name, dtype=batch.dtype, num_heads=batch.num_heads, num_kv_heads=batch.num_kv_heads,
+        head_dim=batch.head_dim, block_size=batch.block_size, scale=batch.scale, query=query,
+        key_cache=batch.key_cache, value_cache=batch.value_cache, block_tables=batch.block_tables,
+        context_lens=batch.context_lens, slot_mapping=sm, new_key=nk, new_value=nv,
+        partition_size=batch.partition_size, meta=dict(batch.meta), query_start_loc=qsl)
+
+
+def sub_batch(batch: "DecodeBatch", seqs) -> "DecodeBatch":
+    """Sequences ``seqs`` of a batch over a compact pool that holds only their blocks (renumbered in order
+    of first use), with their query rows and new tokens. Used to time the CPU oracle on a bounded sample."""
+    seqs = [int(s) for s in seqs]
+    B = batch.block_size
+    ctx = batch.context_lens[seqs].astype(np.int64)
+    nblk = (ctx + B - 1) // B
+    old = []
+    index = {}
+    for s, n in zip(seqs, nblk):
+        for j in range(int(n)):
+            b = int(batch.block_tables[s, j])
+            if b not in index:
+                index[b] = len(old)
+                old.append(b)
+    old = np.asarray(old if old else [0], dtype=np.int64)
+    tables = np.full((len(seqs), max(1, int(nblk.max()) if len(seqs) else 1)), -1, dtype=np.int32)
+    for i, (s, n) in enumerate(zip(seqs, nblk)):
+        tables[i, :n] = [index[int(b)] for b in batch.block_tables[s, :n]]
+    qsl = batch.query_start_loc
+    if qsl is None:
+        rows = np.asarray(seqs, dtype=np.int64)
+        new_qsl = None
+    else:
+        rows = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seqs]).astype(np.int64) if seqs else \
+            np.zeros(0, np.int64)
+        new_qsl = np.concatenate([[0], np.cumsum([qsl[s + 1] - qsl[s] for s in seqs])]).astype(np.int32)
+    slots = batch.slot_mapping[rows]
+    blk = np.where(slots >= 0, slots // B, 0)
+    remap = np.array([index.get(int(b), -1) for b in blk], dtype=np.int64)
+    new_slots = np.where((slots >= 0) & (remap >= 0), remap * B + np.where(slots >= 0, slots % B, 0), -1)
+    return DecodeBatch(
+        name=batch.name + "-sample", dtype=batch.dtype, num_heads=batch.num_heads, num_kv_heads=batch.num_kv_heads,
+        head_dim=batch.head_dim, block_size=B, scale=batch.scale, query=batch.query[rows],
+        key_cache=batch.key_cache[old], value_cache=batch.value_cache[old], block_tables=tables,
+        context_lens=ctx.astype(np.int32), slot_mapping=new_slots.astype(np.int64),
+        new_key=batch.new_key[rows], new_value=batch.new_value[rows], partition_size=batch.partition_size,
+        meta=dict(batch.meta, sample_of=batch.name, sample_seqs=seqs), query_start_loc=new_qsl)
+
+
 def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
                 head_dim: int, block_size: int, dtype: str, num_blocks: int | None = None,
                 pool_factor: float = 1.0, shared_prefix_tokens: int = 0,
@@ -237,17 +333,7 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
         pos += n
 
     H, Hkv, D = num_heads, num_kv_heads, head_dim
-    qrng = np.random.default_rng([seed, _S_QUERY])
-    if query_lens is None:
-        qlen = (ctx > 0).astype(np.int64)
-        qsl = None
-        query = round_f32_to(qrng.standard_normal((S, H, D), dtype=np.float32), dtype)
-    else:
-        qlen = np.asarray(query_lens, dtype=np.int64)
-        if qlen.shape != ctx.shape or (qlen < 0).any() or (qlen > ctx).any():
-            raise ValueError("query_lens must give 0 <= q_s <= ctx_s per sequence")
-        qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
-        query = round_f32_to(qrng.standard_normal((int(qsl[-1]), H, D), dtype=np.float32), dtype)
+    qlen, qsl, query = _draw_queries(seed, ctx, query_lens, H, D, dtype)
 
     threads = threads or max(1, min(32, os.cpu_count() or 1))
     shape = (num_blocks, Hkv, B, D)
@@ -264,24 +350,7 @@ def build_batch(*, seed: int, context_lens, num_heads: int, num_kv_heads: int,
     kc[bi, :, oi, :] = CANARY[dtype]
     vc[bi, :, oi, :] = CANARY[dtype]
 
-    # one row per new token: sequence s's last qlen[s] positions (decode: row s, or -1 when ctx = 0)
-    rows = S if qsl is None else int(qsl[-1])
-    slot_mapping = np.full(rows, -1, dtype=np.int64)
-    new_key = np.zeros((rows, Hkv, D), dtype=np.uint16)
-    new_value = np.zeros((rows, Hkv, D), dtype=np.uint16)
-    for s in range(S):
-        c, n = int(ctx[s]), int(qlen[s])
-        r0 = s if qsl is None else int(qsl[s])
-        for i in range(n):
-            p = c - n + i
-            phys = int(tables[s, p // B])
-            off = p % B
-            slot_mapping[r0 + i] = phys * B + off
-            new_key[r0 + i] = kc[phys, :, off, :]
-            new_value[r0 + i] = vc[phys, :, off, :]
-    live = slot_mapping[slot_mapping >= 0]
-    if len(np.unique(live)) != len(live):
-        raise ValueError("two sequences write the same slot")
+    slot_mapping, new_key, new_value = _new_tokens(ctx, qlen, qsl, tables, kc, vc, B)
 
     return DecodeBatch(
         name=name, dtype=dtype, num_heads=H, num_kv_heads=Hkv, head_dim=D, block_size=B,

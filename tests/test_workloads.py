@@ -154,3 +154,40 @@ def test_algorithmic_bytes():
     b = W.build_batch(seed=6, context_lens=[10, 20], num_heads=4, num_kv_heads=2, head_dim=64,
                       block_size=16, dtype=F16)
     assert W.algorithmic_kv_bytes(b) == 30 * 2 * 64 * 2 * 2
+
+
+@pytest.mark.parametrize("q", [None, 1, 3, 40])
+def test_with_query_lens_equals_a_rebuilt_batch(q):
+    """The bench derives multi-query batches from an already built pool; they must be the batches that
+    building with query_len gives."""
+    base = W.make_config(4, max_seqs=6)
+    rebuilt = W.make_config(4, max_seqs=6, query_len=q)
+    derived = W.with_query_lens(base, None if q is None else np.minimum(base.context_lens, q))
+    for f in ("query", "key_cache", "value_cache", "block_tables", "context_lens", "slot_mapping", "new_key",
+              "new_value"):
+        assert np.array_equal(getattr(rebuilt, f), getattr(derived, f)), f
+    if q is None:
+        assert derived.query_start_loc is None
+    else:
+        assert np.array_equal(rebuilt.query_start_loc, derived.query_start_loc)
+
+
+def test_sub_batch_keeps_each_sequence_and_compacts_the_pool():
+    b = W.make_config(4, max_seqs=5, query_len=3)  # shared prefix: blocks used by several sequences
+    sb = W.sub_batch(b, [4, 1])
+    B = b.block_size
+    assert sb.num_seqs == 2 and list(sb.context_lens) == [b.context_lens[4], b.context_lens[1]]
+    used = sb.block_tables[sb.block_tables >= 0]
+    assert sorted(set(used.tolist())) == list(range(sb.num_blocks))  # every compact block is used
+    for i, s in enumerate([4, 1]):
+        n = -(-int(b.context_lens[s]) // B)
+        for j in range(n):  # same bits behind every logical block
+            assert np.array_equal(sb.key_cache[sb.block_tables[i, j]], b.key_cache[b.block_tables[s, j]])
+            assert np.array_equal(sb.value_cache[sb.block_tables[i, j]], b.value_cache[b.block_tables[s, j]])
+        rows = np.arange(b.query_start_loc[s], b.query_start_loc[s + 1])
+        got = np.arange(sb.query_start_loc[i], sb.query_start_loc[i + 1])
+        assert np.array_equal(sb.query[got], b.query[rows])
+        # the new tokens' slots point at the same (logical) positions
+        for r_new, r_old in zip(got, rows):
+            so, sn = int(b.slot_mapping[r_old]), int(sb.slot_mapping[r_new])
+            assert np.array_equal(sb.key_cache[sn // B, :, sn % B], b.key_cache[so // B, :, so % B])
