@@ -75,7 +75,13 @@ def parse_args():
                          "attended once for the whole batch, then each tail, then a merge")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="wall-time budget of the CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-time budget of the CPU baseline on all host cores (half of it again single-threaded)")
+    ap.add_argument("--no-suite", action="store_true",
+                    help="skip the other workloads (the default run also times workloads 1, 3, 4, 5, the FP8 cache "
+                         "and multi-query steps, each in its own timed region, into the line's workloads object)")
+    ap.add_argument("--suite-steps", type=int, default=200, help="timed steps of each suite entry")
+    ap.add_argument("--suite-cpu-seconds", type=float, default=1.5, help="CPU oracle budget of each suite entry")
     return ap.parse_args()
 
 
@@ -240,6 +246,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_id: str):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -247,7 +254,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         self.windows = []
@@ -281,14 +288,18 @@ class ClockSampler:
         return rows
 
     @staticmethod
-    def summarise(rows, t0, t1):
-        inside = [r for r in rows if t0 - 0.15 <= r["ts"] <= t1 + 0.15]
-        used = inside or sorted(rows, key=lambda r: min(abs(r["ts"] - t0), abs(r["ts"] - t1)))[:3]
+    def summarise(rows, t0, t1, margin: float = 0.25):
+        """Clocks of a timed region: the samples taken inside it, or, when fewer than 3 fall inside (a region
+        of a few ms), every sample within ``margin`` seconds of it, labelled so."""
+        inside = [r for r in rows if t0 <= r["ts"] <= t1]
+        near = [r for r in rows if t0 - margin <= r["ts"] <= t1 + margin]
+        used, window = (inside, "timed region") if len(inside) >= 3 else (near, f"timed region +- {margin} s")
         if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
         reasons = sorted({x for r in used for x in r["reasons"]})
         return {"sm_mhz": statistics.median(r["sm"] for r in used), "sm_max_mhz": max(r["smax"] for r in used),
-                "reasons": reasons, "samples": len(inside)}
+                "sm_mhz_min": min(r["sm"] for r in used), "reasons": reasons, "samples": len(used),
+                "samples_inside": len(inside), "window": window}
 
 
 def gpu_id_for(device) -> str:
@@ -313,8 +324,8 @@ def oracle_fp8_pools(batch, scale: float):
 
     import oracle
 
-    vals = oracle.widen_np(np.arange(65536, dtype=np.uint32).astype(np.uint16), batch.dtype).astype(np.float32)
     with np.errstate(invalid="ignore", over="ignore"):
+        vals = oracle.widen_np(np.arange(65536, dtype=np.uint32).astype(np.uint16), batch.dtype).astype(np.float32)
         lut = oracle.e4m3_encode_np(vals / np.float32(scale))
     return lut[batch.key_cache], lut[batch.value_cache]
 
@@ -463,8 +474,378 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, dist):
+class Case:
+    """One timed configuration: a batch resident on the device and the library calls of its step (the
+    cache write of the step's new tokens, then the attention call)."""
+
+    def __init__(self, batch, config: int, dev, *, fp8=False, shared=False, partition_size=0, mq_tile="auto",
+                 path=None):
+        import numpy as np
+        import torch
+
+        from paged_kv_cache_91_gb300 import binding
+        from paged_kv_cache_91_gb300 import workloads as W
+
+        self.binding = binding
+        self.batch, self.config, self.dev = batch, config, dev
+        self.fp8, self.shared, self.P = fp8, shared, partition_size
+        self.mq = batch.query_start_loc is not None
+        self.mq_tile, self.path = mq_tile, path
+        if shared and (self.mq or config != 4):
+            raise SystemExit("--shared-prefix runs workload 4 (one query token per sequence)")
+        self.apply_settings()
+        t = W.as_torch(batch, dev)
+        self.t = t
+        self.max_query_len = int(np.diff(batch.query_start_loc).max()) if self.mq else 1
+        self.n_query_rows = int(batch.query_start_loc[-1]) if self.mq else batch.num_seqs
+        self.out = torch.empty_like(t["query"])
+        self.mcl = batch.max_context_len
+        if shared:
+            # the call's own inputs: the common prefix's blocks, then each sequence's tail table and length
+            pb, tails, tail_lens = W.split_shared_prefix(batch, SHARED_PREFIX_TOKENS)
+            self.prefix_dev = torch.from_numpy(pb).to(dev)
+            t["block_tables"] = torch.from_numpy(tails).to(dev)
+            t["context_lens"] = torch.from_numpy(tail_lens).to(dev)
+            self.max_tail = int(tail_lens.max())
+            ws_bytes = binding.paged_attention_shared_prefix_workspace_size(
+                batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+                SHARED_PREFIX_TOKENS, self.max_tail)
+        elif self.mq:
+            ws_bytes = binding.paged_attention_multi_query_workspace_size(
+                self.n_query_rows, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+                self.mcl, partition_size)
+        else:
+            wsize = binding.paged_attention_workspace_size_fp8 if fp8 else binding.paged_attention_workspace_size
+            ws_bytes = wsize(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
+                             self.mcl, partition_size)
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.nparts = -(-self.mcl // (partition_size or default_partition(fp8, self.mq, batch.block_size)))
+        self.launches_per_step = 2 + (1 if self.nparts > 1 else 0)
+        self.cache_bytes = 1 if fp8 else 2
+        self.kv_bytes, self.call_bytes = step_bytes(batch, partition_size, self.cache_bytes)
+        if shared:
+            self.launches_per_step = 4  # write, prefix, tails, merge
+            self.call_bytes = shared_prefix_call_bytes(batch, SHARED_PREFIX_TOKENS, ws_bytes, self.cache_bytes)
+        self.unique_kv_bytes = (W.unique_kv_bytes(batch) * self.cache_bytes // batch.elem_bytes
+                                if batch.meta.get("shared_prefix_tokens") else self.kv_bytes)
+        if fp8:
+            # the FP8 pool: every slot of the 16-bit pool quantized by the library's own write (setup, untimed)
+            NB, Hkv, B, D = t["key_cache"].shape
+            kc, vc = (torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=dev) for _ in range(2))
+            all_slots = torch.arange(NB * B, dtype=torch.int64, device=dev)
+            binding.paged_kv_write_fp8(t["key_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                                       t["value_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D), kc, vc,
+                                       all_slots, FP8_SCALE, FP8_SCALE, stream=self.stream)
+            torch.cuda.synchronize()
+            del all_slots
+            t["key_cache"], t["value_cache"] = kc, vc
+
+    def apply_settings(self):
+        b = self.binding
+        b.set_multi_query_tile({"auto": b.MQ_TILE_AUTO, "columns": b.MQ_TILE_COLUMNS, "rows": b.MQ_TILE_ROWS,
+                                "tensor": b.MQ_TILE_TENSOR, "pairs": b.MQ_TILE_PAIRS}[self.mq_tile])
+        b.set_decode_path({None: b.DECODE_AUTO, "partitioned": b.DECODE_PARTITIONED,
+                           "persistent": b.DECODE_PERSISTENT}[self.path])
+
+    def write(self, nk, nv, sm):
+        b, t = self.binding, self.t
+        if self.fp8:
+            b.paged_kv_write_fp8(nk, nv, t["key_cache"], t["value_cache"], sm, FP8_SCALE, FP8_SCALE,
+                                 stream=self.stream)
+        else:
+            b.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=self.stream)
+
+    def decode(self, q, bt, cl, o, qsl=None):
+        b, t, batch, P, ws, st = self.binding, self.t, self.batch, self.P, self.ws, self.stream
+        kc, vc = t["key_cache"], t["value_cache"]
+        if self.shared and self.fp8:  # bt, cl: the tail tables and lengths
+            b.paged_attention_decode_shared_prefix_fp8(o, q, kc, vc, self.prefix_dev, SHARED_PREFIX_TOKENS, bt, cl,
+                                                       batch.scale, FP8_SCALE, FP8_SCALE,
+                                                       max_tail_len=self.max_tail, workspace=ws, stream=st)
+        elif self.shared:
+            b.paged_attention_decode_shared_prefix(o, q, kc, vc, self.prefix_dev, SHARED_PREFIX_TOKENS, bt, cl,
+                                                   batch.scale, max_tail_len=self.max_tail, workspace=ws, stream=st)
+        elif self.mq and self.fp8:
+            b.paged_attention_multi_query_fp8(o, q, kc, vc, bt, cl, qsl, batch.scale, FP8_SCALE, FP8_SCALE,
+                                              max_query_len=self.max_query_len, max_context_len=self.mcl,
+                                              partition_size=P, workspace=ws, stream=st)
+        elif self.mq:
+            b.paged_attention_multi_query(o, q, kc, vc, bt, cl, qsl, batch.scale, max_query_len=self.max_query_len,
+                                          max_context_len=self.mcl, partition_size=P, workspace=ws, stream=st)
+        elif self.fp8:
+            b.paged_attention_decode_fp8(o, q, kc, vc, bt, cl, batch.scale, FP8_SCALE, FP8_SCALE,
+                                         max_context_len=self.mcl, partition_size=P, workspace=ws, stream=st)
+        else:
+            b.paged_attention_decode(o, q, kc, vc, bt, cl, batch.scale, max_context_len=self.mcl, partition_size=P,
+                                     workspace=ws, stream=st)
+
+    def step(self, q, nk, nv, sm, bt, cl, o, qsl=None):
+        self.write(nk, nv, sm)
+        self.decode(q, bt, cl, o, qsl)
+
+    def device_args(self):
+        t = self.t
+        return (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"], t["context_lens"],
+                self.out, t.get("query_start_loc"))
+
+    def time_device(self, K: int, warmup: int, dist):
+        """K steps with every input resident in HBM: events around the whole region, around each attention
+        call and before each write, all on the launching stream."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        for _ in range(warmup):
+            self.step(*self.device_args())
+        torch.cuda.synchronize()
+        self.binding.device_errors(clear=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t_wall0 = time.time()
+        start.record(st)
+        for k in range(K):
+            ev_w[k].record(st)
+            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+            ev[k][0].record(st)
+            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+            ev[k][1].record(st)
+        end.record(st)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t_wall1 = time.time()
+        total_ms = dist.max(start.elapsed_time(end))
+        return dict(total_ms=total_ms, call_ms=statistics.fmean(a.elapsed_time(b) for a, b in ev),
+                    write_ms=statistics.fmean(w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)),
+                    t0=t_wall0, t1=t_wall1, errors=self.binding.device_errors(clear=True))
+
+    def time_e2e(self, K: int, warmup: int, dist):
+        """The same step through the public API with the step's inputs copied from pinned host memory and
+        the output read back, every step. The pool stays resident: it is the cache."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        host = {k: t[k].cpu().pin_memory() for k in ("query", "new_key", "new_value", "slot_mapping",
+                                                      "block_tables", "context_lens")
+                + (("query_start_loc",) if self.mq else ())}
+        dbuf = {k: torch.empty_like(t[k]) for k in host}
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            self.step(dbuf["query"], dbuf["new_key"], dbuf["new_value"], dbuf["slot_mapping"], dbuf["block_tables"],
+                      dbuf["context_lens"], self.out, dbuf.get("query_start_loc"))
+            out_h.copy_(self.out, non_blocking=True)
+
+        for _ in range(warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(st)
+        for _ in range(K):
+            e2e_step()
+        s1.record(st)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = dist.max(s0.elapsed_time(s1))
+        return dict(ms=e2e_ms / K, h2d=int(h2d), d2h=int(d2h))
+
+    def kernel_kind(self) -> str:
+        G = self.batch.num_heads // self.batch.num_kv_heads
+        if self.mq:
+            kind = "mq_fp8" if self.fp8 else "mq"
+            if mq_summary(self.batch, self.mq_tile, 1.0, self.fp8)["tile"] == "pairs":
+                kind = "mq_fp8_pairs"
+            return kind
+        if self.fp8:
+            return "mma_fp8" if G <= 8 and self.batch.head_dim == 128 else "simt_fp8"
+        return "mma" if 2 <= G <= 8 else "simt"
+
+    def workload_key(self) -> str:
+        return (f"cfg{self.config}" + ("-fp8" if self.fp8 else "")
+                + (f"-q{self.max_query_len}" if self.mq else "") + ("-shared" if self.shared else ""))
+
+    def call_name(self) -> str:
+        if self.shared:
+            return "paged_attention_decode_shared_prefix" + ("_fp8" if self.fp8 else "")
+        if self.mq:
+            return "paged_attention_multi_query" + ("_fp8" if self.fp8 else "")
+        return "paged_attention_decode" + ("_fp8" if self.fp8 else "")
+
+    def roofline(self, call_ms: float):
+        peak, peak_kind = hbm_peak()
+        # a shared-prefix batch must bring each shared block from HBM once: its roofline counts unique bytes
+        hbm_bytes = self.call_bytes - (self.kv_bytes - self.unique_kv_bytes) if not self.shared else self.call_bytes
+        achieved = hbm_bytes / (call_ms / 1e3) / 1e9
+        what = ("prefix, tail and merge kernels; bytes: the prefix once, the tails, q, out, partials" if self.shared
+                else ("multi-query kernel" if self.mq else "decode kernel")
+                + (" + log-sum-exp reduce" if self.nparts > 1 else ""))
+        traffic = None if self.shared else ncu_traffic(self.workload_key(), self.kernel_kind())
+        return {"bound": "hbm", "kernel": f"{self.call_name()} ({what})", "achieved": round(achieved, 2),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4), "traffic": traffic,
+                "algorithmic_bytes_per_call": int(hbm_bytes), "avg_call_ms": round(call_ms, 4),
+                "kernel_hash": kernel_hash(self.kernel_kind())}
+
+    def close(self):
+        import torch
+
+        self.t.clear()
+        self.out = self.ws = None
+        torch.cuda.empty_cache()
+
+
+SPEC_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth
+
+
+def cpu_oracle(batch, budget_s: float, threads: int, fp8: bool, seed: int = 7):
+    """The oracle, as it stands, on a seeded random sample of the batch's sequences (compact pool, all heads,
+    every query row), repeated until budget_s. Returns a cpu_baseline dict: KV GB/s of the sample's contexts,
+    the threads used and what the sample was."""
     import numpy as np
+
+    import oracle
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    S = batch.num_seqs
+    order = np.random.default_rng(seed).permutation(S).tolist()
+    cb = 1 if fp8 else 2
+
+    def run(sb):
+        kc, vc, sc = sb.key_cache, sb.value_cache, 1.0
+        if fp8:
+            kc, vc = oracle_fp8_pools(sb, FP8_SCALE)
+            sc = FP8_SCALE
+        t0 = time.perf_counter()
+        if sb.query_start_loc is None:
+            oracle.decode_c(sb.query, kc, vc, sb.block_tables, sb.context_lens, sb.scale, sb.dtype,
+                            num_threads=threads, k_scale=sc, v_scale=sc)
+        else:
+            oracle.multi_query_c(sb.query, kc, vc, sb.block_tables, sb.context_lens, sb.query_start_loc, sb.scale,
+                                 sb.dtype, num_threads=threads, k_scale=sc, v_scale=sc)
+        return time.perf_counter() - t0
+
+    # size the sample from one sequence's time, so that one pass takes about a third of the budget
+    one = W.sub_batch(batch, order[:1])
+    t_one = max(run(one), 1e-4) / max(1, sample_kv_bytes(one, [0], cb))
+    n = 1
+    while n < S and sample_kv_bytes(batch, order[:n + 1], cb) * t_one < budget_s / 3:
+        n += 1
+    seqs = sorted(order[:n])
+    sb = W.sub_batch(batch, seqs)
+    el, reps = 0.0, 0
+    while reps == 0 or el < budget_s:
+        el += run(sb)
+        reps += 1
+    kv = sample_kv_bytes(batch, seqs, cb)
+    rows = int(sb.query_start_loc[-1]) if sb.query_start_loc is not None else n
+    return {"value": round(kv * reps / el / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {S} sequences ({rows} query rows x {batch.num_heads} heads), drawn at random, "
+                      f"{reps} pass(es), fp64, {el:.1f} s"}
+
+
+def entry_summary(case: Case, dev_t, e2e_t, clocks, cpu, steps: int):
+    """One workload's figures: per-call and per-step times, KV GB/s, roofline, e2e, clocks, CPU oracle."""
+    b = case.batch
+    step_s = dev_t["total_ms"] / steps / 1e3
+    e = {
+        "workload": workload_config(b, case.config, case.P, int(b.key_cache.nbytes * case.cache_bytes // 2),
+                                    case.fp8)["workload"],
+        "call": case.call_name(), "cache_dtype": "e4m3" if case.fp8 else b.dtype, "steps": steps,
+        "ms_per_step": round(dev_t["total_ms"] / steps, 4), "call_ms": round(dev_t["call_ms"], 4),
+        "write_call_ms": round(dev_t["write_ms"], 4), "new_tokens_per_step": int((b.slot_mapping >= 0).sum()),
+        "kv_gbs": round(case.kv_bytes / step_s / 1e9, 2), "kv_bytes_per_step": int(case.kv_bytes),
+        "tokens_per_s": round(case.n_query_rows / step_s, 1),
+        "roofline": case.roofline(dev_t["call_ms"]),
+        "e2e": None if e2e_t is None else {
+            "value": round(case.kv_bytes / (e2e_t["ms"] / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(e2e_t["ms"], 4), "h2d_bytes_per_step": e2e_t["h2d"],
+            "d2h_bytes_per_step": e2e_t["d2h"]},
+        "gpu_launches_per_step": case.launches_per_step, "clocks": clocks, "device_errors": dev_t["errors"],
+        "cpu_baseline": cpu,
+    }
+    if case.unique_kv_bytes != case.kv_bytes:
+        e["unique_kv_bytes_per_step"] = int(case.unique_kv_bytes)
+        e["kv_gbs_note"] = "kv_gbs counts every sequence's prefix (logical bytes; repeats come from L2)"
+    if case.mq:
+        e["multi_query"] = mq_summary(b, case.mq_tile, dev_t["call_ms"], case.fp8)
+    if b.num_seqs <= 4:  # the tiny batch is launch-bound: its figures are latencies
+        e["us_per_step"] = round(1e3 * dev_t["total_ms"] / steps, 2)
+        e["call_us"] = round(1e3 * dev_t["call_ms"], 2)
+        e["write_us"] = round(1e3 * dev_t["write_ms"], 2)
+        if e2e_t is not None:
+            e["e2e"]["us_per_step"] = round(1e3 * e2e_t["ms"], 2)
+    return e
+
+
+# The workloads the default run measures beside the headline: (key, config, options). Each is timed with
+# its own events; multi-query batches reuse the pool of their workload.
+SUITE = [
+    ("w2_fp8", 2, {"fp8": True}),
+    ("w2_q4", 2, {"query_len": 4}),
+    ("w2_q128", 2, {"query_len": 128}),
+    ("w2_q128_fp8", 2, {"query_len": 128, "fp8": True}),
+    ("w1_tiny", 1, {}),
+    ("w3_gqa_bf16", 3, {}),
+    ("w3_fp8", 3, {"fp8": True}),
+    ("w3_q32", 3, {"query_len": 32}),
+    ("w3_q4_fp8", 3, {"query_len": 4, "fp8": True}),
+    ("w3_q32_fp8", 3, {"query_len": 32, "fp8": True}),
+    ("w4_shared_prefix", 4, {}),
+    ("w4_shared_prefix_call", 4, {"shared": True}),
+    ("w4_fp8", 4, {"fp8": True}),
+    ("w5_long_split_k", 5, {}),
+    ("w5_fp8", 5, {"fp8": True}),
+]
+
+
+def run_suite(args, dist, dev, base_batch):
+    """Every other workload, one after another, each with its own timed region (args.suite_steps steps)."""
+    import numpy as np
+
+    from paged_kv_cache_91_gb300 import workloads as W
+
+    results = {}
+    # one workload's pool at a time in host memory; the headline's batch serves the suite's entries of its
+    # workload, which come first
+    batches = {args.config: base_batch} if args.max_seqs is None and args.block_size == 16 else {}
+    cpu_on = dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
+    for key, n, opt in SUITE:
+        if n not in batches:
+            batches = {n: W.make_config(n)}
+        batch = batches[n]
+        if opt.get("query_len"):
+            batch = W.with_query_lens(batch, np.minimum(batch.context_lens, opt["query_len"]))
+        case = Case(batch, n, dev, fp8=opt.get("fp8", False), shared=opt.get("shared", False))
+        K = args.suite_steps
+        dev_t = case.time_device(K, args.warmup, dist)
+        e2e_t = None if args.no_e2e else case.time_e2e(K, args.warmup, dist)
+        cpu = cpu_oracle(batch, args.suite_cpu_seconds, _all_cores(), case.fp8) if cpu_on else None
+        results[key] = entry_summary(case, dev_t, e2e_t, None, cpu, K)
+        results[key]["_window"] = (dev_t["t0"], dev_t["t1"])
+        case.close()
+    return results
+
+
+def _all_cores() -> int:
+    import oracle
+
+    try:
+        n = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        n = os.cpu_count() or 1
+    return max(1, min(n, oracle.max_threads()))
+
+
+def run_ours(args, dist):
     import torch
 
     from paged_kv_cache_91_gb300 import binding
@@ -475,240 +856,72 @@ def run_ours(args, dist):
     binding.load()
     batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size,
                           query_len=args.query_len)
-    P = args.partition_size
-    t = W.as_torch(batch, dev)
-    mq = args.query_len is not None
-    max_query_len = int(np.diff(batch.query_start_loc).max()) if mq else 1
-    n_query_rows = int(batch.query_start_loc[-1]) if mq else batch.num_seqs  # query tokens per step
-    out = torch.empty_like(t["query"])
-    mcl = batch.max_context_len
-    binding.set_multi_query_tile({"auto": binding.MQ_TILE_AUTO, "columns": binding.MQ_TILE_COLUMNS,
-                                  "rows": binding.MQ_TILE_ROWS, "tensor": binding.MQ_TILE_TENSOR,
-                                  "pairs": binding.MQ_TILE_PAIRS}[args.mq_tile])
-    if args.path:
-        binding.set_decode_path({"partitioned": binding.DECODE_PARTITIONED,
-                                 "persistent": binding.DECODE_PERSISTENT}[args.path])
-    fp8 = args.kv_dtype == "fp8_e4m3"
-    shared = args.shared_prefix
-    if shared:
-        if mq or args.config != 4:
-            raise SystemExit("--shared-prefix runs workload 4 (one query token per sequence)")
-        # the call's own inputs: the common prefix's blocks, then each sequence's tail table and length
-        pb, tails, tail_lens = W.split_shared_prefix(batch, SHARED_PREFIX_TOKENS)
-        prefix_dev = torch.from_numpy(pb).to(dev)
-        t["block_tables"] = torch.from_numpy(tails).to(dev)
-        t["context_lens"] = torch.from_numpy(tail_lens).to(dev)
-        max_tail = int(tail_lens.max())
-    if shared:
-        ws_bytes = binding.paged_attention_shared_prefix_workspace_size(
-            batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
-            SHARED_PREFIX_TOKENS, max_tail)
-    elif mq:
-        ws_bytes = binding.paged_attention_multi_query_workspace_size(
-            int(batch.query_start_loc[-1]), batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
-            mcl, P)
-    else:
-        wsize = binding.paged_attention_workspace_size_fp8 if fp8 else binding.paged_attention_workspace_size
-        ws_bytes = wsize(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size,
-                         mcl, P)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    nparts = -(-mcl // (P or default_partition(fp8, mq, batch.block_size)))
-    launches_per_step = 2 + (1 if nparts > 1 else 0)
-    cache_bytes = 1 if fp8 else 2
-    kv_bytes, call_bytes = step_bytes(batch, P, cache_bytes)
-    if shared:
-        launches_per_step = 4  # write, prefix, tails, merge
-        call_bytes = shared_prefix_call_bytes(batch, SHARED_PREFIX_TOKENS, ws_bytes, cache_bytes)
-    if fp8:
-        # the FP8 pool: every slot of the 16-bit pool quantized by the library's own write (setup, untimed)
-        NB, Hkv, B, D = t["key_cache"].shape
-        kc, vc = (torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=dev) for _ in range(2))
-        all_slots = torch.arange(NB * B, dtype=torch.int64, device=dev)
-        binding.paged_kv_write_fp8(t["key_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D),
-                                   t["value_cache"].permute(0, 2, 1, 3).reshape(NB * B, Hkv, D), kc, vc, all_slots,
-                                   FP8_SCALE, FP8_SCALE, stream=stream)
-        torch.cuda.synchronize()
-        del all_slots
-        t["key_cache"], t["value_cache"] = kc, vc
-
-    def write(nk, nv, sm):
-        if fp8:
-            binding.paged_kv_write_fp8(nk, nv, t["key_cache"], t["value_cache"], sm, FP8_SCALE, FP8_SCALE,
-                                       stream=stream)
-        else:
-            binding.paged_kv_write(nk, nv, t["key_cache"], t["value_cache"], sm, stream=stream)
-
-    def decode(q, bt, cl, o, qsl=None):
-        if shared and fp8:  # bt, cl: the tail tables and lengths
-            binding.paged_attention_decode_shared_prefix_fp8(o, q, t["key_cache"], t["value_cache"], prefix_dev,
-                                                             SHARED_PREFIX_TOKENS, bt, cl, batch.scale, FP8_SCALE,
-                                                             FP8_SCALE, max_tail_len=max_tail, workspace=ws,
-                                                             stream=stream)
-        elif shared:
-            binding.paged_attention_decode_shared_prefix(o, q, t["key_cache"], t["value_cache"], prefix_dev,
-                                                         SHARED_PREFIX_TOKENS, bt, cl, batch.scale,
-                                                         max_tail_len=max_tail, workspace=ws, stream=stream)
-        elif mq and fp8:
-            binding.paged_attention_multi_query_fp8(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
-                                                    FP8_SCALE, FP8_SCALE, max_query_len=max_query_len,
-                                                    max_context_len=mcl, partition_size=P, workspace=ws,
-                                                    stream=stream)
-        elif mq:
-            binding.paged_attention_multi_query(o, q, t["key_cache"], t["value_cache"], bt, cl, qsl, batch.scale,
-                                                max_query_len=max_query_len, max_context_len=mcl, partition_size=P,
-                                                workspace=ws, stream=stream)
-        elif fp8:
-            binding.paged_attention_decode_fp8(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
-                                               FP8_SCALE, FP8_SCALE, max_context_len=mcl, partition_size=P,
-                                               workspace=ws, stream=stream)
-        else:
-            binding.paged_attention_decode(o, q, t["key_cache"], t["value_cache"], bt, cl, batch.scale,
-                                           max_context_len=mcl, partition_size=P, workspace=ws, stream=stream)
-
-    def step(q, nk, nv, sm, bt, cl, o, qsl=None):
-        write(nk, nv, sm)
-        decode(q, bt, cl, o, qsl)
-
-    args_dev = (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"],
-                t["context_lens"], out, t.get("query_start_loc"))
+    case = Case(batch, args.config, dev, fp8=args.kv_dtype == "fp8_e4m3", shared=args.shared_prefix,
+                partition_size=args.partition_size, mq_tile=args.mq_tile, path=args.path)
     sampler = ClockSampler(gpu_id_for(dev))
-    for _ in range(args.warmup):
-        step(*args_dev)
-    torch.cuda.synchronize()
-    binding.device_errors(clear=True)
-
-    # --- device-resident timed region
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    dist.barrier()
-    t_wall0 = time.time()
-    start.record(stream)
-    for k in range(K):
-        ev_w[k].record(stream)
-        write(t["new_key"], t["new_value"], t["slot_mapping"])
-        ev[k][0].record(stream)
-        decode(t["query"], t["block_tables"], t["context_lens"], out, t.get("query_start_loc"))
-        ev[k][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    t_wall1 = time.time()
-    total_ms = start.elapsed_time(end)
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-    write_ms = [w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)]
-    total_ms = dist.max(total_ms)
-    dec_avg_ms = statistics.fmean(decode_ms)
-    errors = binding.device_errors(clear=True)
-
-    # --- end to end through the public API, inputs from pinned host memory
-    e2e = None
-    if not args.no_e2e:
-        host = {k: t[k].cpu().pin_memory() for k in ("query", "new_key", "new_value", "slot_mapping",
-                                                      "block_tables", "context_lens")
-                + (("query_start_loc",) if mq else ())}
-        dbuf = {k: torch.empty_like(t[k]) for k in host}
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = out_h.numel() * out_h.element_size()
-
-        def e2e_step():
-            for k, v in host.items():
-                dbuf[k].copy_(v, non_blocking=True)
-            step(dbuf["query"], dbuf["new_key"], dbuf["new_value"], dbuf["slot_mapping"], dbuf["block_tables"],
-                 dbuf["context_lens"], out, dbuf.get("query_start_loc"))
-            out_h.copy_(out, non_blocking=True)
-
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        dist.barrier()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize()
-        dist.barrier()
-        e2e_ms = dist.max(s0.elapsed_time(s1))
-        e2e_val = dist.sum(kv_bytes) * K / (e2e_ms / 1e3) / 1e9
-        e2e = {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / K, 4)}
-
-    rows = sampler.stop()
-    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1)
-
-    total_kv = dist.sum(kv_bytes)
-    value = total_kv * K / (total_ms / 1e3) / 1e9
-    peak, peak_kind = hbm_peak()
-    achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
-    workload = f"cfg{args.config}" + ("-fp8" if fp8 else "") + (f"-q{args.query_len}" if mq else "")
-    G = batch.num_heads // batch.num_kv_heads
-    if mq:
-        kind = "mq_fp8" if fp8 else "mq"
-        if mq_summary(batch, args.mq_tile, 1.0, fp8)["tile"] == "pairs":
-            kind = "mq_fp8_pairs"
-    elif fp8:
-        kind = "mma_fp8" if G <= 8 and batch.head_dim == 128 else "simt_fp8"
-    else:
-        kind = "mma" if 2 <= G <= 8 else "simt"
-    traffic = None if shared else ncu_traffic(workload, kind)
+    dev_t = case.time_device(K, args.warmup, dist)
+    e2e_t = None if args.no_e2e else case.time_e2e(K, args.warmup, dist)
+    total_ms = dev_t["total_ms"]
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        import oracle
+        cores = _all_cores()
+        cpu = cpu_oracle(batch, args.cpu_seconds, cores, case.fp8)
+        single = cpu_oracle(batch, args.cpu_seconds / 2, 1, case.fp8)
+        cpu["single_thread"] = {"value": single["value"], "unit": "GB/s", "cores": 1, "sample": single["sample"]}
+    case.close()
 
-        seqs = list(range(batch.num_seqs))
-        pools = oracle_fp8_pools(batch, FP8_SCALE) if fp8 else None
-        if mq:
-            el, reps = time_oracle_mq(batch, args.cpu_seconds, fp8_pools=pools)
-            what = "multi-query"
-        else:
-            el, reps = time_oracle(batch, seqs, args.cpu_seconds, fp8_pools=pools)
-            what = "decode"
-        cpu = {"value": round(kv_bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
-               "kind": "oracle",
-               "sample": f"{reps} full {what} pass(es) of the workload (all {batch.num_seqs} sequences x "
-                         f"{batch.num_heads} heads), fp64, {el:.1f} s"}
+    suite = None
+    if not args.no_suite and dist.world == 1 and args.query_len is None and not args.shared_prefix \
+            and args.kv_dtype == "auto":
+        suite = run_suite(args, dist, dev, batch)
 
+    rows = sampler.stop()
+    clocks = ClockSampler.summarise(rows, dev_t["t0"], dev_t["t1"])
+    if suite:
+        for e in suite.values():
+            e["clocks"] = ClockSampler.summarise(rows, *e.pop("_window"))
+
+    value = dist.sum(case.kv_bytes) * K / (total_ms / 1e3) / 1e9
+    peak, _ = hbm_peak()
     if dist.rank == 0:
+        b = case.batch
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3" if fp8 else ("f16" if batch.dtype == "f16" else "bf16"),
+            "dtype": "e4m3" if case.fp8 else ("f16" if b.dtype == "f16" else "bf16"),
             "accumulate": "f32", "data": "synthetic (seeded N(0,1) K/V/q, block tables from a shuffled free list)",
-            "config": workload_config(batch, args.config, P, int(batch.key_cache.nbytes * cache_bytes), fp8),
-            "tokens_per_s": round(n_query_rows * dist.world * K / (total_ms / 1e3), 1),
+            "config": workload_config(b, args.config, args.partition_size, int(b.key_cache.nbytes * case.cache_bytes
+                                                                               // 2), case.fp8),
+            "tokens_per_s": round(case.n_query_rows * dist.world * K / (total_ms / 1e3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * value / dist.world / peak, 2),
-                            "spec_8tbs": round(100 * value / dist.world / 8000.0, 2)},
-            "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_shared_prefix" + ("_fp8" if fp8 else "")
-                         + " (prefix, tail and merge "
-                         "kernels; bytes: the prefix once, the tails, q, out, partials)" if shared else
-                         ("paged_attention_multi_query" + ("_fp8" if fp8 else "") if mq else
-                                                    "paged_attention_decode_fp8" if fp8 else "paged_attention_decode")
-                         + (" (multi-query kernel" if mq else " (decode kernel")
-                         + (" + log-sum-exp reduce)" if nparts > 1 else ")"),
-                         "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "algorithmic_bytes_per_call": call_bytes, "avg_call_ms": round(dec_avg_ms, 4)},
-            "write_call_ms": round(statistics.fmean(write_ms), 4),
-            "attention_only_model_tokens_per_s": model_extrapolation(args.config, n_query_rows * dist.world * K
+                            "spec_8tbs": round(100 * value / dist.world / SPEC_HBM_GBS, 2)},
+            "roofline": case.roofline(dev_t["call_ms"]),
+            "write_call_ms": round(dev_t["write_ms"], 4),
+            "attention_only_model_tokens_per_s": model_extrapolation(args.config, case.n_query_rows * dist.world * K
                                                                      / (total_ms / 1e3)),
-            "gpu_launches": K * launches_per_step,
+            "gpu_launches": K * case.launches_per_step,
             "clocks": clocks,
-            "device_errors": errors,
-            "e2e": e2e,
+            "device_errors": dev_t["errors"],
+            "e2e": None if e2e_t is None else {
+                "value": round(dist.sum(case.kv_bytes) / (e2e_t["ms"] / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e_t["h2d"], "d2h_bytes_per_step": e2e_t["d2h"],
+                "ms_per_step": round(e2e_t["ms"], 4)},
             "cpu_baseline": cpu,
         }
-        if mq:
-            line["multi_query"] = mq_summary(batch, args.mq_tile, dec_avg_ms, fp8)
-        if shared:
+        if case.mq:
+            line["multi_query"] = mq_summary(b, args.mq_tile, dev_t["call_ms"], case.fp8)
+        if case.shared:
             line["config"]["call"] = (f"paged_attention_decode_shared_prefix: the {SHARED_PREFIX_TOKENS}-token "
                                       "prefix attended once for the whole batch, then each tail, then a merge")
+        if suite:
+            line["workloads"] = suite
+            line["workloads_note"] = (f"each entry: {args.suite_steps} steps of its own after {args.warmup} warm-up "
+                                      "steps, events on the launching stream; inputs larger than L2 except w1 "
+                                      "(a latency case); cpu_baseline: the oracle on all host cores over a "
+                                      "random sample of the workload's sequences")
         print(json.dumps(line), flush=True)
 
 
