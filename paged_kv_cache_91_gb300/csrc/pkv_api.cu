@@ -151,13 +151,13 @@ __global__ void pkv_write_fp8_kernel(const uint4* __restrict__ key, const uint4*
     const int t = (int)(r / num_kv_heads);
     const size_t src = (((size_t)t * num_kv_heads + h) * pieces_per_row + c) * 2;
     const long long slot = __ldg(slot_mapping + t);
-    const uint4 kv[2] = {__ldg(key + src), __ldg(key + src + 1)};
-    const uint4 vv[2] = {__ldg(value + src), __ldg(value + src + 1)};
-    if (slot < 0) continue;  // padding token
+    if (slot < 0) continue;  // padding token: its rows are not read
     if (slot >= num_slots) {
       if (c == 0 && h == 0) atomicOr(err, PKV_DEVERR_SLOT);
       continue;
     }
+    const uint4 kv[2] = {__ldg(key + src), __ldg(key + src + 1)};
+    const uint4 vv[2] = {__ldg(value + src), __ldg(value + src + 1)};
     const long long blk = slot / block_size, off = slot - blk * block_size;
     const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * pieces_per_row + c;
     key_cache[dst] = quantize16<T>(kv, k_scale);
