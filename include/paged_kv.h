@@ -240,10 +240,15 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
  *     loads the library, held until the process exits.
  *   - The first call on each device (with that device current) looks up the
  *     scratch array's device address with cudaGetSymbolAddress; make that first
- *     call before any stream capture on that device.
+ *     call before any stream capture on that device. The address is kept per
+ *     device ordinal for the life of the process (the device's primary
+ *     context): do not call this entry point on a device after
+ *     cudaDeviceReset there.
  *   - A call whose split-K scratch (paged_attention_workspace_size) exceeds
  *     PKV_STATIC_WORKSPACE_BYTES launches nothing and returns PKV_ERR_WORKSPACE,
- *     with the sizes in pkv_last_error_message().
+ *     with the sizes in pkv_last_error_message(). The other arguments are
+ *     checked first: a bad one returns its own error, as in
+ *     paged_attention_decode.
  *   - Every call on a device shares the one scratch array, which keeps the last
  *     call's contents. Nothing in it needs clearing: each call writes every
  *     partial before reading it. Calls whose kernels overlap on the GPU (other
