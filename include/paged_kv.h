@@ -123,45 +123,11 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
                                   cudaStream_t stream);
 
 /*
- * Decode paths (pkv_set_decode_path). Both compute the same result, up to
- * rounding order.
- *   PKV_DECODE_PERSISTENT  one wave of CTAs. The (sequence, head group, block)
- *                          tiles of the whole batch are split into equal ranges,
- *                          one per warp. A sequence cut by a range boundary
- *                          leaves per-warp partials (m, l, o) that a
- *                          log-sum-exp reduce kernel merges. Needs
- *                          num_seqs <= 2048.
- *   PKV_DECODE_PARTITIONED one CTA per (partition_size tokens of context, head
- *                          group, sequence). Contexts longer than
- *                          partition_size leave one partial per partition,
- *                          merged by the same kind of reduce.
- *   PKV_DECODE_AUTO        the library's choice (default): currently PARTITIONED,
- *                          which measures faster on every workload here.
- */
-#define PKV_DECODE_AUTO 0
-#define PKV_DECODE_PARTITIONED 1
-#define PKV_DECODE_PERSISTENT 2
-
-/*
- * pkv_set_decode_path -- choose the decode path for later calls in this process
- * (PKV_DECODE_*). Returns the previous choice, or -1 for an unknown value
- * (nothing changes). PERSISTENT falls back to PARTITIONED for batches it does
- * not take. The workspace size depends on the path: size workspaces after
- * choosing it.
- */
-int32_t pkv_set_decode_path(int32_t path);
-
-/*
  * paged_attention_workspace_size -- bytes of device workspace that
- * paged_attention_decode needs for its split-K partial results, under the
- * current decode path.
- *
- *   PERSISTENT:  a (num_seqs + 1)-int prefix plus two fp32 partials (m, l and
- *                head_dim outputs for each query head of a group) per warp,
- *                for at most 2048 warps.
- *   PARTITIONED: ceil(max_context_len / partition_size) partitions of
- *                num_heads * (head_dim + 2) fp32 per sequence. The size is 0
- *                when max_context_len <= partition_size (no split).
+ * paged_attention_decode needs for its split-K partial results:
+ * ceil(max_context_len / partition_size) partitions of num_heads *
+ * (head_dim + 2) fp32 per sequence. The size is 0 when max_context_len <=
+ * partition_size (no split).
  *
  * partition_size 0 selects the default, 512. Returns 0 for invalid arguments,
  * which paged_attention_decode then rejects.
@@ -199,9 +165,9 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32
  *   head_dim             64 or 128; block_size 8, 16 or 32
  *   num_heads            a multiple of num_kv_heads (GQA when larger)
  *   partition_size       0 = 512; else a multiple of block_size in
- *                        [block_size, 128 * block_size]; sets the split on
- *                        the PARTITIONED path (the PERSISTENT path splits by
- *                        equal work instead)
+ *                        [block_size, 128 * block_size]: the tokens of one
+ *                        CTA's share of a context (contexts longer than this
+ *                        are split and merged by log-sum-exp)
  *   workspace            paged_attention_workspace_size(...) bytes, 16-byte aligned;
  *                        may be NULL when that size is 0
  *
@@ -518,10 +484,9 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
 
 /*
  * paged_attention_workspace_size_fp8 -- workspace bytes of
- * paged_attention_decode_fp8. The FP8 decode always runs on the PARTITIONED
- * path, whatever pkv_set_decode_path chose, so this is the PARTITIONED size of
- * paged_attention_workspace_size, except that partition_size 0 selects 1024
- * (an FP8 tile carries half the bytes, and longer partitions measure faster).
+ * paged_attention_decode_fp8: the size paged_attention_workspace_size gives,
+ * except that partition_size 0 selects 1024 (an FP8 tile carries half the
+ * bytes, and longer partitions measure faster).
  */
 size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                           int32_t head_dim, int32_t block_size,

@@ -44,8 +44,6 @@ def load():
     lib.paged_kv_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.paged_attention_workspace_size.restype = sz
     lib.paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
-    lib.pkv_set_decode_path.restype = i32
-    lib.pkv_set_decode_path.argtypes = [i32]
     lib.paged_attention_decode.restype = i32
     lib.paged_attention_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, f32, i32, i32, i32, i32, i32, i32,
                                            i32, P, sz, P]
@@ -96,23 +94,37 @@ def _check(lib, status: int) -> None:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    # the argtypes are c_void_p: a Python int (or None) converts without a wrapper object
+    return t.data_ptr() if t is not None else None
 
 
-def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
+# The current stream's handle as an int, without building a torch Stream object (about 2 us per call);
+# torch.cuda.current_stream where that accessor is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(t: torch.Tensor, stream):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(t.get_device())
         stream = torch.cuda.current_stream(t.device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _cuda16(name: str, t: torch.Tensor) -> int:
-    if not t.is_cuda:
-        raise PagedKVError(-1, f"{name} must be a CUDA tensor")
-    if t.dtype not in _DTYPE:
-        raise PagedKVError(-1, f"{name} must be float16 or bfloat16, got {t.dtype}")
-    if not t.is_contiguous():
+    dt = _DTYPE.get(t.dtype)
+    if dt is None or not t.is_cuda or not t.is_contiguous():
+        if not t.is_cuda:
+            raise PagedKVError(-1, f"{name} must be a CUDA tensor")
+        if dt is None:
+            raise PagedKVError(-1, f"{name} must be float16 or bfloat16, got {t.dtype}")
         raise PagedKVError(-1, f"{name} must be contiguous")
-    return _DTYPE[t.dtype]
+    return dt
+
+
+def _cuda_i32(name: str, t: torch.Tensor) -> None:
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise PagedKVError(-1, f"{name} must be a contiguous CUDA int32 tensor")
 
 
 def _cuda_fp8(name: str, t: torch.Tensor) -> None:
@@ -143,17 +155,6 @@ def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tens
         raise PagedKVError(-1, "shape mismatch between key/value, caches and slot_mapping")
     _check(lib, lib.paged_kv_write(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping),
                                    T, Hkv, D, B, NB, dt, _stream(key_cache, stream)))
-
-
-DECODE_AUTO, DECODE_PARTITIONED, DECODE_PERSISTENT = 0, 1, 2
-
-
-def set_decode_path(path: int) -> int:
-    """Choose the decode path for later calls (DECODE_*); returns the previous choice."""
-    prev = int(load().pkv_set_decode_path(int(path)))
-    if prev < 0:
-        raise PagedKVError(-1, f"unknown decode path {path}")
-    return prev
 
 
 def paged_kv_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, block_mapping: torch.Tensor,
@@ -195,9 +196,8 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
         if _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
-    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    _cuda_i32("block_tables", block_tables)
+    _cuda_i32("context_lens", context_lens)
     NB, Hkv, B, D = key_cache.shape
     if block_size is not None and block_size != B:
         raise PagedKVError(-1, f"block_size {block_size} != key_cache.shape[2] {B}")
@@ -211,9 +211,10 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     maxb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = maxb * B
-    need = int(lib.paged_attention_workspace_size(S, H, Hkv, D, B, max_context_len, partition_size))
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    if workspace is None:  # (a workspace passed in is checked against the size by the library)
+        need = int(lib.paged_attention_workspace_size(S, H, Hkv, D, B, max_context_len, partition_size))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib, lib.paged_attention_decode(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
@@ -261,9 +262,8 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
         raise PagedKVError(-1, "out dtype differs from query")
     _cuda_fp8("key_cache", key_cache)
     _cuda_fp8("value_cache", value_cache)
-    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    _cuda_i32("block_tables", block_tables)
+    _cuda_i32("context_lens", context_lens)
     NB, Hkv, B, D = key_cache.shape
     S, H, D2 = query.shape
     if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
@@ -273,9 +273,10 @@ def paged_attention_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache
     maxb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = maxb * B
-    need = int(lib.paged_attention_workspace_size_fp8(S, H, Hkv, D, B, max_context_len, partition_size))
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    if workspace is None:
+        need = int(lib.paged_attention_workspace_size_fp8(S, H, Hkv, D, B, max_context_len, partition_size))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib, lib.paged_attention_decode_fp8(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
@@ -314,10 +315,9 @@ def _multi_query(out, query, key_cache, value_cache, block_tables, context_lens,
             _cuda_fp8(n, t)
         elif _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
-    for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
-                 ("query_start_loc", query_start_loc)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    _cuda_i32("block_tables", block_tables)
+    _cuda_i32("context_lens", context_lens)
+    _cuda_i32("query_start_loc", query_start_loc)
     NB, Hkv, B, D = key_cache.shape
     T, H, D2 = query.shape
     S = context_lens.shape[0]
@@ -330,9 +330,11 @@ def _multi_query(out, query, key_cache, value_cache, block_tables, context_lens,
         max_context_len = maxb * B
     if max_query_len is None:
         max_query_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
-    need = int(lib.paged_attention_multi_query_workspace_size(T, H, Hkv, D, B, max_context_len, partition_size))
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    if workspace is None:
+        need = int(lib.paged_attention_multi_query_workspace_size(T, H, Hkv, D, B, max_context_len,
+                                                                  partition_size))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     head = (_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), maxb,
             _ptr(context_lens), _ptr(query_start_loc), S, T, int(max_query_len), int(max_context_len), float(scale),
@@ -389,9 +391,9 @@ def _shared_prefix(out, query, key_cache, value_cache, prefix_blocks, prefix_len
             _cuda_fp8(n, t)
         elif _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
-    for n, t in (("prefix_blocks", prefix_blocks), ("block_tables", block_tables), ("tail_lens", tail_lens)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    _cuda_i32("prefix_blocks", prefix_blocks)
+    _cuda_i32("block_tables", block_tables)
+    _cuda_i32("tail_lens", tail_lens)
     NB, Hkv, B, D = key_cache.shape
     S, H, D2 = query.shape
     if D2 != D or out.shape != query.shape or value_cache.shape != key_cache.shape:
@@ -401,8 +403,8 @@ def _shared_prefix(out, query, key_cache, value_cache, prefix_blocks, prefix_len
     maxb = block_tables.shape[1]
     if max_tail_len is None:
         max_tail_len = maxb * B
-    need = paged_attention_shared_prefix_workspace_size(S, H, Hkv, D, B, int(prefix_len), int(max_tail_len))
     if workspace is None:
+        need = paged_attention_shared_prefix_workspace_size(S, H, Hkv, D, B, int(prefix_len), int(max_tail_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
     wbytes = workspace.numel() * workspace.element_size()
     head = (_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(prefix_blocks), int(prefix_len),
@@ -467,9 +469,8 @@ def paged_attention_decode_static_workspace(out: torch.Tensor, query: torch.Tens
     for n, t in (("out", out), ("key_cache", key_cache), ("value_cache", value_cache)):
         if _cuda16(n, t) != dt:
             raise PagedKVError(-1, f"{n} dtype differs from query")
-    for n, t in (("block_tables", block_tables), ("context_lens", context_lens)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise PagedKVError(-1, f"{n} must be a contiguous CUDA int32 tensor")
+    _cuda_i32("block_tables", block_tables)
+    _cuda_i32("context_lens", context_lens)
     NB, Hkv, B, D = key_cache.shape
     S, H, _ = query.shape
     if out.shape != query.shape or value_cache.shape != key_cache.shape:

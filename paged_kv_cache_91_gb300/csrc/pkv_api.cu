@@ -13,7 +13,6 @@
 #include "paged_kv.h"
 #include "pkv_common.cuh"
 #include "pkv_decode_mq.cuh"
-#include "pkv_decode_stream.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -588,46 +587,28 @@ int max_partitions_for(int max_context_len, int partition_size) {
   return n < 1 ? 1 : n;
 }
 
-std::atomic<int> g_decode_path{PKV_DECODE_AUTO};
 std::atomic<int> g_mq_tile{PKV_MQ_TILE_AUTO};
-
-size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 // How one decode call runs and what workspace it needs.
 struct Plan {
-  bool stream;  // persistent equal-work kernel (else the partitioned grid kernel)
   bool mma;     // tensor-core grouped-query tile (else CUDA cores)
-  int ng, gc;   // head groups per sequence, query heads per group
-  int np;       // partitions per sequence on the grid path
-  int wcap;     // warps the stream path may use (multiple of kDecodeWarps)
-  size_t pre_bytes, need;
+  int np;       // partitions per sequence
+  size_t need;  // split-K workspace bytes
 };
 
-// fp8: an FP8 (E4M3) cache, always on the partitioned path: the tensor-core tile
-// for head_dim 128 and any group size up to 8 (MHA included), else the CUDA cores.
+// One CTA per (partition of P tokens, head group, sequence). fp8: an FP8 (E4M3)
+// cache, on the tensor-core tile for head_dim 128 and any group size up to 8 (MHA
+// included), else the CUDA cores; a 16-bit cache takes the tensor-core tile for
+// 2 <= G <= 8. Contexts longer than P leave one partial per partition.
 Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_context_len,
                int partition_size, bool fp8) {
+  (void)block_size;
   Plan pl{};
   const int G = num_heads / num_kv_heads;
   pl.mma = fp8 ? (G <= 8 && head_dim == 128) : (G >= 2 && G <= 8);
-  pl.ng = pl.mma ? num_kv_heads : num_heads;
-  pl.gc = pl.mma ? G : 1;
-  const long long mb = (max_context_len + block_size - 1) / block_size;
-  const long long tiles = (long long)num_seqs * pl.ng * mb;  // upper bound on the flattened tile count
-  const bool stream_ok = num_seqs <= kStreamMaxSeqs && tiles < (1LL << 31);
-  const int path = g_decode_path.load(std::memory_order_relaxed);
-  pl.stream = !fp8 && stream_ok && path == PKV_DECODE_PERSISTENT;
   const int P = partition_size ? partition_size : (fp8 ? kDefaultPartitionFp8 : kDefaultPartition);
   pl.np = max_partitions_for(max_context_len, P);
-  if (pl.stream) {
-    long long w = tiles < kStreamMaxWarps ? tiles : kStreamMaxWarps;
-    if (w < 1) w = 1;
-    pl.wcap = (int)((w + kStreamWarps - 1) / kStreamWarps * kStreamWarps);
-    pl.pre_bytes = align256((size_t)(num_seqs + 1) * sizeof(int));
-    pl.need = pl.pre_bytes + (size_t)2 * pl.wcap * pl.gc * (head_dim + 2) * sizeof(float);
-  } else {
-    pl.need = pl.np > 1 ? (size_t)num_seqs * num_heads * pl.np * (head_dim + 2) * sizeof(float) : 0;
-  }
+  pl.need = pl.np > 1 ? (size_t)num_seqs * num_heads * pl.np * (head_dim + 2) * sizeof(float) : 0;
   return pl;
 }
 
@@ -653,16 +634,6 @@ SideStream* side_stream(int dev) {
       x.s = nullptr;
   }
   return x.s ? &x : nullptr;
-}
-
-int sm_count(int dev) {
-  static int counts[kMaxDevices] = {};
-  if (!counts[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
-    counts[dev] = n;
-  }
-  return counts[dev];
 }
 
 size_t workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -760,35 +731,6 @@ pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, co
                  : !make_pool_map(&kmap, key_cache, rows, head_dim, block_size, cache_dtype) ||
                        !make_pool_map(&vmap, value_cache, rows, head_dim, block_size, cache_dtype))
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
-  }
-
-  if (pl.stream) {
-    const int sms = sm_count(dev);
-    if (!sms) return fail(PKV_ERR_CUDA, "could not read the SM count of device %d", dev);
-    int occ = 0;
-    e = dtype == PKV_F16 ? decode_stream_occupancy_f16(head_dim, block_size, pl.mma, num_seqs, &occ)
-                         : decode_stream_occupancy_bf16(head_dim, block_size, pl.mma, num_seqs, &occ);
-    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the persistent decode kernel");
-    if (occ < 1) occ = 1;
-    int grid = sms * occ;
-    if (grid > pl.wcap / kStreamWarps) grid = pl.wcap / kStreamWarps;
-    StreamParams sp{};
-    sp.p = p;
-    sp.num_seqs = num_seqs;
-    sp.ng = pl.ng;
-    sp.gc = pl.gc;
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    sp.pre_out = reinterpret_cast<int*>(ws);
-    sp.slot_o = reinterpret_cast<float*>(ws + pl.pre_bytes);
-    sp.slot_m = sp.slot_o + (size_t)2 * pl.wcap * pl.gc * head_dim;
-    sp.slot_l = sp.slot_m + (size_t)2 * pl.wcap * pl.gc;
-    e = dtype == PKV_F16 ? decode_stream_f16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream)
-                         : decode_stream_bf16(sp, kmap, vmap, head_dim, block_size, pl.mma, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "persistent decode kernel launch");
-    e = dtype == PKV_F16 ? stream_reduce_f16(sp, head_dim, grid * kStreamWarps, stream)
-                         : stream_reduce_bf16(sp, head_dim, grid * kStreamWarps, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
-    return PKV_OK;
   }
 
   if (pl.need) {
@@ -957,11 +899,6 @@ int32_t pkv_set_multi_query_tile(int32_t tile) {
       tile != PKV_MQ_TILE_TENSOR && tile != PKV_MQ_TILE_PAIRS)
     return -1;
   return g_mq_tile.exchange(tile);
-}
-
-int32_t pkv_set_decode_path(int32_t path) {
-  if (path != PKV_DECODE_AUTO && path != PKV_DECODE_PARTITIONED && path != PKV_DECODE_PERSISTENT) return -1;
-  return g_decode_path.exchange(path);
 }
 
 pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping,

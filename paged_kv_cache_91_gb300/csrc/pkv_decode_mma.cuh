@@ -13,9 +13,8 @@
 //
 // Tiles come in through a 2D tensor map in boxes of 64 head dims x block_size
 // tokens with the 128-byte swizzle, which makes every ldmatrix phase
-// conflict-free. MmaTile holds the per-tile arithmetic shared by the grid
-// kernel below (one CTA per (partition, kv head, sequence), per-warp rings) and
-// the persistent kernel (pkv_decode_stream.cuh).
+// conflict-free. MmaTile holds the per-tile arithmetic of the grid kernel
+// below (one CTA per (partition, kv head, sequence), per-warp rings).
 #pragma once
 
 #include "pkv_common.cuh"

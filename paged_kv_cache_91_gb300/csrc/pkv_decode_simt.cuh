@@ -7,13 +7,12 @@
 // softmax, accumulate the weighted values; "vLLM: LLM 서빙 메모리 최적화의
 // 교과서", eq. (4).
 //
-// SimtTile holds the per-tile arithmetic shared by the grid kernel below and the
-// persistent kernel (pkv_decode_stream.cuh). The grid kernel runs one CTA per
-// (context partition, query head, sequence): each warp owns a private ring of
-// SPW stages, each stage the K tile and V tile of one (physical block, kv head)
-// pair brought in by two linear bulk copies (TMA engine) completing on the
-// stage's mbarrier; warp w takes the partition's blocks w, w+NW, ... and refills
-// the stage it just consumed. A single-partition context writes its output
+// SimtTile holds the per-tile arithmetic of the grid kernel below, which runs
+// one CTA per (context partition, query head, sequence): each warp owns a
+// private ring of SPW stages, each stage the K tile and V tile of one (physical
+// block, kv head) pair brought in by two linear bulk copies (TMA engine)
+// completing on the stage's mbarrier; warp w takes the partition's blocks w,
+// w+NW, ... and refills the stage it just consumed. A single-partition context writes its output
 // directly; longer ones write (m, l, o) partials that pkv_reduce_kernel merges.
 #pragma once
 

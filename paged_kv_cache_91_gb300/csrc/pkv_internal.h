@@ -61,17 +61,6 @@ cudaError_t decode_mq_pairs_fp8_bf16(const DecodeParams& p, const MqParams& mq, 
                                      const CUtensorMap& vmap, int head_dim, int block_size, int num_seqs,
                                      cudaStream_t stream);
 
-// Persistent equal-work decode (pkv_decode_stream.cuh): CTAs per SM, launch, reduce.
-struct StreamParams;
-cudaError_t decode_stream_occupancy_f16(int head_dim, int block_size, bool mma, int num_seqs, int* ctas);
-cudaError_t decode_stream_occupancy_bf16(int head_dim, int block_size, bool mma, int num_seqs, int* ctas);
-cudaError_t decode_stream_f16(const StreamParams& sp, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              int head_dim, int block_size, bool mma, int grid, cudaStream_t stream);
-cudaError_t decode_stream_bf16(const StreamParams& sp, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               int head_dim, int block_size, bool mma, int grid, cudaStream_t stream);
-cudaError_t stream_reduce_f16(const StreamParams& sp, int head_dim, int nwarps, cudaStream_t stream);
-cudaError_t stream_reduce_bf16(const StreamParams& sp, int head_dim, int nwarps, cudaStream_t stream);
-
 // Set the calling thread's pkv_last_error_message() text.
 void set_last_error_message(const char* msg);
 

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("paged_kv_write", "paged_attention_decode", "paged_attention_workspace_size",
-              "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message", "pkv_set_decode_path",
+              "paged_kv_device_errors", "pkv_status_string", "pkv_last_error_message",
               "pkv_selftest_wait_timeout", "paged_attention_decode_static_workspace", "paged_kv_copy_blocks",
               "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
               "paged_attention_multi_query", "paged_attention_multi_query_workspace_size",
@@ -59,23 +59,12 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.paged_attention_workspace_size
-    prev = lib.pkv_set_decode_path(1)  # partitioned
-    try:
-        assert ws(64, 40, 40, 128, 16, 512, 512) == 0  # one partition: no workspace
-        assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
-        assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
-        assert ws(0, 40, 40, 128, 16, 4096, 0) == 0 and ws(4, 40, 40, 128, 16, -1, 0) == 0
-        assert lib.pkv_set_decode_path(2) == 1  # persistent
-        # prefix of S + 1 ints (256-byte aligned) + 2 partials of (D + 2) floats per warp and group head
-        assert ws(64, 40, 40, 128, 16, 2048, 0) == 512 + 2 * 2048 * 1 * 130 * 4
-        assert ws(256, 32, 8, 128, 16, 8192, 0) == 1280 + 2 * 2048 * 4 * 130 * 4
-        assert ws(2, 4, 4, 64, 16, 33, 0) == 256 + 2 * 24 * 66 * 4  # 2 seqs x 4 heads x 3 blocks = 24 warps
-        assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 8 * 66 * 4  # too many sequences: partitioned
-        assert lib.pkv_set_decode_path(7) == -1
-        assert lib.pkv_set_decode_path(0) == 2  # auto chooses the partitioned path
-        assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
-    finally:
-        lib.pkv_set_decode_path(prev)
+    assert ws(64, 40, 40, 128, 16, 512, 512) == 0  # one partition: no workspace
+    assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
+    assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
+    assert ws(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 16 * 130 * 4
+    assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 8 * 66 * 4
+    assert ws(0, 40, 40, 128, 16, 4096, 0) == 0 and ws(4, 40, 40, 128, 16, -1, 0) == 0
 
 
 P = ctypes.c_void_p
@@ -169,17 +158,13 @@ def test_package_does_not_import_the_oracle():
                 assert "liboracle" not in src and "pkv_oracle" not in src, f
 
 
-def test_fp8_workspace_is_the_partitioned_size_on_every_path(lib):
+def test_fp8_workspace_size(lib):
     ws8 = lib.paged_attention_workspace_size_fp8
-    prev = lib.pkv_set_decode_path(2)  # persistent: the FP8 decode ignores it
-    try:
-        assert ws8(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
-        assert ws8(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 8 * 130 * 4  # 0 selects 1024 for FP8
-        assert ws8(256, 32, 8, 128, 16, 1024, 0) == 0
-        assert ws8(64, 40, 40, 128, 16, 512, 512) == 0
-        assert ws8(0, 40, 40, 128, 16, 4096, 0) == 0
-    finally:
-        lib.pkv_set_decode_path(prev)
+    assert ws8(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
+    assert ws8(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 8 * 130 * 4  # 0 selects 1024 for FP8
+    assert ws8(256, 32, 8, 128, 16, 1024, 0) == 0
+    assert ws8(64, 40, 40, 128, 16, 512, 512) == 0
+    assert ws8(0, 40, 40, 128, 16, 4096, 0) == 0
 
 
 def decode_fp8(lib, **kw):
@@ -328,8 +313,6 @@ def test_binding_constants_match_the_header():
     defines = {m[0]: int(m[1]) for m in re.findall(r"^#define PKV_(\w+) (\d+)u?\b", text, flags=re.M)}
     enum = {m[0]: int(m[1]) for m in re.findall(r"PKV_(F16|BF16|FP8_E4M3) = (\d+)", text)}
     assert enum == {"F16": binding.PKV_F16, "BF16": binding.PKV_BF16, "FP8_E4M3": binding.PKV_FP8_E4M3}
-    for name in ("AUTO", "PARTITIONED", "PERSISTENT"):
-        assert defines[f"DECODE_{name}"] == getattr(binding, f"DECODE_{name}")
     for name in ("AUTO", "COLUMNS", "ROWS", "TENSOR", "PAIRS"):
         assert defines[f"MQ_TILE_{name}"] == getattr(binding, f"MQ_TILE_{name}")
     header_bits = {v: k[len("DEVERR_"):] for k, v in defines.items() if k.startswith("DEVERR_")}

@@ -242,20 +242,14 @@ def test_decode_fp8_full_range_codes_and_outliers():
     assert binding.device_errors() == 0
 
 
-def test_decode_fp8_empty_contexts_and_path_independence():
+def test_decode_fp8_empty_contexts_and_repeat_calls():
     batch = W.build_batch(seed=84, context_lens=[0, 5, 0, 700], num_heads=4, num_kv_heads=4, head_dim=64,
                           block_size=16, dtype=BF16, pool_factor=1.5)
     kc8, vc8 = fp8_pools(batch, 0.02, 0.02)
     ref = reference(batch, kc8, vc8, 0.02, 0.02)
     t = W.as_torch(batch, DEV)
     K, V = to_dev_u8(kc8), to_dev_u8(vc8)
-    outs = []
-    for path in (binding.DECODE_PERSISTENT, binding.DECODE_PARTITIONED):
-        prev = binding.set_decode_path(path)
-        try:
-            outs.append(decode_fp8(batch, t, K, V, 0.02, 0.02))
-        finally:
-            binding.set_decode_path(prev)
+    outs = [decode_fp8(batch, t, K, V, 0.02, 0.02) for _ in range(2)]
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
     check_close(as_bits(outs[0]), ref, BF16)

@@ -23,14 +23,10 @@ RTOL = 1e-2
 DEV = "cuda:0"
 
 
-@pytest.fixture(autouse=True, params=["persistent", "partitioned"])
-def decode_path(request, cuda_lib):
-    """Every test runs on both decode paths (they must give the same results)."""
-    path = binding.DECODE_PERSISTENT if request.param == "persistent" else binding.DECODE_PARTITIONED
-    prev = binding.set_decode_path(path)
+@pytest.fixture(autouse=True)
+def clear_device_errors(cuda_lib):
     binding.device_errors(clear=True)
-    yield request.param
-    binding.set_decode_path(prev)
+    yield
 
 
 def as_np(t: torch.Tensor) -> np.ndarray:
@@ -283,12 +279,12 @@ def test_largest_partition_and_group():
 
 
 # ----------------------------------------------------------------------------
-# shapes that stress the persistent path's equal-work split
+# edge shapes: thousands of tiny sequences, one very long sequence
 
 
 @pytest.mark.parametrize("Hkv", [8, 2])
 def test_many_tiny_sequences(Hkv):
-    """2000 sequences of 0..40 tokens: many segments per warp, complete and split, and empty ones."""
+    """2000 sequences of 0..40 tokens, empty ones among them."""
     rng = np.random.default_rng(41)
     ctx = rng.integers(0, 41, size=2000)
     ctx[::97] = 0
@@ -303,7 +299,7 @@ def test_many_tiny_sequences(Hkv):
 
 @pytest.mark.parametrize("H,Hkv", [(2, 2), (8, 2)])
 def test_one_long_sequence_across_all_warps(H, Hkv):
-    """A single 32768-token sequence: every warp holds a piece of each segment."""
+    """A single 32768-token sequence with 1% of its keys x8: 64 partitions merged by the reduce."""
     batch = W.build_batch(seed=42, context_lens=[32768], num_heads=H, num_kv_heads=Hkv, head_dim=128,
                           block_size=16, dtype=F16, key_outlier_frac=0.01)
     t = W.as_torch(batch, DEV)
@@ -312,8 +308,8 @@ def test_one_long_sequence_across_all_warps(H, Hkv):
     check_close(as_np(out), reference(batch), F16, "long")
 
 
-def test_more_sequences_than_the_persistent_path_takes():
-    """2100 sequences: the persistent choice falls back to the partitioned kernels."""
+def test_2100_short_sequences_in_blocks_of_8():
+    """2100 sequences of 1..59 tokens in 8-token blocks."""
     rng = np.random.default_rng(43)
     batch = W.build_batch(seed=43, context_lens=rng.integers(1, 60, size=2100), num_heads=4, num_kv_heads=4,
                           head_dim=64, block_size=8, dtype=F16)

@@ -93,16 +93,6 @@ def test_static_workspace_matches_oracle_and_decode_on_two_calls(cuda_lib):
     run_two_calls(static_entry(binding.load()))
 
 
-def test_static_workspace_on_the_persistent_path(cuda_lib):
-    """The persistent path keeps a per-sequence block prefix and per-warp partials in the scratch."""
-    fn = static_entry(binding.load())
-    prev = binding.set_decode_path(binding.DECODE_PERSISTENT)
-    try:
-        run_two_calls(fn)
-    finally:
-        binding.set_decode_path(prev)
-
-
 def test_static_workspace_reports_bad_arguments_before_the_size(cuda_lib):
     """An oversize call with a bad argument gets that argument's error, not PKV_ERR_WORKSPACE."""
     lib = binding.load()
@@ -120,7 +110,7 @@ def test_static_workspace_reports_bad_arguments_before_the_size(cuda_lib):
 def test_static_workspace_rejects_oversize_requests(cuda_lib):
     lib = binding.load()
     fn = static_entry(lib)
-    S, H, D, mcl, P = 3000, 64, 128, 32768, 512  # more sequences than the persistent path takes
+    S, H, D, mcl, P = 3000, 64, 128, 32768, 512  # 3000 x 64 heads x 64 partitions of partials
     need = binding.paged_attention_workspace_size(S, H, H, D, 16, mcl, P)
     assert need > STATIC_BYTES
     fake = ctypes.c_void_p(0x10000)
