@@ -59,8 +59,6 @@ def parse_args():
     ap.add_argument("--max-seqs", type=int, default=None, help="use only the workload's first N sequences")
     ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32],
                     help="tokens per KV block (the pages' block-size ablation)")
-    ap.add_argument("--path", choices=["persistent", "partitioned"], default=None,
-                    help="decode path (default: the library's automatic choice)")
     ap.add_argument("--kv-dtype", choices=["auto", "fp8_e4m3"], default="auto",
                     help="auto: the cache holds the workload's fp16/bf16 values; fp8_e4m3: E4M3 codes "
                          "(paged_kv_write_fp8 / paged_attention_decode_fp8, or paged_attention_multi_query_fp8 "
@@ -478,8 +476,7 @@ class Case:
     """One timed configuration: a batch resident on the device and the library calls of its step (the
     cache write of the step's new tokens, then the attention call)."""
 
-    def __init__(self, batch, config: int, dev, *, fp8=False, shared=False, partition_size=0, mq_tile="auto",
-                 path=None):
+    def __init__(self, batch, config: int, dev, *, fp8=False, shared=False, partition_size=0, mq_tile="auto"):
         import numpy as np
         import torch
 
@@ -490,7 +487,7 @@ class Case:
         self.batch, self.config, self.dev = batch, config, dev
         self.fp8, self.shared, self.P = fp8, shared, partition_size
         self.mq = batch.query_start_loc is not None
-        self.mq_tile, self.path = mq_tile, path
+        self.mq_tile = mq_tile
         if shared and (self.mq or config != 4):
             raise SystemExit("--shared-prefix runs workload 4 (one query token per sequence)")
         self.apply_settings()
@@ -545,8 +542,6 @@ class Case:
         b = self.binding
         b.set_multi_query_tile({"auto": b.MQ_TILE_AUTO, "columns": b.MQ_TILE_COLUMNS, "rows": b.MQ_TILE_ROWS,
                                 "tensor": b.MQ_TILE_TENSOR, "pairs": b.MQ_TILE_PAIRS}[self.mq_tile])
-        b.set_decode_path({None: b.DECODE_AUTO, "partitioned": b.DECODE_PARTITIONED,
-                           "persistent": b.DECODE_PERSISTENT}[self.path])
 
     def write(self, nk, nv, sm):
         b, t = self.binding, self.t
@@ -588,6 +583,23 @@ class Case:
         t = self.t
         return (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"], t["context_lens"],
                 self.out, t.get("query_start_loc"))
+
+    def time_plain(self, K: int):
+        """ms per step of K steps with events around the region only (no per-call events, whose host time
+        shows in a launch-bound step)."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(st)
+        for _ in range(K):
+            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
 
     def time_device(self, K: int, warmup: int, dist):
         """K steps with every input resident in HBM: events around the whole region, around each attention
@@ -657,6 +669,39 @@ class Case:
         dist.barrier()
         e2e_ms = dist.max(s0.elapsed_time(s1))
         return dict(ms=e2e_ms / K, h2d=int(h2d), d2h=int(d2h))
+
+    def time_graph(self, K: int, replays: int = 20):
+        """us per step with K steps captured in one CUDA graph and replayed: the device-side latency of the
+        step, without the per-call host work (for the launch-bound tiny batch)."""
+        import torch
+
+        self.apply_settings()
+        t = self.t
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        main, self.stream = self.stream, side  # the calls take the capturing stream
+        try:
+            with torch.cuda.stream(side):
+                self.step(*self.device_args())  # warm the calls on the capturing stream
+            torch.cuda.current_stream(self.dev).wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(K):
+                    self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+                    self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+        finally:
+            self.stream = main
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(replays):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return 1e3 * a.elapsed_time(b) / (replays * K)
 
     def kernel_kind(self) -> str:
         G = self.batch.num_heads // self.batch.num_kv_heads
@@ -830,6 +875,9 @@ def run_suite(args, dist, dev, base_batch):
         e2e_t = None if args.no_e2e else case.time_e2e(K, args.warmup, dist)
         cpu = cpu_oracle(batch, args.suite_cpu_seconds, _all_cores(), case.fp8) if cpu_on else None
         results[key] = entry_summary(case, dev_t, e2e_t, None, cpu, K)
+        if batch.num_seqs <= 4:  # launch-bound: the step without per-call events, and from a CUDA graph
+            results[key]["us_per_step_no_call_events"] = round(1e3 * case.time_plain(K), 2)
+            results[key]["graph_us_per_step"] = round(case.time_graph(100), 2)
         results[key]["_window"] = (dev_t["t0"], dev_t["t1"])
         case.close()
     return results
@@ -857,7 +905,7 @@ def run_ours(args, dist):
     batch = W.make_config(args.config, max_seqs=args.max_seqs, block_size=args.block_size,
                           query_len=args.query_len)
     case = Case(batch, args.config, dev, fp8=args.kv_dtype == "fp8_e4m3", shared=args.shared_prefix,
-                partition_size=args.partition_size, mq_tile=args.mq_tile, path=args.path)
+                partition_size=args.partition_size, mq_tile=args.mq_tile)
     sampler = ClockSampler(gpu_id_for(dev))
     K = args.steps
     dev_t = case.time_device(K, args.warmup, dist)
