@@ -566,6 +566,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     const int lim = active ? mq_limit(mq, ctx, q_len, r, G) : 0;  // this row sees positions < lim
     const int vis = min(lim, tok1);
     const float sl2 = p.scale_log2 * qscale;
+    const bool neg = sl2 < 0.f;  // a negative scale: the largest score comes from the smallest product
     const uint32_t all = (1u << NBT) - 1u;
     // which blocks of each tile were fetched: the same test as the producer's
     int ids[Sh::IDS];
@@ -600,37 +601,59 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
       }
       const uint32_t mask = __ballot_sync(kFull, lane < NBT && fetched) & all;
       const int nv = vis - tb;  // leading tokens of the tile this row may see
+      // x[t] * mul is the score in the base-2 domain. A tile the row sees whole keeps the raw products
+      // (mul = sl2): the max of the raw scores, times sl2, is the max of the scaled ones (the min, for a
+      // negative scale), and each weight is then one fused multiply-add into exp2. A partial tile scales
+      // first and masks with -inf (mul = 1).
       float x[NT];
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent max chains
+      float mq[4];  // four independent max (or min) chains
+      float mx, mul;
       if (nv >= NT && mask == all) {
+        mul = sl2;
+        if (neg) {
+          mq[0] = mq[1] = mq[2] = mq[3] = INFINITY;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          x[t] = __uint_as_float(sr[t >> 5][t & 31]) * sl2;
-          mq[t & 3] = fmaxf(mq[t & 3], x[t]);
+          for (int t = 0; t < NT; ++t) {
+            x[t] = __uint_as_float(sr[t >> 5][t & 31]);
+            mq[t & 3] = fminf(mq[t & 3], x[t]);
+          }
+          mx = fminf(fminf(mq[0], mq[1]), fminf(mq[2], mq[3])) * sl2;
+        } else {
+          mq[0] = mq[1] = mq[2] = mq[3] = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            x[t] = __uint_as_float(sr[t >> 5][t & 31]);
+            mq[t & 3] = fmaxf(mq[t & 3], x[t]);
+          }
+          mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
         }
       } else {
+        mul = 1.f;
+        mq[0] = mq[1] = mq[2] = mq[3] = -INFINITY;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const bool see = t < nv && ((mask >> (t / BS)) & 1u);
           x[t] = see ? __uint_as_float(sr[t >> 5][t & 31]) * sl2 : -INFINITY;
           mq[t & 3] = fmaxf(mq[t & 3], x[t]);
         }
+        mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const bool move = mx > m_ref + 8.f;
       const bool resc = j > 0 && move && m_ref != -INFINITY;  // O's row holds terms to rescale
       const float f = resc ? fast_exp2(m_ref - mx) : 1.f;
       if (move) m_ref = mx;
-      // P row as 16-bit pairs (exp2(-inf) = 0 for masked tokens; a row that has
-      // seen nothing yet keeps m_ref = -inf and gets zeros)
+      // P row as 16-bit pairs (exp2(-inf) = 0 for masked tokens; a row that has seen nothing yet keeps
+      // m_ref = -inf and gets zeros). l sums the fp32 weights before their rounding to 16 bits, which
+      // moves the result by at most the rounding unit times the row's largest |v| (2^-9 for bf16 P).
       uint32_t pw[NT / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
       if (m_ref != -INFINITY) {
+        const float nm = -m_ref;
 #pragma unroll
         for (int u = 0; u < NT / 2; ++u) {
-          pw[u] = Elem<TP>::pack2(fast_exp2(x[2 * u] - m_ref), fast_exp2(x[2 * u + 1] - m_ref));
-          const float2 r = Elem<TP>::to_float2(pw[u]);  // l sums the weights PV multiplies
-          ls[u & 3] += r.x + r.y;
+          const float p0 = fast_exp2(fmaf(x[2 * u], mul, nm)), p1 = fast_exp2(fmaf(x[2 * u + 1], mul, nm));
+          pw[u] = Elem<TP>::pack2(p0, p1);
+          ls[u & 3] += p0 + p1;
         }
       } else {
 #pragma unroll
