@@ -232,6 +232,29 @@ pkv_status_t paged_attention_decode_static_workspace(
     int32_t num_blocks, pkv_dtype_t dtype, int32_t partition_size, cudaStream_t stream);
 
 /*
+ * pkv_read_chunks -- a measurement helper with no counterpart on the pages (it
+ * is not a step of the method). Reads num_reads chunks of chunk_bytes from
+ * `buffer`: read i is chunk order[i], the bytes [order[i] * chunk_bytes,
+ * (order[i] + 1) * chunk_bytes). Each chunk is one bulk copy into a per-warp
+ * shared-memory ring; nothing is written to global memory. Timed over a random
+ * order of whole chunks the size of one (block, kv head) tile, in a buffer
+ * larger than L2, it measures the read ceiling of the decode's access pattern
+ * (the decode reads every tile as such a chunk at a random place in the pool).
+ *
+ *   buffer       device memory, 16-byte aligned, buffer_bytes long (caller-owned)
+ *   order        [num_reads] int32 chunk indices on the device; an index outside
+ *                [0, buffer_bytes / chunk_bytes) is skipped and sets
+ *                PKV_DEVERR_BLOCK_ID
+ *   chunk_bytes  1024, 2048, 4096 or 8192
+ *
+ * Asynchronous on `stream`. Returns PKV_OK, PKV_ERR_INVALID_ARG (null or
+ * unaligned pointer, negative size), PKV_ERR_UNSUPPORTED (chunk size) or
+ * PKV_ERR_CUDA (launch).
+ */
+pkv_status_t pkv_read_chunks(const void* buffer, int64_t buffer_bytes, const int32_t* order,
+                             int64_t num_reads, int32_t chunk_bytes, cudaStream_t stream);
+
+/*
  * paged_kv_device_errors -- read the current device's error word (PKV_DEVERR_* bits
  * set by kernels since it was last cleared) into *flags, and clear it if `clear`
  * is non-zero. Synchronises the current device first. Returns PKV_OK, or

@@ -484,6 +484,22 @@ def paged_attention_decode_static_workspace(out: torch.Tensor, query: torch.Tens
     return out
 
 
+def read_chunks(buffer: torch.Tensor, order: torch.Tensor, chunk_bytes: int, stream=None) -> None:
+    """Read the chunks order[i] (int32, on the device) of chunk_bytes from buffer (uint8), one bulk copy each
+    into shared memory: the read ceiling of an access pattern (a measurement helper, not a step of the method)."""
+    lib = load()
+    fn = lib.pkv_read_chunks
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int32
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                       ctypes.c_void_p]
+    if buffer.dtype != torch.uint8 or not buffer.is_cuda or not buffer.is_contiguous():
+        raise PagedKVError(-1, "buffer must be a contiguous CUDA uint8 tensor")
+    _cuda_i32("order", order)
+    _check(lib, fn(_ptr(buffer), buffer.numel(), _ptr(order), order.numel(), int(chunk_bytes),
+                   _stream(buffer, stream)))
+
+
 def selftest_wait_timeout(limit_cycles: int = 2_000_000) -> int:
     """Run the bounded-wait self-test; returns the error word it leaves (PKV_DEVERR_TIMEOUT expected)."""
     lib = load()

@@ -803,6 +803,8 @@ PrefixPlan prefix_plan(int num_seqs, int group, int num_kv_heads, int block_size
 
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
 
+unsigned* device_error_word(int dev) { return error_word(dev); }
+
 }  // namespace pkv
 
 using namespace pkv;

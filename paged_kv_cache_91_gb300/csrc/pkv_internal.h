@@ -64,4 +64,7 @@ cudaError_t decode_mq_pairs_fp8_bf16(const DecodeParams& p, const MqParams& mq, 
 // Set the calling thread's pkv_last_error_message() text.
 void set_last_error_message(const char* msg);
 
+// The device address of a device's error word (PKV_DEVERR_* bits), or null.
+unsigned* device_error_word(int dev);
+
 }  // namespace pkv

@@ -37,7 +37,7 @@ def test_header_declares_the_boundary():
               "paged_kv_write_fp8", "paged_attention_decode_fp8", "paged_attention_workspace_size_fp8",
               "paged_attention_multi_query", "paged_attention_multi_query_workspace_size",
               "paged_attention_multi_query_fp8", "paged_attention_decode_shared_prefix_fp8",
-              "pkv_set_multi_query_tile"):
+              "pkv_set_multi_query_tile", "pkv_read_chunks"):
         assert n in names
 
 
@@ -317,3 +317,18 @@ def test_binding_constants_match_the_header():
         assert defines[f"MQ_TILE_{name}"] == getattr(binding, f"MQ_TILE_{name}")
     header_bits = {v: k[len("DEVERR_"):] for k, v in defines.items() if k.startswith("DEVERR_")}
     assert header_bits == binding.DEVERR_BITS
+
+
+def test_read_chunks_host_checks(lib):
+    """The read helper rejects bad chunk sizes and null or unaligned pointers before any CUDA call."""
+    import ctypes
+
+    fn = lib.pkv_read_chunks
+    fn.restype = ctypes.c_int32
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
+    fake = 0x10000
+    assert fn(fake, 1 << 20, fake, 16, 3000, None) == -2
+    assert fn(None, 1 << 20, fake, 16, 2048, None) == -1
+    assert fn(fake + 8, 1 << 20, fake, 16, 2048, None) == -1
+    assert fn(fake, 1 << 20, fake, -1, 2048, None) == -1
+    assert fn(fake, 1 << 20, fake, 0, 2048, None) == 0  # nothing to read

@@ -406,3 +406,23 @@ def test_copy_blocks_many_pairs_and_bad_pair(D, B):
     np.testing.assert_array_equal(as_np(tk), ek)
     np.testing.assert_array_equal(as_np(tv), ev)
     assert binding.device_errors() & 1
+
+
+def test_read_chunks_helper_reads_in_bounds_and_reports_bad_indices():
+    """The bench's read-ceiling helper: valid orders leave no error; an index past the buffer is skipped and
+    reported, and the context stays usable."""
+    buf = torch.empty(64 << 20, dtype=torch.uint8, device=DEV)
+    for ch in (1024, 2048, 4096, 8192):
+        n = buf.numel() // ch
+        order = torch.randperm(n, device=DEV, dtype=torch.int32, generator=torch.Generator(DEV).manual_seed(ch))
+        binding.read_chunks(buf, order, ch)
+        binding.read_chunks(buf, order[: 1000], ch)  # a partial last warp
+    assert binding.device_errors() == 0
+    bad = torch.tensor([0, 1, buf.numel() // 2048, -5, 3], dtype=torch.int32, device=DEV)
+    binding.read_chunks(buf, bad, 2048)
+    assert binding.device_errors() == 1  # PKV_DEVERR_BLOCK_ID
+    batch = W.make_config(1)
+    t = W.as_torch(batch, DEV)
+    out = run_step(batch, t, write=False)
+    torch.cuda.synchronize()
+    check_close(as_np(out), reference(batch), F16, "after the read helper")
