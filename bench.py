@@ -734,11 +734,16 @@ class Case:
                 else ("multi-query kernel" if self.mq else "decode kernel")
                 + (" + log-sum-exp reduce" if self.nparts > 1 else ""))
         traffic = None if self.shared else ncu_traffic(self.workload_key(), self.kernel_kind())
+        tile = self.batch.block_size * self.batch.head_dim * self.cache_bytes  # bytes of one (block, kv head) tile
+        ceil = read_ceiling(self.dev, tile)
         return {"bound": "hbm", "kernel": f"{self.call_name()} ({what})", "achieved": round(achieved, 2),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4), "traffic": traffic,
                 "algorithmic_bytes_per_call": int(hbm_bytes), "avg_call_ms": round(call_ms, 4),
-                "kernel_hash": kernel_hash(self.kernel_kind())}
+                "kernel_hash": kernel_hash(self.kernel_kind()),
+                "read_ceiling": None if ceil is None else {
+                    "gbs": ceil, "frac": round(achieved / ceil, 4), "chunk_bytes": tile,
+                    "what": "pkv_read_chunks over random whole tiles of a 2 GiB buffer (read only, no arithmetic)"}}
 
     def close(self):
         import torch
@@ -749,6 +754,41 @@ class Case:
 
 
 SPEC_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth
+
+_CEILING = {}
+
+
+def read_ceiling(dev, chunk_bytes: int, buf_bytes: int = 2 << 30, reps: int = 5):
+    """GB/s of the library's read helper over a random order of whole chunk_bytes chunks of a 2 GiB buffer
+    (larger than L2): the read ceiling of the decode's access pattern, where every (block, kv head) tile is
+    such a chunk at a random place in the pool. Measured once per chunk size and process."""
+    if chunk_bytes not in (1024, 2048, 4096, 8192):
+        return None
+    if chunk_bytes in _CEILING:
+        return _CEILING[chunk_bytes]
+    import torch
+
+    from paged_kv_cache_91_gb300 import binding
+
+    buf = torch.empty(buf_bytes, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    order = torch.randperm(buf_bytes // chunk_bytes, device=dev, dtype=torch.int32, generator=gen)
+    st = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        binding.read_chunks(buf, order, chunk_bytes, stream=st)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(st)
+    for _ in range(reps):
+        binding.read_chunks(buf, order, chunk_bytes, stream=st)
+    b.record(st)
+    torch.cuda.synchronize()
+    gbs = round(order.numel() * chunk_bytes * reps / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+    del buf, order
+    torch.cuda.empty_cache()
+    _CEILING[chunk_bytes] = gbs
+    return gbs
 
 
 def cpu_oracle(batch, budget_s: float, threads: int, fp8: bool, seed: int = 7):
