@@ -149,6 +149,8 @@ def test_write_fp8_bad_slot_is_skipped_and_reported():
     (8, 8, 128, 16, F16), (8, 8, 128, 16, BF16), (16, 4, 128, 16, BF16), (12, 4, 64, 16, F16),
     (8, 8, 128, 8, F16), (8, 2, 128, 32, BF16), (6, 6, 64, 8, BF16), (4, 4, 64, 32, F16),
     (32, 2, 128, 16, F16), (9, 1, 64, 16, BF16),
+    # an odd number of kv heads: no kv-head pairs, the one-head tile
+    (6, 3, 128, 16, F16), (5, 5, 128, 8, BF16), (8, 1, 128, 16, F16),
 ])
 def test_decode_fp8_shapes(H, Hkv, D, B, dtype):
     ctx = [1, 2, 7, B, B + 1, 100, 511, 512, 513, 1300]
