@@ -636,6 +636,115 @@ class Case:
 
     def time_e2e(self, K: int, warmup: int, dist):
         """The same step through the public API with the step's inputs copied from pinned host memory and
+        the output read back, every step. The pool stays resident: it is the cache. The copies run on a
+        second stream into two alternating sets of device buffers, so that step k + 1's inputs upload (and
+        step k - 1's output downloads) while step k computes; events order every copy against the steps
+        that use its buffers."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        names = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens") + \
+            (("query_start_loc",) if self.mq else ())
+        host = {k: t[k].cpu().pin_memory() for k in names}
+        dbuf = [{k: torch.empty_like(t[k]) for k in names} for _ in range(2)]
+        outs = [torch.empty_like(self.out) for _ in range(2)]
+        out_h = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(2)]
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h[0].numel() * out_h[0].element_size()
+        cs = torch.cuda.Stream(self.dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        uploaded = [ev(), ev()]   # inputs of the set are on the device
+        consumed = [ev(), ev()]   # the step that read the set (and wrote its output) has run
+        downloaded = [ev(), ev()]  # the set's output is back on the host
+
+        def run(n):
+            for k in range(n):
+                i = k & 1
+                with torch.cuda.stream(cs):
+                    if k >= 2:
+                        cs.wait_event(consumed[i])  # step k - 2 has finished with this set
+                    for name in names:
+                        dbuf[i][name].copy_(host[name], non_blocking=True)
+                    uploaded[i].record(cs)
+                st.wait_event(uploaded[i])
+                if k >= 2:
+                    st.wait_event(downloaded[i])  # step k - 2's output is read out before this one overwrites it
+                b = dbuf[i]
+                self.step(b["query"], b["new_key"], b["new_value"], b["slot_mapping"], b["block_tables"],
+                          b["context_lens"], outs[i], b.get("query_start_loc"))
+                consumed[i].record(st)
+                with torch.cuda.stream(cs):
+                    cs.wait_event(consumed[i])
+                    out_h[i].copy_(outs[i], non_blocking=True)
+                    downloaded[i].record(cs)
+            st.wait_stream(cs)  # the last output is on the host before the region ends
+
+        run(warmup)
+        torch.cuda.synchronize()
+        dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(st)
+        cs.wait_event(s0)  # no copy of the timed steps starts before the region
+        run(K)
+        s1.record(st)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = dist.max(s0.elapsed_time(s1))
+        return dict(ms=e2e_ms / K, h2d=int(h2d), d2h=int(d2h))
+
+    def time_plain(self, K: int):
+        """ms per step of K steps with events around the region only (no per-call events, whose host time
+        shows in a launch-bound step)."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(st)
+        for _ in range(K):
+            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+
+    def time_device(self, K: int, warmup: int, dist):
+        """K steps with every input resident in HBM: events around the whole region, around each attention
+        call and before each write, all on the launching stream."""
+        import torch
+
+        self.apply_settings()
+        t, st = self.t, self.stream
+        for _ in range(warmup):
+            self.step(*self.device_args())
+        torch.cuda.synchronize()
+        self.binding.device_errors(clear=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t_wall0 = time.time()
+        start.record(st)
+        for k in range(K):
+            ev_w[k].record(st)
+            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+            ev[k][0].record(st)
+            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+            ev[k][1].record(st)
+        end.record(st)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t_wall1 = time.time()
+        total_ms = dist.max(start.elapsed_time(end))
+        return dict(total_ms=total_ms, call_ms=statistics.fmean(a.elapsed_time(b) for a, b in ev),
+                    write_ms=statistics.fmean(w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)),
+                    t0=t_wall0, t1=t_wall1, errors=self.binding.device_errors(clear=True))
+
+    def time_e2e(self, K: int, warmup: int, dist):
+        """The same step through the public API with the step's inputs copied from pinned host memory and
         the output read back, every step. The pool stays resident: it is the cache."""
         import torch
 
