@@ -187,12 +187,18 @@ __device__ __forceinline__ void mq_tc_widen_tile(unsigned char* dst, const unsig
   for (int a = 0; a < 8; ++a) {
     const uint32_t w[8] = {c[a][0].x, c[a][0].y, c[a][0].z, c[a][0].w, c[a][1].x, c[a][1].y, c[a][1].z, c[a][1].w};
     unsigned char* row = dst + a * 2048 + (q >> 1) * 1024 + t8 * 128;
+    // Lanes q = 2, 3 store their chunks in the order 2, 3, 0, 1: an 8-lane phase of the 16-byte stores then
+    // covers 8 distinct 16-byte bank groups (in order, lanes q and q + 2 would hit the same one).
+    const bool rot = (q >> 1) != 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
+      const int kk = rot ? (k ^ 2) : k;
+      const uint32_t wa = rot ? w[2 * (k ^ 2)] : w[2 * k];
+      const uint32_t wb = rot ? w[2 * (k ^ 2) + 1] : w[2 * k + 1];
       uint32_t h[4];
-      e4m3x4_to_f16x2(w[2 * k], h[0], h[1]);
-      e4m3x4_to_f16x2(w[2 * k + 1], h[2], h[3]);
-      const int cc = (q & 1) * 4 + k;
+      e4m3x4_to_f16x2(wa, h[0], h[1]);
+      e4m3x4_to_f16x2(wb, h[2], h[3]);
+      const int cc = (q & 1) * 4 + kk;
       *reinterpret_cast<uint4*>(row + ((cc ^ t8) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
   }
