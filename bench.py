@@ -996,6 +996,7 @@ SUITE = [
     ("w4_shared_prefix", 4, {}),
     ("w4_shared_prefix_call", 4, {"shared": True}),
     ("w4_fp8", 4, {"fp8": True}),
+    ("w4_shared_prefix_call_fp8", 4, {"shared": True, "fp8": True}),
     ("w5_long_split_k", 5, {}),
     ("w5_fp8", 5, {"fp8": True}),
 ]
