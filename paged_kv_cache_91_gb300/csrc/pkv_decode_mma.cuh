@@ -164,37 +164,40 @@ struct MmaTile {
         const float x01 = va1 ? sacc[1] * slb : -INFINITY;
         const float x10 = vb0 ? sacc[2] * sla : -INFINITY;
         const float x11 = vb1 ? sacc[3] * slb : -INFINITY;
+        // Lazy rescaling: a column's reference m moves (and its state is rescaled) only when one of its
+        // scores exceeds m by more than 8, so p = 2^(x - m) <= 2^8. Each lane tests its own scores and the
+        // warp votes; the max is reduced across the lanes only when some score does exceed.
         float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+        if (__any_sync(kFull, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+          }
+          const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
+          const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+          // a column that keeps its m may still hold -inf there (it has seen nothing yet): factor 1
+          const float al0 = up0 ? fast_exp2(m0 - mn0) : 1.f, al1 = up1 ? fast_exp2(m1 - mn1) : 1.f;
+          l0 *= al0;
+          l1 *= al1;
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+          m0 = mn0;
+          m1 = mn1;
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        // a column that has seen no token yet keeps m = -inf; exponentiate against 0 there
-        const float ms0 = CAUSAL && mn0 == -INFINITY ? 0.f : mn0;
-        const float ms1 = CAUSAL && mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+        // a column that has seen no token yet keeps m = -inf (all its x are -inf): exponentiate against 0
+        const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
         const uint32_t pa = Elem<T>::pack2(fast_exp2(x00 - ms0), fast_exp2(x01 - ms1));
         const uint32_t pb = Elem<T>::pack2(fast_exp2(x10 - ms0), fast_exp2(x11 - ms1));
         const float2 fa = Elem<T>::to_float2(pa), fb = Elem<T>::to_float2(pb);
-        float rs0 = fa.x + fb.x, rs1 = fa.y + fb.y;
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          rs0 += __shfl_xor_sync(kFull, rs0, o);
-          rs1 += __shfl_xor_sync(kFull, rs1, o);
-        }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-          acc[mt][0] *= al0;
-          acc[mt][1] *= al1;
-          acc[mt][2] *= al0;
-          acc[mt][3] *= al1;
-        }
+        // l: this lane's rows only (the weights PV multiplies); finish() adds the lanes of a column
+        l0 += fa.x + fb.x;
+        l1 += fa.y + fb.y;
         // P^T as the B operand of the PV MMA: transpose the 8x8 score fragments
         const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
         {
@@ -212,7 +215,14 @@ struct MmaTile {
   }
 
   // The running sums are complete after every tile here.
-  static __device__ __forceinline__ void finish(float&, float&) {}
+  // Complete the running sums: add the per-lane partial sums of each column.
+  static __device__ __forceinline__ void finish(float& l0, float& l1) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, o);
+      l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+  }
 
   // The accumulators as red[head][dim] (head = column, dims in natural order).
   static __device__ __forceinline__ void store_acc(float* red, const float (&acc)[KT][4], int lane) {

@@ -197,16 +197,18 @@ struct MmaTileE4M3 {
         const float x01 = va1 ? sacc[1] * slb : -INFINITY;
         const float x10 = vb0 ? sacc[2] * sla : -INFINITY;
         const float x11 = vb1 ? sacc[3] * slb : -INFINITY;
-        float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-        }
         // Lazy rescaling: a column's reference m moves (and its state is rescaled)
-        // only when a score exceeds it by more than 8, so p = 2^(x - m) <= 2^8.
-        const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
-        if (__any_sync(kFull, up0 || up1)) {
+        // only when a score exceeds it by more than 8, so p = 2^(x - m) <= 2^8. Each
+        // lane tests its own scores and the warp votes; the max is reduced across
+        // the lanes only when some score does exceed.
+        float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+        if (__any_sync(kFull, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+          }
+          const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
           const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
           float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
           if constexpr (CAUSAL) {  // a column that keeps its m may still hold -inf there
