@@ -143,21 +143,23 @@ struct SimtTile {
         const int nv = min(Sh::TPC, nvalid - c * Sh::TPC);
         sc = tl < nv ? sc : -INFINITY;  // tokens past the context do not take part
 
-        // running softmax update; the LPT lanes of a token hold the same score,
-        // so the reductions run over the TPC distinct tokens only
-        float mx = sc;
+        // Running softmax with a lazily moved reference: m moves (and l and acc are
+        // rescaled) only when a score exceeds it by more than 8, so every weight is
+        // at most 2^8. Each lane tests its token and the warp votes; the max is
+        // reduced (over the TPC distinct tokens: the LPT lanes of a token hold the
+        // same score) only then.
+        if (__any_sync(kFull, sc > m + 8.f)) {
+          float mx = sc;
 #pragma unroll
-        for (int o = Sh::LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-        const float mnew = fmaxf(m, mx);
-        const float alpha = fast_exp2(m - mnew);
-        const float pr = fast_exp2(sc - mnew);
-        float ps = pr;
+          for (int o = Sh::LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+          const float alpha = fast_exp2(m - mx);  // 0 while m is still -inf (l and acc are 0 then)
+          l *= alpha;
 #pragma unroll
-        for (int o = Sh::LPT; o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
-        l = l * alpha + ps;
-        m = mnew;
-#pragma unroll
-        for (int e = 0; e < Sh::DPV; ++e) acc[e] *= alpha;
+          for (int e = 0; e < Sh::DPV; ++e) acc[e] *= alpha;
+          m = mx;
+        }
+        const float pr = fast_exp2(sc - m);
+        if (pt == 0) l += pr;  // one lane per token; the lanes' sums are added after the last tile
 
         // weighted values: lane owns DPV consecutive head dims. A full chunk runs
         // without per-token branches so its loads can all be in flight at once;
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(NW * 32, PKV_DECODE_MIN_CTAS) pkv_decode_simt_
 #pragma unroll
     for (int e = 0; e < Sh::DPV; ++e) acc[e] = 0.f;
   }
+  l = warp_sum(l);  // the tiles' sums were kept per lane
 
   // merge the warps' running states
   float* red = reinterpret_cast<float*>(smem + Sh::RED);
