@@ -132,10 +132,10 @@ class Dist:
 
 
 def default_partition(fp8: bool, mq: bool = False, block_size: int = 16) -> int:
-    """The library's partition size when the call passes 0 (longer for an FP8 cache and for multi-query)."""
+    """The library's partition size when the call passes 0 (longer for multi-query)."""
     if mq:
         return min(2048, 128 * block_size)
-    return 1024 if fp8 else 512
+    return 1024
 
 
 SHARED_PREFIX_TOKENS = 1024  # workload 4's common prefix

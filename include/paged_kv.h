@@ -129,7 +129,7 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
  * (head_dim + 2) fp32 per sequence. The size is 0 when max_context_len <=
  * partition_size (no split).
  *
- * partition_size 0 selects the default, 512. Returns 0 for invalid arguments,
+ * partition_size 0 selects the default, 1024. Returns 0 for invalid arguments,
  * which paged_attention_decode then rejects.
  */
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
@@ -164,7 +164,7 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32
  *   scale                usually 1 / sqrt(head_dim)
  *   head_dim             64 or 128; block_size 8, 16 or 32
  *   num_heads            a multiple of num_kv_heads (GQA when larger)
- *   partition_size       0 = 512; else a multiple of block_size in
+ *   partition_size       0 = 1024; else a multiple of block_size in
  *                        [block_size, 128 * block_size]: the tokens of one
  *                        CTA's share of a context (contexts longer than this
  *                        are split and merged by log-sum-exp)
@@ -186,7 +186,8 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
 
 /* Size of the library-owned split-K scratch of
  * paged_attention_decode_static_workspace: 32 MiB per device. It covers, for
- * example, 16 sequences x 40 heads x 32768-token contexts at partition_size 512. */
+ * example, 16 sequences x 40 heads x 32768-token contexts at partition_size 512
+ * (16 MiB at the default 1024). */
 #define PKV_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 
 /*
@@ -507,9 +508,8 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
 
 /*
  * paged_attention_workspace_size_fp8 -- workspace bytes of
- * paged_attention_decode_fp8: the size paged_attention_workspace_size gives,
- * except that partition_size 0 selects 1024 (an FP8 tile carries half the
- * bytes, and longer partitions measure faster).
+ * paged_attention_decode_fp8: the size paged_attention_workspace_size gives
+ * (partition_size 0 selects 1024 for both).
  */
 size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                           int32_t head_dim, int32_t block_size,
@@ -527,7 +527,7 @@ size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, i
  * f16 with fp32 accumulation: the codes widen exactly to f16, a bf16 query is
  * scaled per head by a power of two into f16 range, and the softmax weights are
  * rounded to f16 (the normaliser sums the rounded weights). Other shapes run on
- * the CUDA cores in fp32. partition_size 0 selects 1024 here. All other
+ * the CUDA cores in fp32. All other
  * arguments, the split-K workspace (paged_attention_workspace_size_fp8) and the
  * error behaviour are those of paged_attention_decode.
  */

@@ -18,7 +18,11 @@
 namespace pkv {
 namespace {
 
-constexpr int kDefaultPartition = 512;
+// Decode partition: 1024 tokens over both cache types. Measured, decode call ms at 512 / 1024 / 2048 tokens
+// (16-bit cache): workload 2 0.1995 / 0.1980 / 0.1988, workload 3 0.1747 / 0.1715 / 0.1718, workload 4
+// 0.0662 / 0.0627 / 0.0619, workload 5 1.485 / 1.464 / 1.454; FP8 cache: workload 2 0.115 / 0.114 / 0.117,
+// workload 3 0.114 / 0.104 / 0.107. A CTA's start and end cost more than the longer per-CTA tail.
+constexpr int kDefaultPartition = 1024;
 #ifndef PKV_MQ_WIDE_MIN_ROWS
 // Multi-query rows per kv head from which the tensor-memory tile runs (build-time knob). Measured: at 16
 // rows (two 8-column CTAs per kv head) the 8-column tile is 3-10% faster; from 20 rows on the tensor tile
@@ -30,9 +34,6 @@ constexpr int kDefaultPartition = 512;
 // 0.362 ms, 32 rows even, 48 rows 0.509 against 0.371 ms (workload 3).
 #define PKV_MQ_WIDE_MIN_ROWS_FP8 33
 #endif
-// An FP8 tile carries half the bytes of a 16-bit one, so a CTA's fixed costs
-// weigh twice as much per byte: longer partitions measure faster.
-constexpr int kDefaultPartitionFp8 = 1024;
 // Multi-query: every query row writes D + 2 partial floats per partition, so
 // few long partitions measure fastest (capped at kMaxPartitionBlocks blocks).
 constexpr int kDefaultPartitionMq = 2048;
@@ -606,7 +607,7 @@ Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int 
   Plan pl{};
   const int G = num_heads / num_kv_heads;
   pl.mma = fp8 ? (G <= 8 && head_dim == 128) : (G >= 2 && G <= 8);
-  const int P = partition_size ? partition_size : (fp8 ? kDefaultPartitionFp8 : kDefaultPartition);
+  const int P = partition_size ? partition_size : kDefaultPartition;
   pl.np = max_partitions_for(max_context_len, P);
   pl.need = pl.np > 1 ? (size_t)num_seqs * num_heads * pl.np * (head_dim + 2) * sizeof(float) : 0;
   return pl;
@@ -672,7 +673,7 @@ pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, co
     return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
                 max_context_len, (long long)max_blocks_per_seq * block_size);
   if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
-  const int P = partition_size ? partition_size : (fp8 ? kDefaultPartitionFp8 : kDefaultPartition);
+  const int P = partition_size ? partition_size : kDefaultPartition;
   if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
                 block_size, kMaxPartitionBlocks * block_size);

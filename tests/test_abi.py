@@ -61,9 +61,10 @@ def test_workspace_size(lib):
     ws = lib.paged_attention_workspace_size
     assert ws(64, 40, 40, 128, 16, 512, 512) == 0  # one partition: no workspace
     assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
-    assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 64 * 130 * 4  # 0 selects 512
-    assert ws(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 16 * 130 * 4
-    assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 8 * 66 * 4
+    assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 32 * 130 * 4  # 0 selects 1024
+    assert ws(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 8 * 130 * 4
+    assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 4 * 66 * 4
+    assert ws(64, 40, 40, 128, 16, 1024, 0) == 0 and ws(64, 40, 40, 128, 16, 1025, 0) == 64 * 40 * 2 * 130 * 4
     assert ws(0, 40, 40, 128, 16, 4096, 0) == 0 and ws(4, 40, 40, 128, 16, -1, 0) == 0
 
 
@@ -97,8 +98,9 @@ def decode(lib, **kw):
     (dict(partition_size=24), UNSUPPORTED),          # not a multiple of block_size
     (dict(partition_size=16 * 129), UNSUPPORTED),    # more blocks than the kernel keeps per partition
     (dict(query=P(0x10008)), INVALID),               # misaligned
-    (dict(max_blocks_per_seq=64, max_context_len=1024), WORKSPACE),   # split needs a workspace
-    (dict(max_blocks_per_seq=64, max_context_len=1024, workspace=fake(9), workspace_bytes=100), WORKSPACE),
+    (dict(max_blocks_per_seq=128, max_context_len=2048), WORKSPACE),   # split needs a workspace
+    (dict(max_blocks_per_seq=128, max_context_len=2048, workspace=fake(9), workspace_bytes=100), WORKSPACE),
+    (dict(max_blocks_per_seq=64, max_context_len=1024, partition_size=512), WORKSPACE),
     (dict(num_seqs=70000), UNSUPPORTED),
 ])
 def test_decode_rejects_on_host(lib, kw, status):

@@ -13,7 +13,7 @@ def tiny(ctx, H=4, Hkv=2, D=64, B=16, query_lens=None, prefix=0):
 
 
 def test_decode_step_bytes_by_hand():
-    b = tiny([10, 40])  # one partition each at 512 tokens: no partials
+    b = tiny([10, 40])  # one partition each (512 or 1024 tokens): no partials
     kv, call = bench.step_bytes(b, 512)
     assert kv == (10 + 40) * 2 * 64 * 2 * 2  # tokens x kv heads x D x (K, V) x 2 bytes
     q_out = 2 * 2 * 4 * 64 * 2  # q and out: S x H x D x 2 bytes

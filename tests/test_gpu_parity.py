@@ -131,7 +131,7 @@ def test_split_k_partitions(H, Hkv, dtype):
 
 
 def test_long_context_with_outliers_split():
-    """1% of keys scaled by 8 (wide score range), 64 partitions of 512 merged by log-sum-exp."""
+    """1% of keys scaled by 8 (wide score range), 32 partitions of 1024 merged by log-sum-exp."""
     batch = W.build_batch(seed=22, context_lens=[32768, 20000, 513], num_heads=8, num_kv_heads=8,
                           head_dim=128, block_size=16, dtype=F16, key_outlier_frac=0.01)
     t = W.as_torch(batch, DEV)
