@@ -168,6 +168,21 @@ def test_decode_fp8_shapes(H, Hkv, D, B, dtype):
     assert binding.device_errors() == 0
 
 
+@pytest.mark.parametrize("H,Hkv,D,dtype", [(8, 8, 128, F16), (16, 4, 128, BF16), (12, 4, 64, F16)])
+def test_decode_fp8_default_partition_boundary(H, Hkv, D, dtype):
+    """partition_size 0 (1024 tokens): contexts just below, at and above one and two partitions."""
+    ctx = [1023, 1024, 1025, 2048, 2049]
+    batch = W.build_batch(seed=91 + H + D, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                          block_size=16, dtype=dtype, pool_factor=1.2)
+    ks, vs = 0.0137, 0.0093
+    kc8, vc8 = fp8_pools(batch, ks, vs)
+    t = W.as_torch(batch, DEV)
+    out = decode_fp8(batch, t, to_dev_u8(kc8), to_dev_u8(vc8), ks, vs)
+    torch.cuda.synchronize()
+    check_close(as_bits(out), reference(batch, kc8, vc8, ks, vs), dtype, "default partition")
+    assert binding.device_errors() == 0
+
+
 @pytest.mark.parametrize("H,Hkv,B,dtype", [(16, 8, 16, F16), (24, 8, 8, BF16), (64, 8, 32, F16), (8, 8, 16, BF16)])
 def test_decode_fp8_group_sizes(H, Hkv, B, dtype):
     """Group sizes 2, 3, 8 and 1 on the tensor-core tile (head_dim 128)."""
