@@ -341,32 +341,79 @@ __global__ void __launch_bounds__(32 * kReduceRows)
                             const int32_t* __restrict__ tail_lens, int tail_limit, int num_seqs, int num_heads) {
   pdl_begin();
   constexpr int DPL = D / 32;
+  constexpr int EARLY = 8;  // prefix partials whose outputs are requested in the first round of loads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row = (size_t)blockIdx.x * kReduceRows + warp;
   if (row >= (size_t)num_seqs * num_heads) return;
   const int s = (int)(row / num_heads);
-  int t = tail_lens[s];
-  t = t < 0 ? 0 : (t > tail_limit ? tail_limit : t);  // as the tail stage clamped it
-  const int n2 = (t + p2 - 1) / p2;
-  const int n = np1 + n2;
   auto at = [&](int q) { return q < np1 ? row * np1 + q : row * np2 + (q - np1); };
-  // one round of loads for the first 32 partials: lane q holds partial q's m and l
+  auto load_o = [&](int q, float (&v)[DPL]) {  // lane's dims of partial q's output
+    const float* o = (q < np1 ? o1 : o2) + at(q) * D + lane * DPL;
+    if constexpr (DPL == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(o);
+      v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(o);
+      v[0] = x.x, v[1] = x.y;
+    }
+  };
+  // First round of loads, all independent: the tail length, the prefix partials' m and l (lane q holds
+  // partial q) and the first EARLY prefix partials' outputs. The prefix count is known without the tail.
+  const int t_raw = tail_lens[s];
   float mq = -INFINITY, lq = 0.f;
-  if (lane < n) {
-    mq = lane < np1 ? m1[at(lane)] : m2[at(lane)];
-    lq = lane < np1 ? l1[at(lane)] : l2[at(lane)];
+  if (lane < np1) {
+    mq = m1[at(lane)];
+    lq = l1[at(lane)];
   }
+  const int ne = np1 < EARLY ? np1 : EARLY;
+  float oe[EARLY][DPL];
+#pragma unroll
+  for (int q = 0; q < EARLY; ++q)
+    if (q < ne) load_o(q, oe[q]);
+  // Second round: the tail's partials (its length clamped as the tail stage clamped it), and the output of
+  // the first partial past the early ones
+  const int t = t_raw < 0 ? 0 : (t_raw > tail_limit ? tail_limit : t_raw);
+  const int n = np1 + (t + p2 - 1) / p2;
+  if (lane >= np1 && lane < n) {
+    mq = m2[at(lane)];
+    lq = l2[at(lane)];
+  }
+  float on[DPL];
+  if (ne < n) load_o(ne, on);
   float M = mq;
   for (int q = 32 + lane; q < n; q += 32) M = fmaxf(M, q < np1 ? m1[at(q)] : m2[at(q)]);
   M = warp_max(M);
-  float acc[DPL], W = 0.f;
+  // partial q < 32: its weight l_q 2^(m_q - M) sits in lane q
+  const float wl = mq == -INFINITY ? 0.f : lq * fast_exp2(mq - M);
+  float W = warp_sum(wl);
+  float acc[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-  for (int q0 = 0; q0 < n; q0 += 32) {
+#pragma unroll
+  for (int q = 0; q < EARLY; ++q) {
+    if (q < ne) {
+      const float wk = __shfl_sync(kFull, wl, q);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, oe[q][e], acc[e]);
+    }
+  }
+  const int n32 = n < 32 ? n : 32;
+  if (ne < n32) {
+    const float wk = __shfl_sync(kFull, wl, ne);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, on[e], acc[e]);
+  }
+#pragma unroll 4
+  for (int q = ne + 1; q < n32; ++q) {  // independent loads of the remaining partial outputs
+    const float wk = __shfl_sync(kFull, wl, q);
+    float v[DPL];
+    load_o(q, v);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
+  }
+  for (int q0 = 32; q0 < n; q0 += 32) {  // more than 32 partials: weights 32 at a time
     float w = 0.f;
-    if (q0 == 0) {
-      w = mq == -INFINITY ? 0.f : lq * fast_exp2(mq - M);
-    } else if (q0 + lane < n) {
+    if (q0 + lane < n) {
       const int q = q0 + lane;
       const float m = q < np1 ? m1[at(q)] : m2[at(q)];
       w = m == -INFINITY ? 0.f : (q < np1 ? l1[at(q)] : l2[at(q)]) * fast_exp2(m - M);
@@ -374,12 +421,13 @@ __global__ void __launch_bounds__(32 * kReduceRows)
     W += warp_sum(w);
     const int cnt = n - q0 < 32 ? n - q0 : 32;
 #pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {  // independent loads of the partial outputs
+    for (int k = 0; k < cnt; ++k) {
       const int q = q0 + k;
       const float wk = __shfl_sync(kFull, w, k);
-      const float* o = (q < np1 ? o1 : o2) + at(q) * D + lane * DPL;
+      float v[DPL];
+      load_o(q, v);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, o[e], acc[e]);
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
     }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
