@@ -15,10 +15,11 @@
 //                                                      16-bit, over S_j's columns
 //   O  += P_j . V_j      M 128, N = head_dim, K 64    A from tensor memory
 //
-// Roles (7 warps): warp 0 copies K tiles into a three-slot ring and warp 2 V
-// tiles into a two-slot ring, one copy per pool block (a copy takes about 100
-// cycles to issue, so one warp for both fell behind); one thread of warp 1
-// issues every MMA; warps 3..6 each own 32 rows (their tensor-memory lane
+// Roles (7 or 8 warps): warp 0 copies K tiles into a three-slot ring and warp
+// 2 V tiles into a two-slot ring, one copy per pool block (a copy takes about
+// 100 cycles to issue, so one warp for both fell behind); one thread of warp 1
+// issues the MMAs (over a 16-bit pool the S MMAs only, and one thread of warp
+// 7 the PV MMAs); warps 3..6 each own 32 rows (their tensor-memory lane
 // quarter) for the softmax, write P_j back into tensor memory where S_j was,
 // and finally normalise and store O. A
 // K slot is refilled as soon as its S MMA has completed, a V slot (and the S/P
@@ -60,7 +61,7 @@ namespace pkv {
 #define PKV_MQ_TC_COPY_WARPS 2  // 1: one warp copies K and V; 2: one warp each (build-time knob)
 #endif
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool F8 = false>
 struct MqTcShape {
   static constexpr int ROWS = 128;                // query rows per CTA (M)
   static constexpr int NT = 64;                   // tokens per K/V tile
@@ -79,7 +80,7 @@ struct MqTcShape {
   // k_full[3], k_empty[3], v_full[2], pv_done[2] (PV_j done: V slot and S/P buffer j % 2 free),
   // s_full[2], p_full[2] (per S/P buffer: no row can reach tile j + 2 before PV_j), fin, q_full,
   // and for an FP8 pool k_raw[3], v_raw[2] (the codes have landed; k_full / v_full then mean widened)
-  static constexpr int NBARS = 21;
+  static constexpr int NBARS = 22;  // (+ fin_pv, the PV warp's completion barrier, last)
   static constexpr int HALF = TILE / 2;           // FP8 pool: the codes of a tile land in its slot's upper half
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;  // tensor-memory base, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 8;
@@ -94,7 +95,13 @@ struct MqTcShape {
   static constexpr int IDS = (kMaxPartitionBlocks + 31) / 32;
   static constexpr int CW = PKV_MQ_TC_COPY_WARPS;  // copy warps: warp 0 (and warp 2 for V)
   static constexpr int SW = CW + 1;                // first of the four row warps
-  static constexpr int THREADS = (SW + 4) * 32;
+  // 16-bit pool: a warp of its own issues the PV MMAs (measured: workload 2 with 128- and 64-token
+  // chunks 0.2861 / 0.2579 ms against 0.2893 / 0.2687 with one issuing thread, workload 3 with
+  // 32-token chunks 0.2589 against 0.2656). Over an FP8 pool it measured mixed (workload 3 0.3543
+  // against 0.3460), so one thread issues both there.
+  static constexpr bool SPLIT = !F8 && CW == 2;
+  static constexpr int PVW = SW + 4;               // the PV warp (when SPLIT)
+  static constexpr int THREADS = (SW + 4 + (SPLIT ? 1 : 0)) * 32;
   static_assert(BS * 128 % 1024 == 0, "a block's rows must fill whole 1024-byte swizzle atoms");
   static_assert(NT % BS == 0 && NBT <= 32, "tile of whole blocks");
   static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -258,7 +265,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     pkv_mq_tc_kernel(const DecodeParams p, const MqParams mq, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   pdl_begin();
-  using Sh = MqTcShape<T, D, BS>;
+  using Sh = MqTcShape<T, D, BS, F8>;
   // FP8 pool: both MMAs multiply f16 (the codes widen exactly; a bf16 query is scaled into f16)
   using TP = typename std::conditional<F8, __half, T>::type;  // the type of P (and, with F8, of Q, K and V)
   static_assert(!F8 || (D == 128 && Sh::CW == 2), "an FP8 pool: head_dim 128, one copy warp each for K and V");
@@ -275,6 +282,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   uint64_t* q_full = k_full + 15;
   uint64_t* k_raw = k_full + 16;  // FP8 pool only
   uint64_t* v_raw = k_full + 19;
+  uint64_t* fin_pv = k_full + 21;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned char* Qs = smem;
@@ -298,7 +306,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
   // as the table row goes; masked below), so that the first copy waits for one memory round trip
   // rather than two. Later partitions are often past the context and load them once it is known.
   // (Requesting the query rows early as well measured slower.)
-  const bool srole = warp >= Sh::SW;
+  const bool srole = warp >= Sh::SW && warp < Sh::SW + 4;
   const int row = 32 * (warp & 3) + lane;
   const bool early = part == 0;
   int raw[Sh::IDS];
@@ -354,6 +362,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
     mbar_init(p_full, 128);
     mbar_init(p_full + 1, 128);
     mbar_init(fin, 1);
+    mbar_init(fin_pv, 1);
     mbar_init(q_full, 128);
     fence_mbar_init();
     *abort = 0;
@@ -522,6 +531,56 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
       for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) mbar_wait(v_full + (j & 1), (j >> 1) & 1);
     }
     }
+  } else if (Sh::SPLIT && (warp == 1 || warp == Sh::PVW)) {
+    // ---- MMA issue, 16-bit pool: one thread of warp 1 the S MMAs, one of the PV warp the PV MMAs, each
+    // in tile order with blocking waits (a tcgen05.mma holds its issuing thread while the tensor core
+    // takes it in, so with one thread S and PV queued behind each other)
+    if (lane == 0) {
+      constexpr bool BF = std::is_same<TP, __nv_bfloat16>::value;
+      constexpr uint32_t IDESC_S = tc::idesc_f16(BF, Sh::ROWS, NT, false, false);
+      constexpr uint32_t IDESC_O = tc::idesc_f16(BF, Sh::ROWS, D, false, true);
+      if (warp == 1) {
+        // S_j once K_j has landed and PV_{j-2}, the last reader of its S/P buffer, is done
+        const uint32_t q_addr = smem_u32(Qs);
+        bool ok = tc_wait(q_full, 0, abort);  // the rows have written Q
+        for (int j = 0; ok && j < ntile; ++j) {
+          ok = tc_wait(k_full + j % KST, (j / KST) & 1, abort) &&
+               (j < 2 || tc_wait(pv_done + (j & 1), ((j >> 1) - 1) & 1, abort));
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t k_addr = smem_u32(k_slot(j));
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a = tc::desc_sw128(q_addr + (k / 4) * (Sh::ROWS * 128) + (k % 4) * 32, 16, 1024);
+            const uint64_t b = tc::desc_sw128(k_addr + (k / 4) * 1024 + (k % 4) * 32, 16, Sh::ATOM);
+            tc::mma_f16(tbase + Sh::S_COL + (j & 1) * NT, a, b, IDESC_S, k > 0);
+          }
+          tc::commit(s_full + (j & 1));
+          tc::commit(k_empty + j % KST);
+        }
+        tc::commit(fin);  // every S MMA issued above has completed once this arrives
+        mbar_wait(fin, 0);
+      } else {
+        // O += P_j . V_j once P_j is written and V_j has landed; then V slot j % 2 and S/P buffer j % 2
+        // are free
+        for (int j = 0; j < ntile; ++j) {
+          const bool ok = tc_wait(p_full + (j & 1), (j >> 1) & 1, abort) &&
+                          tc_wait(v_full + (j & 1), (j >> 1) & 1, abort);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t v_addr = smem_u32(v_slot(j));
+#pragma unroll
+          for (int k = 0; k < NT / 16; ++k) {
+            const uint64_t b = tc::desc_sw128(v_addr + k * 2 * Sh::ATOM, 1024, Sh::ATOM);
+            tc::mma_f16_ta(tbase, tbase + Sh::S_COL + (j & 1) * NT + k * 8, b, IDESC_O, j > 0 || k > 0);
+          }
+          tc::commit(pv_done + (j & 1));
+        }
+        tc::commit(fin_pv);  // every PV MMA issued above has completed once this arrives
+        mbar_wait(fin_pv, 0);
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issue (one thread)
     if (lane == 0) {
@@ -780,7 +839,7 @@ __global__ void __maxnreg__(PKV_MQ_TC_COPY_WARPS == 2 ? 128 : 168)
 template <typename T, int D, int BS, bool F8 = false>
 cudaError_t launch_mq_tc(const DecodeParams& p, const MqParams& mq, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, int num_seqs, cudaStream_t stream) {
-  using Sh = MqTcShape<T, D, BS>;
+  using Sh = MqTcShape<T, D, BS, F8>;
   auto kern = pkv_mq_tc_kernel<T, D, BS, F8>;
   static bool configured[64] = {};
   int dev = 0;
