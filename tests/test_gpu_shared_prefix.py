@@ -60,6 +60,7 @@ CASES = [
     (64, 8, 128, 16, BF16, 40, 2048, (1, 64)),     # GQA 8, 320 rows (3 row tiles), long prefix in partitions
     (12, 4, 64, 16, F16, 30, 0, (1, 700)),         # no prefix at all: the tails are the whole contexts
     (24, 8, 128, 16, BF16, 8, 512, (1, 300)),      # GQA 3, 24 rows (above 16): tensor tile, group not a power of 2
+    (8, 1, 128, 16, F16, 2, 4096, (1, 100)),       # one kv head: 64 prefix partitions, more than 32 partials a row
 ]
 
 
