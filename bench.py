@@ -131,11 +131,12 @@ class Dist:
 # byte accounting
 
 
-def default_partition(fp8: bool, mq: bool = False, block_size: int = 16) -> int:
-    """The library's partition size when the call passes 0 (longer for multi-query)."""
+def default_partition(fp8: bool, mq: bool = False, block_size: int = 16, max_context_len: int = 0) -> int:
+    """The library's partition size when the call passes 0 (longer for multi-query and for contexts that may
+    exceed 8192 tokens; at most 128 blocks)."""
     if mq:
         return min(2048, 128 * block_size)
-    return 1024
+    return min(2048 if max_context_len > 8192 else 1024, 128 * block_size)
 
 
 SHARED_PREFIX_TOKENS = 1024  # workload 4's common prefix
@@ -161,7 +162,8 @@ def step_bytes(batch, partition_size: int, cache_bytes: int = 2):
 
     from paged_kv_cache_91_gb300 import workloads as W
 
-    P = partition_size or default_partition(cache_bytes == 1, batch.query_start_loc is not None, batch.block_size)
+    P = partition_size or default_partition(cache_bytes == 1, batch.query_start_loc is not None, batch.block_size,
+                                            batch.max_context_len)
     ctx = batch.context_lens.astype(np.int64)
     kv = W.algorithmic_kv_bytes(batch) * cache_bytes // batch.elem_bytes
     S, H, D, B = batch.num_seqs, batch.num_heads, batch.head_dim, batch.block_size
@@ -419,7 +421,7 @@ def workload_config(batch, n, partition_size, pool_bytes, fp8=False):
         "context_lens": {"min": int(batch.context_lens.min()), "mean": float(batch.context_lens.mean()),
                          "max": int(batch.context_lens.max())},
         "partition_size": partition_size or default_partition(fp8, batch.query_start_loc is not None,
-                                                              batch.block_size),
+                                                              batch.block_size, batch.max_context_len),
         "new_tokens_per_step": int((batch.slot_mapping >= 0).sum()),
         "pool_bytes": pool_bytes,
         "l2": "inputs larger than L2 (KV pool > 129 MB); no flush between steps",
@@ -517,7 +519,7 @@ class Case:
                              self.mcl, partition_size)
         self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream(dev)
-        self.nparts = -(-self.mcl // (partition_size or default_partition(fp8, self.mq, batch.block_size)))
+        self.nparts = -(-self.mcl // (partition_size or default_partition(fp8, self.mq, batch.block_size, self.mcl)))
         self.launches_per_step = 2 + (1 if self.nparts > 1 else 0)
         self.cache_bytes = 1 if fp8 else 2
         self.kv_bytes, self.call_bytes = step_bytes(batch, partition_size, self.cache_bytes)

@@ -129,7 +129,8 @@ pkv_status_t paged_kv_copy_blocks(void* key_cache, void* value_cache, const int6
  * (head_dim + 2) fp32 per sequence. The size is 0 when max_context_len <=
  * partition_size (no split).
  *
- * partition_size 0 selects the default, 1024. Returns 0 for invalid arguments,
+ * partition_size 0 selects the default: 1024, or 2048 when max_context_len >
+ * 8192 (at most 128 blocks either way). Returns 0 for invalid arguments,
  * which paged_attention_decode then rejects.
  */
 size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
@@ -164,7 +165,8 @@ size_t paged_attention_workspace_size(int32_t num_seqs, int32_t num_heads, int32
  *   scale                usually 1 / sqrt(head_dim)
  *   head_dim             64 or 128; block_size 8, 16 or 32
  *   num_heads            a multiple of num_kv_heads (GQA when larger)
- *   partition_size       0 = 1024; else a multiple of block_size in
+ *   partition_size       0 = the default (see paged_attention_workspace_size);
+ *                        else a multiple of block_size in
  *                        [block_size, 128 * block_size]: the tokens of one
  *                        CTA's share of a context (contexts longer than this
  *                        are split and merged by log-sum-exp)
@@ -187,7 +189,7 @@ pkv_status_t paged_attention_decode(void* out, const void* query, const void* ke
 /* Size of the library-owned split-K scratch of
  * paged_attention_decode_static_workspace: 32 MiB per device. It covers, for
  * example, 16 sequences x 40 heads x 32768-token contexts at partition_size 512
- * (16 MiB at the default 1024). */
+ * (about 5 MiB at the default, 2048 for such contexts). */
 #define PKV_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 
 /*
@@ -509,7 +511,7 @@ pkv_status_t paged_kv_write_fp8(const void* key, const void* value, void* key_ca
 /*
  * paged_attention_workspace_size_fp8 -- workspace bytes of
  * paged_attention_decode_fp8: the size paged_attention_workspace_size gives
- * (partition_size 0 selects 1024 for both).
+ * (partition_size 0 selects the same default for both).
  */
 size_t paged_attention_workspace_size_fp8(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                           int32_t head_dim, int32_t block_size,

@@ -18,11 +18,20 @@
 namespace pkv {
 namespace {
 
-// Decode partition: 1024 tokens over both cache types. Measured, decode call ms at 512 / 1024 / 2048 tokens
-// (16-bit cache): workload 2 0.1995 / 0.1980 / 0.1988, workload 3 0.1747 / 0.1715 / 0.1718, workload 4
-// 0.0662 / 0.0627 / 0.0619, workload 5 1.485 / 1.464 / 1.454; FP8 cache: workload 2 0.115 / 0.114 / 0.117,
-// workload 3 0.114 / 0.104 / 0.107. A CTA's start and end cost more than the longer per-CTA tail.
+// Decode partition when the call passes 0: 1024 tokens over both cache types, 2048 for batches whose
+// contexts may exceed 8192 tokens (at most 128 blocks either way). Measured, decode call ms at 512 / 1024 /
+// 2048 tokens (16-bit cache): workload 2 0.1995 / 0.1980 / 0.1988, workload 3 (contexts up to 8192) 0.1747
+// / 0.1715 / 0.1718, workload 4 0.0662 / 0.0627 / 0.0619, workload 5 (32768) 1.485 / 1.464 / 1.454; FP8
+// cache: workload 2 0.115 / 0.114 / 0.117, workload 3 0.114 / 0.104 / 0.107, workload 5 - / 0.771 / 0.760.
+// A CTA's start and end cost more than the longer per-CTA tail.
 constexpr int kDefaultPartition = 1024;
+constexpr int kDefaultPartitionLong = 2048;
+constexpr int kLongContext = 8192;
+int default_partition(int max_context_len, int block_size) {
+  const int P = max_context_len > kLongContext ? kDefaultPartitionLong : kDefaultPartition;
+  const int cap = kMaxPartitionBlocks * block_size;
+  return P < cap ? P : cap;
+}
 #ifndef PKV_MQ_WIDE_MIN_ROWS
 // Multi-query rows per kv head from which the tensor-memory tile runs (build-time knob). Measured: at 16
 // rows (two 8-column CTAs per kv head) the 8-column tile is 3-10% faster; from 20 rows on the tensor tile
@@ -651,11 +660,10 @@ struct Plan {
 // 2 <= G <= 8. Contexts longer than P leave one partial per partition.
 Plan make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_context_len,
                int partition_size, bool fp8) {
-  (void)block_size;
   Plan pl{};
   const int G = num_heads / num_kv_heads;
   pl.mma = fp8 ? (G <= 8 && head_dim == 128) : (G >= 2 && G <= 8);
-  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int P = partition_size ? partition_size : default_partition(max_context_len, block_size);
   pl.np = max_partitions_for(max_context_len, P);
   pl.need = pl.np > 1 ? (size_t)num_seqs * num_heads * pl.np * (head_dim + 2) * sizeof(float) : 0;
   return pl;
@@ -721,7 +729,7 @@ pkv_status_t decode_impl(void* out, const void* query, const void* key_cache, co
     return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * block_size = %lld",
                 max_context_len, (long long)max_blocks_per_seq * block_size);
   if (partition_size < 0) return fail(PKV_ERR_INVALID_ARG, "partition_size < 0");
-  const int P = partition_size ? partition_size : kDefaultPartition;
+  const int P = partition_size ? partition_size : default_partition(max_context_len, block_size);
   if (P % block_size || P < block_size || P > kMaxPartitionBlocks * block_size)
     return fail(PKV_ERR_UNSUPPORTED, "partition_size %d must be a multiple of block_size in [%d, %d]", P,
                 block_size, kMaxPartitionBlocks * block_size);

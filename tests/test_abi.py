@@ -61,7 +61,9 @@ def test_workspace_size(lib):
     ws = lib.paged_attention_workspace_size
     assert ws(64, 40, 40, 128, 16, 512, 512) == 0  # one partition: no workspace
     assert ws(64, 40, 40, 128, 16, 513, 512) == 64 * 40 * 2 * 130 * 4
-    assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 32 * 130 * 4  # 0 selects 1024
+    assert ws(16, 40, 40, 128, 16, 32768, 0) == 16 * 40 * 16 * 130 * 4  # 0 selects 2048 above 8192 tokens
+    assert ws(16, 40, 40, 128, 8, 32768, 0) == 16 * 40 * 32 * 130 * 4  # at most 128 blocks: 1024 for blocks of 8
+    assert ws(16, 40, 40, 128, 16, 8192, 0) == 16 * 40 * 8 * 130 * 4  # 8192 and below: 1024
     assert ws(256, 32, 8, 128, 16, 8192, 0) == 256 * 32 * 8 * 130 * 4
     assert ws(3000, 8, 8, 64, 16, 4096, 0) == 3000 * 8 * 4 * 66 * 4
     assert ws(64, 40, 40, 128, 16, 1024, 0) == 0 and ws(64, 40, 40, 128, 16, 1025, 0) == 64 * 40 * 2 * 130 * 4

@@ -132,11 +132,13 @@ def test_split_k_partitions(H, Hkv, dtype):
 
 @pytest.mark.parametrize("H,Hkv,D,B,dtype", [(8, 8, 128, 16, F16), (16, 4, 128, 16, BF16), (8, 8, 64, 8, BF16),
                                                (16, 2, 64, 32, F16)])
-def test_default_partition_boundary(H, Hkv, D, B, dtype):
-    """partition_size 0 (1024 tokens): contexts just below, at and above one and two partitions, and the
-    1024-token maximum of 128 blocks of 8; the direct and the split path side by side."""
-    ctx = [1023, 1024, 1025, 2047, 2048, 2049, 3073]
-    batch = W.build_batch(seed=23 + H + D, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+@pytest.mark.parametrize("ctx", [[1023, 1024, 1025, 2047, 2048, 2049, 3073],
+                                 [2047, 2048, 2049, 4097, 9000]])
+def test_default_partition_boundary(H, Hkv, D, B, dtype, ctx):
+    """partition_size 0: 1024 tokens, or 2048 when the longest context passes 8192 (second set; 1024 for blocks
+    of 8, whose partitions hold 128 blocks at most). Contexts just below, at and above one and two
+    partitions: the direct and the split path side by side."""
+    batch = W.build_batch(seed=23 + H + D + len(ctx), context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
                           block_size=B, dtype=dtype, pool_factor=1.2)
     t = W.as_torch(batch, DEV)
     out = run_step(batch, t, write=False)
@@ -146,7 +148,7 @@ def test_default_partition_boundary(H, Hkv, D, B, dtype):
 
 
 def test_long_context_with_outliers_split():
-    """1% of keys scaled by 8 (wide score range), 32 partitions of 1024 merged by log-sum-exp."""
+    """1% of keys scaled by 8 (wide score range), 16 partitions of 2048 merged by log-sum-exp."""
     batch = W.build_batch(seed=22, context_lens=[32768, 20000, 513], num_heads=8, num_kv_heads=8,
                           head_dim=128, block_size=16, dtype=F16, key_outlier_frac=0.01)
     t = W.as_torch(batch, DEV)
