@@ -586,26 +586,11 @@ class Case:
         return (t["query"], t["new_key"], t["new_value"], t["slot_mapping"], t["block_tables"], t["context_lens"],
                 self.out, t.get("query_start_loc"))
 
-    def time_plain(self, K: int):
-        """ms per step of K steps with events around the region only (no per-call events, whose host time
-        shows in a launch-bound step)."""
-        import torch
-
-        self.apply_settings()
-        t, st = self.t, self.stream
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(st)
-        for _ in range(K):
-            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
-            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
-        b.record(st)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / K
-
     def time_device(self, K: int, warmup: int, dist):
-        """K steps with every input resident in HBM: events around the whole region, around each attention
-        call and before each write, all on the launching stream."""
+        """K steps with every input resident in HBM, timed twice on the launching stream: first with events
+        around the whole region only (the step time: value and ms_per_step), then with events around each
+        attention call and before each write as well (the call's own time, for the roofline; events between
+        the launches cost the step a little)."""
         import torch
 
         self.apply_settings()
@@ -614,34 +599,39 @@ class Case:
             self.step(*self.device_args())
         torch.cuda.synchronize()
         self.binding.device_errors(clear=True)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         dist.barrier()
         t_wall0 = time.time()
         start.record(st)
+        for _ in range(K):
+            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
+            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
+        end.record(st)
+        torch.cuda.synchronize()
+        dist.barrier()
+        total_ms = dist.max(start.elapsed_time(end))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
         for k in range(K):
             ev_w[k].record(st)
             self.write(t["new_key"], t["new_value"], t["slot_mapping"])
             ev[k][0].record(st)
             self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
             ev[k][1].record(st)
-        end.record(st)
         torch.cuda.synchronize()
-        dist.barrier()
         t_wall1 = time.time()
-        total_ms = dist.max(start.elapsed_time(end))
         return dict(total_ms=total_ms, call_ms=statistics.fmean(a.elapsed_time(b) for a, b in ev),
                     write_ms=statistics.fmean(w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)),
                     t0=t_wall0, t1=t_wall1, errors=self.binding.device_errors(clear=True))
 
     def time_e2e(self, K: int, warmup: int, dist):
         """The same step through the public API with the step's inputs copied from pinned host memory and
-        the output read back, every step. The pool stays resident: it is the cache. The copies run on a
-        second stream into two alternating sets of device buffers, so that step k + 1's inputs upload (and
-        step k - 1's output downloads) while step k computes; events order every copy against the steps
-        that use its buffers."""
+        the output read back, every step. The pool stays resident: it is the cache. The uploads and the
+        downloads run on two more streams, into and out of two alternating sets of device buffers, so that
+        step k + 1's inputs upload (and step k - 1's output downloads) while step k computes; events order
+        every copy against the steps that use its buffers. (With one stream for both, step k + 1's uploads
+        queued behind step k's download, which waits for step k.)"""
         import torch
 
         self.apply_settings()
@@ -654,7 +644,8 @@ class Case:
         out_h = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = out_h[0].numel() * out_h[0].element_size()
-        cs = torch.cuda.Stream(self.dev)
+        cs = torch.cuda.Stream(self.dev)  # uploads
+        ds = torch.cuda.Stream(self.dev)  # downloads
         ev = lambda: torch.cuda.Event()  # noqa: E731
         uploaded = [ev(), ev()]   # inputs of the set are on the device
         consumed = [ev(), ev()]   # the step that read the set (and wrote its output) has run
@@ -676,11 +667,11 @@ class Case:
                 self.step(b["query"], b["new_key"], b["new_value"], b["slot_mapping"], b["block_tables"],
                           b["context_lens"], outs[i], b.get("query_start_loc"))
                 consumed[i].record(st)
-                with torch.cuda.stream(cs):
-                    cs.wait_event(consumed[i])
+                with torch.cuda.stream(ds):
+                    ds.wait_event(consumed[i])
                     out_h[i].copy_(outs[i], non_blocking=True)
-                    downloaded[i].record(cs)
-            st.wait_stream(cs)  # the last output is on the host before the region ends
+                    downloaded[i].record(ds)
+            st.wait_stream(ds)  # the last output is on the host before the region ends
 
         run(warmup)
         torch.cuda.synchronize()
@@ -688,93 +679,8 @@ class Case:
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(st)
         cs.wait_event(s0)  # no copy of the timed steps starts before the region
+        ds.wait_event(s0)
         run(K)
-        s1.record(st)
-        torch.cuda.synchronize()
-        dist.barrier()
-        e2e_ms = dist.max(s0.elapsed_time(s1))
-        return dict(ms=e2e_ms / K, h2d=int(h2d), d2h=int(d2h))
-
-    def time_plain(self, K: int):
-        """ms per step of K steps with events around the region only (no per-call events, whose host time
-        shows in a launch-bound step)."""
-        import torch
-
-        self.apply_settings()
-        t, st = self.t, self.stream
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(st)
-        for _ in range(K):
-            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
-            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
-        b.record(st)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / K
-
-    def time_device(self, K: int, warmup: int, dist):
-        """K steps with every input resident in HBM: events around the whole region, around each attention
-        call and before each write, all on the launching stream."""
-        import torch
-
-        self.apply_settings()
-        t, st = self.t, self.stream
-        for _ in range(warmup):
-            self.step(*self.device_args())
-        torch.cuda.synchronize()
-        self.binding.device_errors(clear=True)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        ev_w = [torch.cuda.Event(enable_timing=True) for _ in range(K)]  # before each step's write
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        dist.barrier()
-        t_wall0 = time.time()
-        start.record(st)
-        for k in range(K):
-            ev_w[k].record(st)
-            self.write(t["new_key"], t["new_value"], t["slot_mapping"])
-            ev[k][0].record(st)
-            self.decode(t["query"], t["block_tables"], t["context_lens"], self.out, t.get("query_start_loc"))
-            ev[k][1].record(st)
-        end.record(st)
-        torch.cuda.synchronize()
-        dist.barrier()
-        t_wall1 = time.time()
-        total_ms = dist.max(start.elapsed_time(end))
-        return dict(total_ms=total_ms, call_ms=statistics.fmean(a.elapsed_time(b) for a, b in ev),
-                    write_ms=statistics.fmean(w.elapsed_time(a) for w, (a, _) in zip(ev_w, ev)),
-                    t0=t_wall0, t1=t_wall1, errors=self.binding.device_errors(clear=True))
-
-    def time_e2e(self, K: int, warmup: int, dist):
-        """The same step through the public API with the step's inputs copied from pinned host memory and
-        the output read back, every step. The pool stays resident: it is the cache."""
-        import torch
-
-        self.apply_settings()
-        t, st = self.t, self.stream
-        host = {k: t[k].cpu().pin_memory() for k in ("query", "new_key", "new_value", "slot_mapping",
-                                                      "block_tables", "context_lens")
-                + (("query_start_loc",) if self.mq else ())}
-        dbuf = {k: torch.empty_like(t[k]) for k in host}
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = out_h.numel() * out_h.element_size()
-
-        def e2e_step():
-            for k, v in host.items():
-                dbuf[k].copy_(v, non_blocking=True)
-            self.step(dbuf["query"], dbuf["new_key"], dbuf["new_value"], dbuf["slot_mapping"], dbuf["block_tables"],
-                      dbuf["context_lens"], self.out, dbuf.get("query_start_loc"))
-            out_h.copy_(self.out, non_blocking=True)
-
-        for _ in range(warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        dist.barrier()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(st)
-        for _ in range(K):
-            e2e_step()
         s1.record(st)
         torch.cuda.synchronize()
         dist.barrier()
@@ -1027,8 +933,7 @@ def run_suite(args, dist, dev, base_batch):
         e2e_t = None if args.no_e2e else case.time_e2e(K, args.warmup, dist)
         cpu = cpu_oracle(batch, args.suite_cpu_seconds, _all_cores(), case.fp8) if cpu_on else None
         results[key] = entry_summary(case, dev_t, e2e_t, None, cpu, K)
-        if batch.num_seqs <= 4:  # launch-bound: the step without per-call events, and from a CUDA graph
-            results[key]["us_per_step_no_call_events"] = round(1e3 * case.time_plain(K), 2)
+        if batch.num_seqs <= 4:  # launch-bound: the step also from a CUDA graph
             results[key]["graph_us_per_step"] = round(case.time_graph(100), 2)
         results[key]["_window"] = (dev_t["t0"], dev_t["t1"])
         case.close()
