@@ -351,24 +351,6 @@ def time_oracle(batch, seqs, budget_s: float, min_reps: int = 1, fp8_pools=None)
             return el, reps
 
 
-def time_oracle_mq(batch, budget_s: float, fp8_pools=None):
-    """Run the multi-query oracle over the whole batch until budget_s; returns (seconds, reps).
-    fp8_pools: (key codes, value codes) of an FP8 cache with k_scale = v_scale = FP8_SCALE."""
-    import oracle
-
-    kc, vc = fp8_pools if fp8_pools is not None else (batch.key_cache, batch.value_cache)
-    sc = FP8_SCALE if fp8_pools is not None else 1.0
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.multi_query_c(batch.query, kc, vc, batch.block_tables, batch.context_lens, batch.query_start_loc,
-                             batch.scale, batch.dtype, k_scale=sc, v_scale=sc)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            return el, reps
-
-
 def sample_kv_bytes(batch, seqs, cache_bytes: int = 2):
     ctx = batch.context_lens[list(seqs)].astype("int64").sum()
     return int(ctx) * batch.num_kv_heads * batch.head_dim * 2 * cache_bytes
